@@ -1,0 +1,60 @@
+"""The five synthetic workloads: shapes, storage types and value distributions.
+
+Each tensor is drawn from its own generator stream under seed 0: x from
+stream 0, w from stream 1, dy from stream 2.  ``N(m, s)`` means mean m and
+standard deviation s.  Nothing here computes any part of the method.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+from . import NORMAL, UNIFORM
+
+SEED = 0
+STREAM_X, STREAM_W, STREAM_DY = 0, 1, 2
+
+
+@dataclass(frozen=True)
+class Dist:
+    kind: int      # NORMAL or UNIFORM
+    a: float       # mean (normal) or low end (uniform)
+    b: float       # standard deviation (normal) or high end (uniform)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    op: str                  # "ws" (weighted sum) or "silu" (scaled SiLU)
+    dtype: str               # storage type of x, dy, y, dx: "f32" | "f16" | "bf16"
+    N: int                   # rows (ws) or leading extent (silu)
+    D: int                   # features (ws) or trailing extent (silu)
+    x: Dist
+    dy: Dist
+    w: Dist | None = None    # ws: w[D] in binary32
+    w_scalar: float | None = None  # silu: the scalar w in binary32
+    block_n: int = 0         # rows per partial tile (0: the library chooses)
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def n(self) -> int:
+        return self.N * self.D
+
+
+WORKLOADS = {
+    "c1": Workload("c1", "ws", "f32", 100, 64, x=Dist(NORMAL, 0.0, 1.0), w=Dist(NORMAL, 0.0, 1.0),
+                   dy=Dist(NORMAL, 0.0, 1.0), block_n=32,
+                   note="weighted sum, fp32 x[100,64]; 32-row tiles give a [4,64] partial buffer"),
+    "c2": Workload("c2", "silu", "f16", 8192, 4096, x=Dist(NORMAL, 0.0, 2.0), w_scalar=0.75,
+                   dy=Dist(NORMAL, 0.0, 1.0),
+                   note="scaled SiLU, fp16 x[8192,4096] ~N(0,2), w=0.75, scalar dw over 33.5M elements"),
+    "c3": Workload("c3", "ws", "bf16", 1 << 20, 1024, x=Dist(NORMAL, 0.0, 1.0),
+                   w=Dist(NORMAL, 0.0, 1.0 / 32.0), dy=Dist(NORMAL, 0.0, 1.0),
+                   note="weighted sum, bf16 x[1048576,1024], w ~N(0,1/sqrt(1024))"),
+    "c4": Workload("c4", "ws", "f16", 1 << 24, 64, x=Dist(UNIFORM, -1.0, 1.0),
+                   w=Dist(NORMAL, 0.0, 1.0), dy=Dist(NORMAL, 0.0, 1.0),
+                   note="tall-skinny weighted sum, fp16 x[16777216,64] ~U(-1,1)"),
+    "c5": Workload("c5", "ws", "f32", 4096, 65536, x=Dist(NORMAL, 0.0, 1.0),
+                   w=Dist(NORMAL, 0.0, 1.0 / 256.0), dy=Dist(NORMAL, 0.0, 1.0),
+                   note="wide weighted sum, fp32 x[4096,65536], w ~N(0,1/256)"),
+}

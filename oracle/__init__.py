@@ -1,0 +1,176 @@
+"""fp64 CPU oracle — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg (``bench.py`` cpu_baseline / ``--impl reference``) may import this
+package.  The product library never loads it and shares no code with it.
+
+The C source (``oracle.c``) states each definition and the page section it
+follows.  This wrapper marshals host torch tensors (contiguous, CPU) into the
+C entry points and returns fp64 results as numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source (gcc, -O2, no fast-math, no
+    contraction of a·b + c into fused multiply-adds)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", _SRC,
+               "-o", _LIB + ".tmp", "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+_lib = None
+_vp, _i64, _int, _dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
+        L.orc_f16_to_f64.restype = _dbl
+        L.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.orc_bf16_to_f64.restype = _dbl
+        L.orc_f64_to_f16.argtypes = [_dbl]
+        L.orc_f64_to_f16.restype = ctypes.c_uint16
+        L.orc_f64_to_bf16.argtypes = [_dbl]
+        L.orc_f64_to_bf16.restype = ctypes.c_uint16
+        L.orc_pairwise_sum.argtypes = [_vp, _i64]
+        L.orc_pairwise_sum.restype = _dbl
+        L.orc_ws_fwd.argtypes = [_vp, _i64, _vp, _i64, _i64, _int, _vp, _vp, _vp]
+        L.orc_ws_fwd.restype = _int
+        L.orc_ws_bwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _i64, _vp]
+        L.orc_ws_bwd.restype = _int
+        L.orc_silu_fwd.argtypes = [_vp, _dbl, _i64, _int, _vp, _vp]
+        L.orc_silu_fwd.restype = _int
+        L.orc_silu_bwd.argtypes = [_vp, _vp, _dbl, _i64, _int, _vp, _vp, _vp, _vp, _vp]
+        L.orc_silu_bwd.restype = _int
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        assert t.flags["C_CONTIGUOUS"]
+        return ctypes.c_void_p(t.ctypes.data)
+    assert t.device.type == "cpu"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with {rc}")
+
+
+def _dt_of(t) -> str:
+    import torch
+    return {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[t.dtype]
+
+
+# ---------------------------------------------------------------- conversions
+def f16_to_f64(bits: int) -> float:
+    return lib().orc_f16_to_f64(bits)
+
+
+def bf16_to_f64(bits: int) -> float:
+    return lib().orc_bf16_to_f64(bits)
+
+
+def f64_to_f16(v: float) -> int:
+    return lib().orc_f64_to_f16(float(v))
+
+
+def f64_to_bf16(v: float) -> int:
+    return lib().orc_f64_to_bf16(float(v))
+
+
+def pairwise_sum(t: np.ndarray) -> float:
+    t = np.ascontiguousarray(t, dtype=np.float64)
+    return lib().orc_pairwise_sum(_ptr(t), t.size)
+
+
+# ---------------------------------------------------------------- weighted sum
+def ws_fwd(x, w):
+    """x: host tensor [N, D] (unit inner stride, any row stride), w: [D] fp32.
+    Returns (y_exact fp64 [N], y_abs fp64 [N], y_out tensor [N] in x's dtype)."""
+    import torch
+    assert x.dim() == 2 and x.stride(1) == 1 and w.dtype == torch.float32 and w.is_contiguous()
+    N, D = x.shape
+    y_exact = np.empty(N, np.float64)
+    y_abs = np.empty(N, np.float64)
+    y_out = torch.empty(N, dtype=x.dtype)
+    _check(lib().orc_ws_fwd(_ptr(x), x.stride(0) if N > 0 else D, _ptr(w), N, D,
+                            DTYPE_CODE[_dt_of(x)], _ptr(y_exact), _ptr(y_abs), _ptr(y_out)),
+           "ws_fwd")
+    return y_exact, y_abs, y_out
+
+
+def ws_bwd(x, w, dy, *, want_dx=True, block_n=0):
+    """Returns dict with dx (tensor [N,D] contiguous, x's dtype) when want_dx,
+    grad_w and grad_w_abs (fp64 [D]), and partial (fp64 [ceil(N/block_n), D])
+    when block_n > 0."""
+    import torch
+    assert x.dim() == 2 and x.stride(1) == 1 and dy.dtype == x.dtype and dy.is_contiguous()
+    N, D = x.shape
+    out = {}
+    dx = torch.empty((N, D), dtype=x.dtype) if want_dx else None
+    gw = np.empty(D, np.float64)
+    gwa = np.empty(D, np.float64)
+    part = None
+    if block_n > 0:
+        part = np.empty(((N + block_n - 1) // block_n, D), np.float64)
+    _check(lib().orc_ws_bwd(_ptr(x), x.stride(0) if N > 0 else D, _ptr(w), _ptr(dy), N, D,
+                            DTYPE_CODE[_dt_of(x)], _ptr(dx), _ptr(gw), _ptr(gwa), block_n,
+                            _ptr(part)), "ws_bwd")
+    out["dx"], out["grad_w"], out["grad_w_abs"], out["partial"] = dx, gw, gwa, part
+    return out
+
+
+# ---------------------------------------------------------------- scaled SiLU
+def silu_fwd(x, w: float):
+    """x: contiguous host tensor (any shape). Returns (y_exact fp64, y_out tensor)."""
+    import torch
+    assert x.is_contiguous()
+    n = x.numel()
+    y_exact = np.empty(n, np.float64)
+    y_out = torch.empty(x.shape, dtype=x.dtype)
+    _check(lib().orc_silu_fwd(_ptr(x), float(w), n, DTYPE_CODE[_dt_of(x)], _ptr(y_exact),
+                              _ptr(y_out)), "silu_fwd")
+    return y_exact, y_out
+
+
+def silu_bwd(dy, x, w: float, *, want_dx=True, want_dw=True):
+    """Returns dict: dx_exact, dx_scale (fp64 [n]), dx (tensor, x's dtype),
+    dw, dw_abs (floats)."""
+    import torch
+    assert x.is_contiguous() and dy.is_contiguous() and dy.dtype == x.dtype
+    n = x.numel()
+    out = {}
+    dxe = np.empty(n, np.float64) if want_dx else None
+    dxs = np.empty(n, np.float64) if want_dx else None
+    dx = torch.empty(x.shape, dtype=x.dtype) if want_dx else None
+    dw = np.zeros(1, np.float64)
+    dwa = np.zeros(1, np.float64)
+    _check(lib().orc_silu_bwd(_ptr(dy), _ptr(x), float(w), n, DTYPE_CODE[_dt_of(x)], _ptr(dxe),
+                              _ptr(dxs), _ptr(dx), _ptr(dw) if want_dw else None,
+                              _ptr(dwa) if want_dw else None), "silu_bwd")
+    out.update(dx_exact=dxe, dx_scale=dxs, dx=dx, dw=float(dw[0]), dw_abs=float(dwa[0]))
+    return out

@@ -1,0 +1,325 @@
+/*
+ * oracle.c — plain, slow, fp64 CPU oracle for the forward and backward
+ * (vector-Jacobian product) of the weighted sum and of the scaled SiLU.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this file's library.  It shares no code, header,
+ * table or constant with the CUDA library; neither includes the other.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [WS]   "Writing Triton Kernels with Autograd: A Minimal End-to-End
+ *          Example", §1 Problem Setup (y = x.dot(w), x [N,D], w [D], y [N];
+ *          the PyTorch form (x * w).sum(-1)), §3 Backward: Deriving Gradients
+ *          First (grad_x = grad_out[:,None] * w[None,:],
+ *          grad_w = (x * grad_out[:,None]).sum(0); the two-stage grad_w with
+ *          one partial row per BLOCK_N-row tile, then a sum over tiles).
+ *  [SILU] "Backward in Triton — autograd.Function and the backward grid",
+ *          § A complete minimal example — fused scaled-SiLU (y = w·x·sigmoid(x)
+ *          with scalar w; s = sigmoid(x), silu = x·s;
+ *          dy/dx = w·(s + silu·(1 − s)); dx = dy·dy/dx; dw = Σ dy·silu).
+ *
+ * Arithmetic.  Every input is converted exactly to double.  Products of a
+ * binary16/bfloat16/binary32 value with a binary32 value are exact in double.
+ * Reductions use pairwise summation (N. Higham, Accuracy and Stability of
+ * Numerical Algorithms, 2nd ed., §4.2): a range of more than eight terms is
+ * split at its midpoint and the two halves' sums are added; up to eight
+ * terms are added left to right.  Elementwise results are rounded once, to
+ * nearest-even, to the output type.
+ *
+ * Storage types: 0 = binary32, 1 = binary16, 2 = bfloat16 (raw 16-bit
+ * patterns for the last two).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_F16 1
+#define ORC_BF16 2
+
+/* ------------------------------------------------------------------ */
+/* Exact decoding of the storage types.                                */
+/* ------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_f16_to_f64(uint16_t h) {
+    const int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);           /* zero or subnormal: m · 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) · 2^(e-15) */
+    return s ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 pattern. */
+double orc_bf16_to_f64(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* The two 16-bit decodings, tabulated once (65,536 entries each) so that
+ * the full-size checks are not dominated by ldexp calls. */
+static double* tab_f16 = NULL;
+static double* tab_bf16 = NULL;
+
+static void make_tables(void) {
+    if (tab_f16) return;
+    double* a = (double*)malloc(sizeof(double) * 65536);
+    double* b = (double*)malloc(sizeof(double) * 65536);
+    for (uint32_t h = 0; h < 65536; h++) {
+        a[h] = orc_f16_to_f64((uint16_t)h);
+        b[h] = orc_bf16_to_f64((uint16_t)h);
+    }
+    tab_bf16 = b;
+    tab_f16 = a;
+}
+
+static double decode(const void* p, int64_t k, int dt) {
+    if (dt == ORC_F32) return (double)((const float*)p)[k];
+    if (dt == ORC_F16) return tab_f16[((const uint16_t*)p)[k]];
+    return tab_bf16[((const uint16_t*)p)[k]];
+}
+
+/* ------------------------------------------------------------------ */
+/* Rounding to the storage types, to nearest with ties to even.        */
+/* The value is scaled by its quantum (a power of two, so exactly),    */
+/* rounded to an integer with rint() (the default rounding mode is     */
+/* nearest-even), and re-encoded.                                      */
+/* ------------------------------------------------------------------ */
+
+/* Generic: p = fraction bits, emin = smallest normal exponent,
+ * emax = largest exponent; returns the value after rounding (±inf on
+ * overflow). */
+static double round_value(double v, int p, int emin, int emax) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    const double a = fabs(v);
+    int e;
+    frexp(a, &e);   /* a = f · 2^e with f in [0.5, 1): exponent of a is e - 1 */
+    e -= 1;
+    if (e < emin) e = emin;                 /* subnormal quantum */
+    const double q = ldexp(1.0, e - p);     /* quantum at this exponent */
+    double r = rint(a / q) * q;             /* exact: a/q has at most 53 bits */
+    const double maxv = ldexp(2.0 - ldexp(1.0, -p), emax);
+    if (r > maxv) r = INFINITY;
+    return v < 0 ? -r : r;
+}
+
+static uint16_t encode_bits(double r, int p, int emin, int ebits) {
+    uint16_t s = signbit(r) ? (uint16_t)(1u << (p + ebits)) : 0;
+    if (isnan(r)) return s | (uint16_t)(((1u << ebits) - 1) << p) | (uint16_t)(1u << (p - 1));
+    const double a = fabs(r);
+    if (isinf(a)) return s | (uint16_t)(((1u << ebits) - 1) << p);
+    if (a == 0.0) return s;
+    if (a < ldexp(1.0, emin)) /* subnormal: a = m · 2^(emin - p) */
+        return s | (uint16_t)(a / ldexp(1.0, emin - p));
+    int e;
+    const double f = frexp(a, &e); /* a = f·2^e, f in [0.5,1) */
+    const int E = e - 1 + ((1 << (ebits - 1)) - 1);
+    const uint16_t m = (uint16_t)((f * 2.0 - 1.0) * ldexp(1.0, p));
+    return s | (uint16_t)(E << p) | m;
+}
+
+uint16_t orc_f64_to_f16(double v) {
+    return encode_bits(round_value(v, 10, -14, 15), 10, -14, 5);
+}
+
+uint16_t orc_f64_to_bf16(double v) {
+    return encode_bits(round_value(v, 7, -126, 127), 7, -126, 8);
+}
+
+/* Round to the storage type and write element k of out. */
+static void store(void* out, int64_t k, int dt, double v) {
+    if (dt == ORC_F32)
+        ((float*)out)[k] = (float)v; /* C conversion: IEEE round-to-nearest-even */
+    else if (dt == ORC_F16)
+        ((uint16_t*)out)[k] = orc_f64_to_f16(v);
+    else
+        ((uint16_t*)out)[k] = orc_f64_to_bf16(v);
+}
+
+/* ------------------------------------------------------------------ */
+/* Pairwise summation (Higham §4.2).                                   */
+/* ------------------------------------------------------------------ */
+
+double orc_pairwise_sum(const double* t, int64_t n) {
+    if (n <= 8) {
+        double s = 0.0;
+        for (int64_t i = 0; i < n; i++) s += t[i];
+        return s;
+    }
+    const int64_t h = n / 2;
+    return orc_pairwise_sum(t, h) + orc_pairwise_sum(t + h, n - h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Weighted sum, forward  [WS §1, §2]:  y[i] = Σ_d x[i,d] · w[d].      */
+/* ------------------------------------------------------------------ */
+
+/* x: [N, D] storage type dt with row stride ldx (elements); w: [D] binary32.
+ * Outputs (any may be NULL): y_exact[i] the fp64 pairwise sum,
+ * y_abs[i] = Σ_d |x[i,d]·w[d]|, y_out[i] = y_exact[i] rounded to dt. */
+int orc_ws_fwd(const void* x, int64_t ldx, const float* w, int64_t N, int64_t D, int dt,
+               double* y_exact, double* y_abs, void* y_out) {
+    if (!x || !w || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* t = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    double* ta = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    if (!t || !ta) { free(t); free(ta); return -2; }
+    for (int64_t i = 0; i < N; i++) {
+        for (int64_t d = 0; d < D; d++) {
+            t[d] = decode(x, i * ldx + d, dt) * (double)w[d];
+            ta[d] = fabs(t[d]);
+        }
+        const double y = orc_pairwise_sum(t, D);
+        if (y_exact) y_exact[i] = y;
+        if (y_abs) y_abs[i] = orc_pairwise_sum(ta, D);
+        if (y_out) store(y_out, i, dt, y);
+    }
+    free(t);
+    free(ta);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Weighted sum, backward  [WS §3, §4]:                                */
+/*   dx[i,d]     = dy[i] · w[d]                                        */
+/*   grad_w[d]   = Σ_i x[i,d] · dy[i]                                  */
+/*   partial[p,d]= Σ_{i in tile p} x[i,d] · dy[i],                      */
+/*                 tile p = rows p·block_n .. min(N, (p+1)·block_n) - 1 */
+/* ------------------------------------------------------------------ */
+
+/* Column-wise pairwise sums over rows [a, b) of the terms x[i,d]·dy[i]
+ * into out[0..D) and of |x[i,d]·dy[i]| into out_abs[0..D) (either may be
+ * NULL).  The split points are those of orc_pairwise_sum applied to each
+ * column separately; rows are walked in storage order so that the loops
+ * read memory sequentially.  scratch holds 2·D doubles per recursion level. */
+static void colsum(const void* x, int64_t ldx, const void* dy, int dt, int64_t a, int64_t b,
+                   int64_t D, double* out, double* out_abs, double* scratch) {
+    const int64_t n = b - a;
+    if (n <= 8) {
+        for (int64_t d = 0; d < D; d++) {
+            if (out) out[d] = 0.0;
+            if (out_abs) out_abs[d] = 0.0;
+        }
+        for (int64_t i = a; i < b; i++) {
+            const double g = decode(dy, i, dt);
+            for (int64_t d = 0; d < D; d++) {
+                const double term = decode(x, i * ldx + d, dt) * g;
+                if (out) out[d] += term;
+                if (out_abs) out_abs[d] += fabs(term);
+            }
+        }
+        return;
+    }
+    const int64_t h = n / 2;
+    double* r = scratch;          /* right half, signed */
+    double* ra = scratch + D;     /* right half, absolute */
+    colsum(x, ldx, dy, dt, a, a + h, D, out, out_abs, scratch + 2 * D);
+    colsum(x, ldx, dy, dt, a + h, b, D, out ? r : NULL, out_abs ? ra : NULL, scratch + 2 * D);
+    for (int64_t d = 0; d < D; d++) {
+        if (out) out[d] += r[d];
+        if (out_abs) out_abs[d] += ra[d];
+    }
+}
+
+static int colsum_range(const void* x, int64_t ldx, const void* dy, int dt, int64_t a, int64_t b,
+                        int64_t D, double* out, double* out_abs) {
+    /* recursion depth <= 64; each level needs 2·D doubles */
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1) * 2 * 66);
+    if (!scratch) return -2;
+    colsum(x, ldx, dy, dt, a, b, D, out, out_abs, scratch);
+    free(scratch);
+    return 0;
+}
+
+/* Inputs: x [N,D] (row stride ldx), w [D] binary32, dy [N], storage dt.
+ * Outputs (any may be NULL):
+ *   dx_out [N,D] contiguous in dt: dy[i]·w[d] (an exact product) rounded once;
+ *   grad_w[d], grad_w_abs[d] = Σ_i |x[i,d]·dy[i]|;
+ *   partial [ceil(N/block_n), D] (only when block_n > 0). */
+int orc_ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64_t N, int64_t D,
+               int dt, void* dx_out, double* grad_w, double* grad_w_abs, int64_t block_n,
+               double* partial) {
+    if (!x || !w || !dy || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
+    make_tables();
+    if (dx_out)
+        for (int64_t i = 0; i < N; i++) {
+            const double g = decode(dy, i, dt);
+            for (int64_t d = 0; d < D; d++) store(dx_out, i * D + d, dt, g * (double)w[d]);
+        }
+    if ((grad_w || grad_w_abs) && colsum_range(x, ldx, dy, dt, 0, N, D, grad_w, grad_w_abs))
+        return -2;
+    if (partial && block_n > 0) {
+        const int64_t P = (N + block_n - 1) / block_n;
+        for (int64_t p = 0; p < P; p++) {
+            const int64_t a = p * block_n, b = (a + block_n < N) ? a + block_n : N;
+            if (colsum_range(x, ldx, dy, dt, a, b, D, partial + p * D, NULL)) return -2;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Scaled SiLU  [SILU]:                                                */
+/*   s = 1 / (1 + exp(-x)),  y = w·x·s                                  */
+/*   dy/dx = w·(s + x·s·(1 - s)),  dx = dy · dy/dx                      */
+/*   dw = Σ_k dy_k · x_k · s_k                                          */
+/* ------------------------------------------------------------------ */
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* x [n] in dt, scalar w.  Outputs (any may be NULL): y_exact, y_out (dt). */
+int orc_silu_fwd(const void* x, double w, int64_t n, int dt, double* y_exact, void* y_out) {
+    if (!x || n < 0 || dt < 0 || dt > 2) return -1;
+    make_tables();
+    for (int64_t k = 0; k < n; k++) {
+        const double xv = decode(x, k, dt);
+        const double y = w * xv * sigmoid(xv);
+        if (y_exact) y_exact[k] = y;
+        if (y_out) store(y_out, k, dt, y);
+    }
+    return 0;
+}
+
+/* dy, x [n] in dt, scalar w.  Outputs (any may be NULL):
+ *   dx_exact[k], dx_scale[k] = |dy·w|·(s + |x·s·(1 - s)|) (the sum of the
+ *   magnitudes of the two terms of dy/dx, scaled), dx_out[k] (dt),
+ *   dw = Σ dy·x·s (pairwise), dw_abs = Σ |dy·x·s|. */
+int orc_silu_bwd(const void* dy, const void* x, double w, int64_t n, int dt, double* dx_exact,
+                 double* dx_scale, void* dx_out, double* dw, double* dw_abs) {
+    if (!dy || !x || n < 0 || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* t = NULL;
+    double* ta = NULL;
+    if (dw || dw_abs) {
+        t = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        ta = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        if (!t || !ta) { free(t); free(ta); return -2; }
+    }
+    for (int64_t k = 0; k < n; k++) {
+        const double g = decode(dy, k, dt);
+        const double xv = decode(x, k, dt);
+        const double s = sigmoid(xv);
+        const double silu = xv * s;
+        const double dydx = w * (s + silu * (1.0 - s));
+        const double dx = g * dydx;
+        if (dx_exact) dx_exact[k] = dx;
+        if (dx_scale) dx_scale[k] = fabs(g * w) * (s + fabs(silu * (1.0 - s)));
+        if (dx_out) store(dx_out, k, dt, dx);
+        if (t) {
+            t[k] = g * silu;
+            ta[k] = fabs(t[k]);
+        }
+    }
+    if (dw) *dw = orc_pairwise_sum(t, n);
+    if (dw_abs) *dw_abs = orc_pairwise_sum(ta, n);
+    free(t);
+    free(ta);
+    return 0;
+}
