@@ -1,0 +1,170 @@
+"""backward_ws_fwd_gb300 — Python binding of libwsfwd (C ABI in include/wsf.h).
+
+Forward and backward (vector-Jacobian product) kernels of two memory-bound
+row operators on one GB300 GPU:
+
+* weighted sum  y[i] = Σ_d x[i,d]·w[d]   ("Writing Triton Kernels with
+  Autograd: A Minimal End-to-End Example", §1–§5)
+* scaled SiLU   y = w·x·sigmoid(x)        ("Backward in Triton —
+  autograd.Function and the backward grid", § A complete minimal example)
+
+This module only marshals torch tensors into the C entry points: pointers,
+sizes, the storage-type code and the current CUDA stream.  Every step runs
+in the library's kernels; there is no fallback.  Importing the module fails
+if the library has not been built (``python -m backward_ws_fwd_gb300.build``
+or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwsfwd.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libwsfwd.so is not built ({LIB_PATH}); run backward_ws_fwd_gb300/build.py")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+lib.wsf_status_string.argtypes = [_int]
+lib.wsf_status_string.restype = ctypes.c_char_p
+lib.wsf_version.argtypes = []
+lib.wsf_version.restype = _int
+lib.ws_fwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _int, _vp]
+lib.ws_fwd.restype = _int
+lib.ws_bwd_workspace_bytes.argtypes = [_i64, _i64, _int, _i64]
+lib.ws_bwd_workspace_bytes.restype = _sz
+lib.ws_bwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _vp, _sz, _i64, _i64, _i64,
+                       _int, _vp]
+lib.ws_bwd.restype = _int
+lib.silu_fwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
+lib.silu_fwd.restype = _int
+lib.silu_bwd_workspace_bytes.argtypes = [_i64, _int]
+lib.silu_bwd_workspace_bytes.restype = _sz
+lib.silu_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _vp, _sz, _i64, _int, _vp]
+lib.silu_bwd.restype = _int
+
+F32, F16, BF16 = 0, 1, 2
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+# status codes (include/wsf.h)
+OK, ERR_NULL_PTR, ERR_BAD_SHAPE, ERR_BAD_DTYPE, ERR_BAD_STRIDE = 0, -1, -2, -3, -4
+ERR_WORKSPACE, ERR_OVERLAP, ERR_MISALIGNED, ERR_BAD_ARG, ERR_CUDA = -5, -6, -7, -8, -9
+
+
+class WsfError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def status_string(status: int) -> str:
+    return lib.wsf_status_string(status).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    try:
+        return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported storage type {t.dtype}") from None
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise WsfError(rc, what)
+
+
+def ws_bwd_workspace_bytes(N: int, D: int, dtype, block_n: int = 0) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code_of_dtype(dtype)
+    return lib.ws_bwd_workspace_bytes(N, D, code, block_n)
+
+
+def silu_bwd_workspace_bytes(n: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code_of_dtype(dtype)
+    return lib.silu_bwd_workspace_bytes(n, code)
+
+
+def _dtype_code_of_dtype(dt) -> int:
+    import torch
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[dt]
+
+
+def ws_fwd(x, w, y=None, stream=None):
+    """y[i] = Σ_d x[i,d]·w[d].  x: [N, D] CUDA tensor with unit inner stride;
+    w: [D] float32; y: [N] of x's dtype (allocated when None)."""
+    import torch
+    N, D = x.shape
+    if y is None:
+        y = torch.empty(N, dtype=x.dtype, device=x.device)
+    _check(lib.ws_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(y), N, D, _dtype_code(x),
+                      _stream(stream)), "ws_fwd")
+    return y
+
+
+def ws_bwd(x, w, dy, dx=None, grad_w=None, accumulate=False, workspace=None, block_n=0,
+           stream=None):
+    """dx[i,d] = dy[i]·w[d]; grad_w[d] (+)= Σ_i x[i,d]·dy[i].  Returns (dx, grad_w)."""
+    import torch
+    N, D = x.shape
+    code = _dtype_code(x)
+    if dx is None:
+        dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    if grad_w is None:
+        grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
+    need = lib.ws_bwd_workspace_bytes(N, D, code, block_n)
+    if workspace is None and need not in (0, SIZE_MAX):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.ws_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
+                      _ptr(grad_w), int(bool(accumulate)), _ptr(workspace), wbytes, block_n, N, D,
+                      code, _stream(stream)), "ws_bwd")
+    return dx, grad_w
+
+
+def silu_fwd(x, w, y=None, stream=None):
+    """y = w·x·sigmoid(x).  x contiguous (any shape); w: one float32 on the device."""
+    import torch
+    assert x.is_contiguous()
+    if y is None:
+        y = torch.empty_like(x)
+    _check(lib.silu_fwd(_ptr(x), _ptr(w), _ptr(y), x.numel(), _dtype_code(x), _stream(stream)),
+           "silu_fwd")
+    return y
+
+
+def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, stream=None):
+    """dx = dy·w·(s + x·s·(1 − s)); dw (+)= Σ dy·x·s.  Returns (dx, dw)."""
+    import torch
+    assert x.is_contiguous() and dy.is_contiguous()
+    code = _dtype_code(x)
+    n = x.numel()
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(1, dtype=torch.float32, device=x.device)
+    need = lib.silu_bwd_workspace_bytes(n, code)
+    if workspace is None and need not in (0, SIZE_MAX):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.silu_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), ctypes.c_void_p(dw.data_ptr()),
+                        int(bool(accumulate)), _ptr(workspace), wbytes, n, code, _stream(stream)),
+           "silu_bwd")
+    return dx, dw
+
+
+__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "silu_fwd",
+           "silu_bwd", "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "F32", "F16", "BF16"]

@@ -1,0 +1,184 @@
+// abi.cu — the extern "C" entry points declared in include/wsf.h.
+//
+// Every entry point validates its arguments on the host, before anything is
+// enqueued, and maps them to a launcher in ws.cu / silu.cu.  Host-only work
+// here never touches the device, so argument errors can be checked without
+// a GPU.
+#include <limits.h>
+#include <stdint.h>
+
+#include "wsf.h"
+#include "wsf_internal.h"
+
+namespace {
+
+using wsf::elt_bytes;
+
+bool valid_dtype(int dtype) { return dtype == WSF_F32 || dtype == WSF_F16 || dtype == WSF_BF16; }
+
+// a * b without overflow of int64 (both non-negative)
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a == 0 || b == 0) {
+        *out = 0;
+        return true;
+    }
+    if (a > INT64_MAX / b) return false;
+    *out = a * b;
+    return true;
+}
+
+// Byte extent of a [rows, cols] matrix with row stride ld (elements): the
+// span from the first to one past the last element; 0 if empty; -1 on
+// overflow.
+int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld, int esize) {
+    if (rows == 0 || cols == 0) return 0;
+    int64_t a;
+    if (!mul_ok(rows - 1, ld, &a)) return -1;
+    if (a > INT64_MAX - cols) return -1;
+    int64_t b;
+    if (!mul_ok(a + cols, esize, &b)) return -1;
+    return b;
+}
+
+bool aligned_to(const void* p, int a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Span span(const void* p, int64_t bytes) {
+    return Span{(uintptr_t)p, (uintptr_t)p + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+
+bool overlap(Span a, Span b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? WSF_OK : WSF_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wsf_status_string(int status) {
+    switch (status) {
+        case WSF_OK: return "ok";
+        case WSF_ERR_NULL_PTR: return "a required pointer is NULL";
+        case WSF_ERR_BAD_SHAPE: return "negative extent or size overflow";
+        case WSF_ERR_BAD_DTYPE: return "unknown storage type";
+        case WSF_ERR_BAD_STRIDE: return "row stride smaller than the row length";
+        case WSF_ERR_WORKSPACE: return "workspace missing or too small";
+        case WSF_ERR_OVERLAP: return "an output overlaps an input or another output";
+        case WSF_ERR_MISALIGNED: return "pointer not aligned to its element type";
+        case WSF_ERR_BAD_ARG: return "invalid argument";
+        case WSF_ERR_CUDA: return "CUDA launch failed";
+        default: return "unknown status";
+    }
+}
+
+int wsf_version(void) { return 100; }
+
+int ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N, int64_t D, int dtype,
+           wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    const int es = elt_bytes(dtype);
+    const bool xin = N > 0 && D > 0;
+    if (xin && ldx < D) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = xin ? extent_bytes(N, D, ldx, es) : 0;
+    int64_t yb, wb;
+    if (xb < 0 || !mul_ok(N, es, &yb) || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
+    if ((xin && (!x || !w)) || (N > 0 && !y)) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(w, 4) || !aligned_to(y, es)) return WSF_ERR_MISALIGNED;
+    if (N == 0) return WSF_OK;
+    const Span sy = span(y, yb);
+    if (overlap(sy, span(x, xb)) || overlap(sy, span(w, xin ? wb : 0))) return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_ws_fwd(x, ldx, w, y, N, D, dtype, (cudaStream_t)stream));
+}
+
+size_t ws_bwd_workspace_bytes(int64_t N, int64_t D, int dtype, int64_t block_n) {
+    if (!valid_dtype(dtype) || N < 0 || D < 0 || block_n < 0) return SIZE_MAX;
+    const int64_t P = wsf::ws_tiles(N, D, dtype, block_n);
+    int64_t b;
+    if (!mul_ok(P, D, &b) || !mul_ok(b, 4, &b) || b > INT64_MAX - 255) return SIZE_MAX;
+    return (size_t)((b + 255) / 256 * 256);
+}
+
+int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx, int64_t lddx,
+           float* grad_w, int accumulate, void* workspace, size_t workspace_bytes, int64_t block_n,
+           int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    if (block_n < 0 || (accumulate != 0 && accumulate != 1)) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldx < D || lddx < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = mat ? extent_bytes(N, D, ldx, es) : 0;
+    const int64_t dxb = mat ? extent_bytes(N, D, lddx, es) : 0;
+    int64_t dyb, wb;
+    if (xb < 0 || dxb < 0 || !mul_ok(N, es, &dyb) || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
+    if ((mat && (!x || !dy || !dx || !w)) || (D > 0 && !grad_w)) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(w, 4) ||
+        !aligned_to(grad_w, 4) || !aligned_to(workspace, 4))
+        return WSF_ERR_MISALIGNED;
+    const size_t need = ws_bwd_workspace_bytes(N, D, dtype, block_n);
+    if (need == SIZE_MAX) return WSF_ERR_BAD_SHAPE;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return WSF_ERR_WORKSPACE;
+    if (D == 0) return WSF_OK;
+    const Span sdx = span(dx, dxb), sg = span(grad_w, wb), sws = span(workspace, (int64_t)need);
+    const Span sx = span(x, xb), sdy = span(dy, mat ? dyb : 0), sw = span(w, mat ? wb : 0);
+    if (overlap(sdx, sx) || overlap(sdx, sdy) || overlap(sdx, sw) || overlap(sg, sx) ||
+        overlap(sg, sdy) || overlap(sg, sw) || overlap(sws, sx) || overlap(sws, sdy) ||
+        overlap(sws, sw) || overlap(sdx, sg) || overlap(sdx, sws) || overlap(sg, sws))
+        return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_ws_bwd(x, ldx, w, dy, dx, lddx, grad_w, accumulate,
+                                          (float*)workspace, block_n, N, D, dtype,
+                                          (cudaStream_t)stream));
+}
+
+int silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (n < 0) return WSF_ERR_BAD_SHAPE;
+    const int es = elt_bytes(dtype);
+    int64_t b;
+    if (!mul_ok(n, es, &b)) return WSF_ERR_BAD_SHAPE;
+    if (n > 0 && (!x || !y || !w)) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(y, es) || !aligned_to(w, 4)) return WSF_ERR_MISALIGNED;
+    if (n == 0) return WSF_OK;
+    const Span sy = span(y, b);
+    if (overlap(sy, span(x, b)) || overlap(sy, span(w, 4))) return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_silu_fwd(x, w, y, n, dtype, (cudaStream_t)stream));
+}
+
+size_t silu_bwd_workspace_bytes(int64_t n, int dtype) {
+    if (!valid_dtype(dtype) || n < 0) return SIZE_MAX;
+    const int64_t P = wsf::silu_tiles(n);
+    return (size_t)((P * 4 + 255) / 256 * 256);
+}
+
+int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw, int accumulate,
+             void* workspace, size_t workspace_bytes, int64_t n, int dtype, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (n < 0) return WSF_ERR_BAD_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    int64_t b;
+    if (!mul_ok(n, es, &b)) return WSF_ERR_BAD_SHAPE;
+    if (!dw || (n > 0 && (!x || !dy || !dx || !w))) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(w, 4) ||
+        !aligned_to(dw, 4) || !aligned_to(workspace, 4))
+        return WSF_ERR_MISALIGNED;
+    const size_t need = silu_bwd_workspace_bytes(n, dtype);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return WSF_ERR_WORKSPACE;
+    const Span sdx = span(dx, b), sdw = span(dw, 4), sws = span(workspace, (int64_t)need);
+    const Span sx = span(x, b), sdy = span(dy, b), sw = span(w, n > 0 ? 4 : 0);
+    if (overlap(sdx, sx) || overlap(sdx, sdy) || overlap(sdx, sw) || overlap(sdw, sx) ||
+        overlap(sdw, sdy) || overlap(sdw, sw) || overlap(sws, sx) || overlap(sws, sdy) ||
+        overlap(sws, sw) || overlap(sdx, sdw) || overlap(sdx, sws) || overlap(sdw, sws))
+        return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_silu_bwd(dy, x, w, dx, dw, accumulate, (float*)workspace, n,
+                                            dtype, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// silu.cu — scaled-SiLU forward and backward kernels for sm_103a.
+//
+// Operator ("Backward in Triton — autograd.Function and the backward grid",
+// § A complete minimal example — fused scaled-SiLU): s = sigmoid(x),
+// y = w·x·s with one learnable scalar w.  Backward: dx = dy·w·(s + x·s·(1−s))
+// is elementwise; dw = Σ dy·x·s reduces over every element.  The page's
+// atomic add of per-block sums is replaced by the two-pass partials buffer
+// that its § The backward grid is not the forward grid names as the
+// deterministic choice: per-block fp32 partials, then one block sums them in
+// a fixed tree order.  s is recomputed from x in the backward (§ Save vs
+// recompute).
+//
+// Evaluation in fp32.  With a = |x| and t = exp(−a) (never overflows),
+// r = 1/(1+t):
+//   x >= 0:  s = r,    silu'(x) = r²·(1 + t·(1+x))
+//   x <  0:  s = t·r,  silu'(x) = t·r²·((1+x) + t)
+// Both are algebraically s + x·s·(1−s).  The second form keeps the
+// cancellation near the minimum of silu (x ≈ −1.2785, where silu' = 0) down
+// to the error of exp: (1+x) is exact for x in [−2, −1/2] and (1+x) + t is
+// an exact difference there.
+#include <algorithm>
+
+#include "wsf_device.cuh"
+#include "wsf_internal.h"
+
+namespace wsf {
+
+constexpr int64_t kSiluTilesMax = 8 * kDesignSMs;   // 1216 partials at most
+constexpr int64_t kSiluElemsPerTileMin = 8192;
+
+int64_t silu_tiles(int64_t n) {
+    if (n <= 0) return 0;
+    const int64_t p = (n + kSiluElemsPerTileMin - 1) / kSiluElemsPerTileMin;
+    return p < kSiluTilesMax ? p : kSiluTilesMax;
+}
+
+struct SiluTerms {
+    float silu;   // x·s
+    float dsilu;  // d(x·s)/dx
+};
+
+__device__ __forceinline__ float silu_only(float x) {
+    const float t = expf(-fabsf(x));
+    const float r = 1.0f / (1.0f + t);
+    const float s = (x >= 0.f) ? r : t * r;
+    return x * s;
+}
+
+__device__ __forceinline__ SiluTerms silu_terms(float x) {
+    const float t = expf(-fabsf(x));
+    const float r = 1.0f / (1.0f + t);
+    SiluTerms o;
+    if (x >= 0.f) {
+        o.silu = x * r;
+        o.dsilu = (r * r) * fmaf(t, 1.0f + x, 1.0f);
+    } else {
+        const float s = t * r;
+        o.silu = x * s;
+        o.dsilu = (s * r) * ((1.0f + x) + t);
+    }
+    return o;
+}
+
+// ---------------------------------------------------------------------------
+// Forward: 16-byte vectors, U per thread in flight, grid-stride.
+template <typename T, int U, int NT>
+__global__ void __launch_bounds__(NT)
+    silu_fwd_vec(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
+                 int64_t n) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    const float wv = __ldg(w);
+    const int64_t nv = n / V;
+    for (int64_t base = (int64_t)blockIdx.x * NT * U; base < nv; base += (int64_t)gridDim.x * NT * U) {
+        Raw16 xr[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = base + (int64_t)u * NT + threadIdx.x;
+            xr[u] = (i < nv) ? ld_stream(x + i * V) : raw_zero();
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = base + (int64_t)u * NT + threadIdx.x;
+            if (i < nv) {
+                float f[V];
+                E::widen(xr[u], f);
+#pragma unroll
+                for (int v = 0; v < V; v++) f[v] = wv * silu_only(f[v]);
+                st_stream(y + i * V, E::narrow(f));
+            }
+        }
+    }
+    if (blockIdx.x == 0) {
+        const int64_t k = nv * V + threadIdx.x;
+        if (k < n) E::store1(y + k, wv * silu_only(E::load1(x + k)));
+    }
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT)
+    silu_fwd_scalar(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
+                    int64_t n) {
+    using E = Elt<T>;
+    const float wv = __ldg(w);
+    for (int64_t k = (int64_t)blockIdx.x * NT + threadIdx.x; k < n; k += (int64_t)gridDim.x * NT)
+        E::store1(y + k, wv * silu_only(E::load1(x + k)));
+}
+
+// ---------------------------------------------------------------------------
+// Backward, stage 1.  Block p owns vectors [p·nv/P, (p+1)·nv/P) (the last
+// block also the n mod V tail elements); each thread accumulates dy·silu(x)
+// over its elements in order, then the block combines: xor butterfly inside
+// each warp, warps added in index order.
+template <int NT>
+__device__ __forceinline__ void block_sum_store(float acc, float* out) {
+    constexpr int NW = NT / 32;
+    __shared__ float red[NW];
+    acc = group_sum<32>(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = red[0];
+#pragma unroll
+        for (int q = 1; q < NW; q++) s += red[q];
+        *out = s;
+    }
+}
+
+template <typename T, int U, int NT>
+__global__ void __launch_bounds__(NT)
+    silu_bwd_vec(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
+                 T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    const float wv = __ldg(w);
+    const int64_t nv = n / V;
+    const int64_t p = blockIdx.x;
+    const int64_t vb = (p * nv) / P, ve = ((p + 1) * nv) / P;
+    float acc = 0.f;
+    for (int64_t base = vb; base < ve; base += (int64_t)NT * U) {
+        Raw16 xr[U], gr[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = base + (int64_t)u * NT + threadIdx.x;
+            const bool ok = i < ve;
+            xr[u] = ok ? ld_stream(x + i * V) : raw_zero();
+            gr[u] = ok ? ld_stream(dy + i * V) : raw_zero();
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = base + (int64_t)u * NT + threadIdx.x;
+            float xf[V], gf[V];
+            E::widen(xr[u], xf);
+            E::widen(gr[u], gf);
+#pragma unroll
+            for (int v = 0; v < V; v++) {
+                const SiluTerms st = silu_terms(xf[v]);
+                acc = fmaf(gf[v], st.silu, acc);
+                xf[v] = (gf[v] * wv) * st.dsilu;
+            }
+            if (i < ve) st_stream(dx + i * V, E::narrow(xf));
+        }
+    }
+    if (p == P - 1) {
+        const int64_t k = nv * V + threadIdx.x;
+        if (k < n) {
+            const float xv = E::load1(x + k), gv = E::load1(dy + k);
+            const SiluTerms st = silu_terms(xv);
+            acc = fmaf(gv, st.silu, acc);
+            E::store1(dx + k, (gv * wv) * st.dsilu);
+        }
+    }
+    block_sum_store<NT>(acc, part + p);
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT)
+    silu_bwd_scalar(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
+                    T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
+    using E = Elt<T>;
+    const float wv = __ldg(w);
+    const int64_t p = blockIdx.x;
+    const int64_t kb = (p * n) / P, ke = ((p + 1) * n) / P;
+    float acc = 0.f;
+    for (int64_t k = kb + threadIdx.x; k < ke; k += NT) {
+        const float xv = E::load1(x + k), gv = E::load1(dy + k);
+        const SiluTerms st = silu_terms(xv);
+        acc = fmaf(gv, st.silu, acc);
+        E::store1(dx + k, (gv * wv) * st.dsilu);
+    }
+    block_sum_store<NT>(acc, part + p);
+}
+
+// Backward, stage 2: one block; thread t sums part[t], part[t + NT], ... in
+// order, then the block combines as above.  dw = (accumulate ? dw : 0) + sum.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+    silu_bwd_reduce(const float* __restrict__ part, int64_t P, float* __restrict__ dw,
+                    int accumulate) {
+    float s = 0.f;
+    for (int64_t i = threadIdx.x; i < P; i += NT) s += part[i];
+    __shared__ float total;
+    block_sum_store<NT>(s, &total);
+    if (threadIdx.x == 0) *dw = accumulate ? *dw + total : total;
+}
+
+// ---------------------------------------------------------------------------
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <typename T>
+static cudaError_t silu_fwd_t(const T* x, const float* w, T* y, int64_t n, cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    if (aligned16(x) && aligned16(y)) {
+        constexpr int NT = 256, U = 4;
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(cdiv(n / V, NT * U), 8 * kDesignSMs));
+        return launch(silu_fwd_vec<T, U, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, w, y,
+                      n);
+    }
+    constexpr int NT = 256;
+    const int64_t grid = std::min<int64_t>(cdiv(n, NT), 8 * kDesignSMs);
+    return launch(silu_fwd_scalar<T, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, w, y, n);
+}
+
+cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
+                            cudaStream_t s) {
+    switch (dtype) {
+        case 0: return silu_fwd_t((const float*)x, w, (float*)y, n, s);
+        case 1: return silu_fwd_t((const __half*)x, w, (__half*)y, n, s);
+        default: return silu_fwd_t((const __nv_bfloat16*)x, w, (__nv_bfloat16*)y, n, s);
+    }
+}
+
+template <typename T>
+static cudaError_t silu_bwd_t(const T* dy, const T* x, const float* w, T* dx, float* dw,
+                              int accumulate, float* part, int64_t n, cudaStream_t s) {
+    const int64_t P = silu_tiles(n);
+    cudaError_t e = cudaSuccess;
+    if (P > 0) {
+        if (aligned16(dy) && aligned16(x) && aligned16(dx)) {
+            constexpr int NT = 256, U = 2;
+            e = launch(silu_bwd_vec<T, U, NT>, dim3((unsigned)P), dim3(NT), 0, s, false, dy, x, w,
+                       dx, part, n, P);
+        } else {
+            constexpr int NT = 256;
+            e = launch(silu_bwd_scalar<T, NT>, dim3((unsigned)P), dim3(NT), 0, s, false, dy, x, w,
+                       dx, part, n, P);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    constexpr int NT = 1024;
+    return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, false, (const float*)part, P, dw,
+                  accumulate);
+}
+
+cudaError_t launch_silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                            int accumulate, float* part, int64_t n, int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return silu_bwd_t((const float*)dy, (const float*)x, w, (float*)dx, dw, accumulate,
+                              part, n, s);
+        case 1:
+            return silu_bwd_t((const __half*)dy, (const __half*)x, w, (__half*)dx, dw, accumulate,
+                              part, n, s);
+        default:
+            return silu_bwd_t((const __nv_bfloat16*)dy, (const __nv_bfloat16*)x, w,
+                              (__nv_bfloat16*)dx, dw, accumulate, part, n, s);
+    }
+}
+
+}  // namespace wsf

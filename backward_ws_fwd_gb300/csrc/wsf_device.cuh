@@ -1,0 +1,154 @@
+// wsf_device.cuh — device helpers shared by the libwsfwd kernels (sm_103a):
+// 128-bit streaming loads/stores, widening of 16-bit storage types to fp32,
+// round-to-nearest-even narrowing, warp reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wsf {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// Number of SMs the launch shapes are designed for (GB300: 2 dies x 76).
+// It fixes grid sizes and tile counts as constants so that the reduction
+// order, and therefore every bit of grad_w / dw, never depends on the device.
+constexpr int kDesignSMs = 152;
+
+// ---------------------------------------------------------------------------
+// 16-byte vector of raw storage.
+struct alignas(16) Raw16 {
+    uint32_t u[4];
+};
+
+__device__ __forceinline__ Raw16 raw_zero() {
+    Raw16 r;
+    r.u[0] = r.u[1] = r.u[2] = r.u[3] = 0u;
+    return r;
+}
+
+// Streaming read of 16 bytes that is used once: read-only path, no L1
+// allocation, and a 256-byte L2 prefetch so DRAM serves whole bursts.
+__device__ __forceinline__ Raw16 ld_stream(const void* p) {
+    Raw16 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.u[0]), "=r"(r.u[1]), "=r"(r.u[2]), "=r"(r.u[3])
+                 : "l"(p));
+    return r;
+}
+
+// Read of 16 bytes expected to be reused from L1/L2 (weights).
+__device__ __forceinline__ Raw16 ld_keep(const void* p) {
+    Raw16 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.u[0]), "=r"(r.u[1]), "=r"(r.u[2]), "=r"(r.u[3])
+                 : "l"(p));
+    return r;
+}
+
+// Streaming write of 16 bytes (evict-first in L2).
+__device__ __forceinline__ void st_stream(void* p, const Raw16& r) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.u[0]), "r"(r.u[1]),
+                 "r"(r.u[2]), "r"(r.u[3])
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Storage-type traits: V elements per 16 bytes, widening, narrowing.
+template <typename T>
+struct Elt;
+
+template <>
+struct Elt<float> {
+    static constexpr int V = 4;
+    __device__ __forceinline__ static void widen(const Raw16& r, float (&f)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) f[i] = __uint_as_float(r.u[i]);
+    }
+    __device__ __forceinline__ static Raw16 narrow(const float (&f)[4]) {
+        Raw16 r;
+#pragma unroll
+        for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(f[i]);
+        return r;
+    }
+    __device__ __forceinline__ static float load1(const float* p) { return __ldg(p); }
+    __device__ __forceinline__ static void store1(float* p, float v) { *p = v; }
+};
+
+template <>
+struct Elt<__half> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static void widen(const Raw16& r, float (&f)[8]) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            __half2 h;
+            memcpy(&h, &r.u[i], 4);
+            const float2 v = __half22float2(h);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+    __device__ __forceinline__ static Raw16 narrow(const float (&f)[8]) {
+        Raw16 r;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            memcpy(&r.u[i], &h, 4);
+        }
+        return r;
+    }
+    __device__ __forceinline__ static float load1(const __half* p) { return __half2float(__ldg(p)); }
+    __device__ __forceinline__ static void store1(__half* p, float v) { *p = __float2half_rn(v); }
+};
+
+template <>
+struct Elt<__nv_bfloat16> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static void widen(const Raw16& r, float (&f)[8]) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            // bfloat16 is the upper half of a binary32 pattern: widening is a shift.
+            f[2 * i] = __uint_as_float(r.u[i] << 16);
+            f[2 * i + 1] = __uint_as_float(r.u[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static Raw16 narrow(const float (&f)[8]) {
+        Raw16 r;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            memcpy(&r.u[i], &h, 4);
+        }
+        return r;
+    }
+    __device__ __forceinline__ static float load1(const __nv_bfloat16* p) {
+        return __bfloat162float(__ldg(p));
+    }
+    __device__ __forceinline__ static void store1(__nv_bfloat16* p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Sum over the lanes of aligned groups of `Width` lanes (xor butterfly); every
+// lane of a group ends with the group's sum.  The operand order is fixed, so
+// the result is the same bits on every run.
+template <int Width>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int off = Width / 2; off > 0; off >>= 1) v += __shfl_xor_sync(FULL_MASK, v, off);
+    return v;
+}
+
+// Pick a[i] for a runtime i without dynamic register indexing.
+template <int K>
+__device__ __forceinline__ float select(const float (&a)[K], int i) {
+    float v = a[0];
+#pragma unroll
+    for (int k = 1; k < K; k++) v = (i == k) ? a[k] : v;
+    return v;
+}
+
+}  // namespace wsf

@@ -1,0 +1,55 @@
+// wsf_internal.h — host-side interface between the C ABI (abi.cu) and the
+// kernel launchers (ws.cu, silu.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace wsf {
+
+// Bytes per element of a storage type (0 for an invalid code).
+inline int elt_bytes(int dtype) { return dtype == 0 ? 4 : (dtype == 1 || dtype == 2) ? 2 : 0; }
+
+// Number of row tiles P of the weighted-sum backward (rows of the partial
+// buffer).  Depends only on the sizes, the storage type and block_n.
+int64_t ws_tiles(int64_t N, int64_t D, int dtype, int64_t block_n);
+
+// Number of per-block partials of the scaled-SiLU backward.
+int64_t silu_tiles(int64_t n);
+
+cudaError_t launch_ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N,
+                          int64_t D, int dtype, cudaStream_t s);
+
+cudaError_t launch_ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                          int64_t lddx, float* grad_w, int accumulate, float* partial,
+                          int64_t block_n, int64_t N, int64_t D, int dtype, cudaStream_t s);
+
+cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
+                            cudaStream_t s);
+
+cudaError_t launch_silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                            int accumulate, float* part, int64_t n, int dtype, cudaStream_t s);
+
+// Launch through cudaLaunchKernelEx so that the status returned is this
+// launch's own.  `pdl` lets the kernel start while the previous kernel on
+// the stream drains; such a kernel must wait (griddepcontrol.wait) before
+// touching that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace wsf

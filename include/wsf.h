@@ -1,0 +1,157 @@
+/*
+ * wsf.h — C ABI of libwsfwd: forward and backward (vector-Jacobian product)
+ * kernels of two memory-bound row operators on one GPU (sm_103a).
+ *
+ *   weighted sum   y[i] = Σ_d x[i,d]·w[d]           x [N,D], w [D], y [N]
+ *   scaled SiLU    y    = w·x·sigmoid(x)            x [n], scalar w
+ *
+ * Sources (web pages, cited by title and section):
+ *   [WS]   "Writing Triton Kernels with Autograd: A Minimal End-to-End
+ *          Example": §1 Problem Setup, §2 Triton Forward Kernel, §3 Backward:
+ *          Deriving Gradients First, §4 Triton Backward Kernel, §5 Wrapping
+ *          with torch.autograd.Function.
+ *   [SILU] "Backward in Triton — autograd.Function and the backward grid":
+ *          § A complete minimal example — fused scaled-SiLU; § The backward
+ *          grid is not the forward grid; § fp32 accumulation, and why
+ *          gradients use +=.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every pointer argument is DEVICE memory owned by the caller.  The
+ * library allocates nothing, keeps no state between calls, and never frees
+ * caller memory.  A pointer may be NULL only when the buffer it addresses
+ * has no elements.  Outputs must not overlap any input or each other
+ * (checked on the host; WSF_ERR_OVERLAP).
+ *
+ * Types.  `dtype` is the storage type of x, dy, y and dx: WSF_F32, WSF_F16
+ * (IEEE binary16) or WSF_BF16 (bfloat16).  w, grad_w and dw are always
+ * binary32.  All arithmetic is binary32 (16-bit inputs are widened exactly);
+ * each 16-bit output is rounded once, to nearest-even.
+ *
+ * Layout.  x and dx are row-major with unit inner stride; row i starts at
+ * element i·ld (ld >= D).  Any alignment of the element type is accepted:
+ * 16-byte-aligned pointers and strides take 128-bit vector paths, others a
+ * scalar path.
+ *
+ * Streams and errors.  Work is enqueued on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and the call returns without waiting.
+ * Arguments are validated on the host before anything is enqueued; a
+ * rejected call enqueues nothing and returns a negative status.  A launch
+ * failure reported by the CUDA runtime returns WSF_ERR_CUDA.  Faults inside
+ * a kernel surface at the caller's next synchronisation.  No entry point
+ * throws or aborts.
+ *
+ * Determinism.  The parameter gradients (grad_w, dw) are reduced in two
+ * stages — per-tile partial sums into the caller's workspace, then a sum
+ * over tiles in a fixed order — with no atomic operations, so repeating a
+ * call with the same arguments gives the same bits.  The tiling depends only
+ * on the sizes, the storage type and block_n, never on the device.
+ */
+#ifndef WSF_H
+#define WSF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* wsf_stream_t;
+
+/* storage types */
+#define WSF_F32 0
+#define WSF_F16 1
+#define WSF_BF16 2
+
+/* status codes */
+#define WSF_OK 0
+#define WSF_ERR_NULL_PTR (-1)   /* a required pointer is NULL */
+#define WSF_ERR_BAD_SHAPE (-2)  /* negative extent, or a size that overflows int64 */
+#define WSF_ERR_BAD_DTYPE (-3)  /* dtype is not WSF_F32 / WSF_F16 / WSF_BF16 */
+#define WSF_ERR_BAD_STRIDE (-4) /* a row stride smaller than D */
+#define WSF_ERR_WORKSPACE (-5)  /* workspace NULL or smaller than the query says */
+#define WSF_ERR_OVERLAP (-6)    /* an output overlaps an input or another output */
+#define WSF_ERR_MISALIGNED (-7) /* a pointer not aligned to its element type */
+#define WSF_ERR_BAD_ARG (-8)    /* another invalid argument (block_n < 0, accumulate not 0/1) */
+#define WSF_ERR_CUDA (-9)       /* the CUDA runtime rejected a launch */
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* wsf_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int wsf_version(void);
+
+/*
+ * ws_fwd — weighted-sum forward  [WS §1, §2]
+ *   y[i] = Σ_{d<D} x[i,d] · w[d]   for 0 <= i < N
+ * x: [N, D] dtype, row stride ldx; w: [D] binary32; y: [N] dtype.
+ * Products and the sum are binary32; y is rounded once to dtype.  D == 0
+ * writes y = 0; N == 0 does nothing.
+ */
+int ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N, int64_t D, int dtype,
+           wsf_stream_t stream);
+
+/*
+ * ws_bwd_workspace_bytes — size in bytes of the fp32 partial buffer that
+ * ws_bwd needs for these sizes: P·D·4 rounded up to 256, where P is the
+ * number of row tiles.  block_n > 0 forces tiles of block_n consecutive rows
+ * (P = ceil(N / block_n)), as in [WS §3]'s BLOCK_N; block_n == 0 lets the
+ * library choose.  Returns 0 when no workspace is needed, and SIZE_MAX for
+ * invalid arguments.  Host-only; touches no device.
+ */
+size_t ws_bwd_workspace_bytes(int64_t N, int64_t D, int dtype, int64_t block_n);
+
+/*
+ * ws_bwd — weighted-sum backward  [WS §3, §4]
+ *   dx[i,d]   = dy[i] · w[d]                       (elementwise, written)
+ *   grad_w[d] = Σ_{i<N} x[i,d] · dy[i]             (reduction over rows)
+ * Inputs: x [N, D] dtype (row stride ldx), w [D] binary32, dy [N] dtype.
+ * Outputs: dx [N, D] dtype (row stride lddx), grad_w [D] binary32.
+ * Stage 1 writes dx and, for each row tile p, partial[p, d] = Σ over the
+ * tile's rows of x[i,d]·dy[i] into `workspace` (binary32, [P, D]).
+ * Stage 2 sums partial[0..P-1, d] in a fixed order; with accumulate == 1 the
+ * result is added to the existing grad_w[d] (old + sum, one binary32 add),
+ * with accumulate == 0 it replaces it ([SILU] § fp32 accumulation ...: a
+ * gradient accumulates with += across micro-batches).  N == 0 gives
+ * grad_w = 0 (or leaves it when accumulating).  The workspace contents are
+ * scratch: nothing needs to be initialised and nothing is kept.
+ */
+int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx, int64_t lddx,
+           float* grad_w, int accumulate, void* workspace, size_t workspace_bytes,
+           int64_t block_n, int64_t N, int64_t D, int dtype, wsf_stream_t stream);
+
+/*
+ * silu_fwd — scaled-SiLU forward  [SILU, forward kernel]
+ *   s = 1 / (1 + exp(-x)),  y = w · x · s       elementwise over n elements
+ * x, y: [n] dtype (contiguous); w: one binary32 value in device memory.
+ */
+int silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype, wsf_stream_t stream);
+
+/*
+ * silu_bwd_workspace_bytes — bytes of the fp32 per-block partial buffer for
+ * silu_bwd (P·4 rounded up to 256); 0 when none is needed, SIZE_MAX for
+ * invalid arguments.  Host-only.
+ */
+size_t silu_bwd_workspace_bytes(int64_t n, int dtype);
+
+/*
+ * silu_bwd — scaled-SiLU backward  [SILU, backward kernel; § The backward
+ * grid is not the forward grid]
+ *   dx = dy · w · (s + x·s·(1 - s))             elementwise (written)
+ *   dw = Σ_k dy_k · x_k · s_k                    scalar reduction over all n
+ * s is recomputed from x (nothing from the forward is needed but x and w).
+ * Stage 1 writes dx and one binary32 partial of dw per block into
+ * `workspace`; stage 2 reduces the partials in a fixed tree order into *dw
+ * (added to the existing value when accumulate == 1).  n == 0 gives dw = 0
+ * (or leaves it when accumulating).
+ */
+int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw, int accumulate,
+             void* workspace, size_t workspace_bytes, int64_t n, int dtype, wsf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSF_H */

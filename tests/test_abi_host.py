@@ -1,0 +1,154 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry
+point that include/wsf.h declares, answers its workspace queries, and
+rejects bad arguments before touching any device (no GPU needed: every
+pointer here is a fake address that must never be dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def wsf():
+    from backward_ws_fwd_gb300 import build
+    build.build()
+    import backward_ws_fwd_gb300 as m
+    return m
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "wsf.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\**\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(wsf):
+    names = _declared_functions()
+    assert {"ws_fwd", "ws_bwd", "silu_fwd", "silu_bwd", "ws_bwd_workspace_bytes",
+            "silu_bwd_workspace_bytes", "wsf_status_string", "wsf_version"} <= set(names)
+    for n in names:
+        assert hasattr(wsf.lib, n), n
+
+
+def test_status_strings(wsf):
+    for code in range(-9, 1):
+        s = wsf.status_string(code)
+        assert s and s != "unknown status"
+    assert wsf.status_string(-100) == "unknown status"
+
+
+def test_workspace_queries(wsf):
+    q = wsf.lib.ws_bwd_workspace_bytes
+    # the worked shape: 100 rows in 32-row tiles -> 4 partial rows of 64 fp32
+    assert q(100, 64, wsf.F32, 32) == 4 * 64 * 4
+    assert q(100, 64, wsf.F32, 1) == ((100 * 64 * 4 + 255) // 256) * 256
+    assert q(0, 64, wsf.F32, 0) == 0 and q(5, 0, wsf.F16, 0) == 0
+    assert q(-1, 4, wsf.F32, 0) == wsf.SIZE_MAX
+    assert q(4, 4, 7, 0) == wsf.SIZE_MAX and q(4, 4, wsf.F32, -1) == wsf.SIZE_MAX
+    for N, D, dt in [(1 << 20, 1024, wsf.BF16), (1 << 24, 64, wsf.F16), (4096, 65536, wsf.F32),
+                     (7, 5, wsf.F32), (1, 1, wsf.F16)]:
+        b = q(N, D, dt, 0)
+        assert b % 256 == 0 and b >= 4 * D and b <= max(4 * D * N, 256) + 255
+        # at most 608 tiles and at most one tile per 64 rows
+        P = b // (4 * D)
+        assert P <= 608 and (P <= max(1, -(-N // 64)) or b - 4 * D * max(1, -(-N // 64)) < 256)
+    s = wsf.lib.silu_bwd_workspace_bytes
+    assert s(0, wsf.F16) == 0 and s(1, wsf.F16) == 256 and s(-1, wsf.F16) == wsf.SIZE_MAX
+    assert s(8192 * 4096, wsf.F16) == 1216 * 4 // 256 * 256 + (256 if 1216 * 4 % 256 else 0)
+
+
+F = 0x10000000  # fake, well-aligned device addresses; never dereferenced
+
+
+def _p(a):
+    return ctypes.c_void_p(a)
+
+
+def test_ws_fwd_rejects(wsf):
+    L = wsf.lib
+    s = None
+    assert L.ws_fwd(_p(F), 64, _p(2 * F), _p(3 * F), 100, 64, 9, s) == wsf.ERR_BAD_DTYPE
+    assert L.ws_fwd(_p(F), 64, _p(2 * F), _p(3 * F), -1, 64, 0, s) == wsf.ERR_BAD_SHAPE
+    assert L.ws_fwd(_p(F), 64, _p(2 * F), _p(3 * F), 100, -3, 0, s) == wsf.ERR_BAD_SHAPE
+    assert L.ws_fwd(_p(F), 63, _p(2 * F), _p(3 * F), 100, 64, 0, s) == wsf.ERR_BAD_STRIDE
+    assert L.ws_fwd(None, 64, _p(2 * F), _p(3 * F), 100, 64, 0, s) == wsf.ERR_NULL_PTR
+    assert L.ws_fwd(_p(F), 64, None, _p(3 * F), 100, 64, 0, s) == wsf.ERR_NULL_PTR
+    assert L.ws_fwd(_p(F), 64, _p(2 * F), None, 100, 64, 0, s) == wsf.ERR_NULL_PTR
+    assert L.ws_fwd(_p(F + 1), 64, _p(2 * F), _p(3 * F), 100, 64, 1, s) == wsf.ERR_MISALIGNED
+    assert L.ws_fwd(_p(F), 64, _p(2 * F + 2), _p(3 * F), 100, 64, 1, s) == wsf.ERR_MISALIGNED
+    # y inside x
+    assert L.ws_fwd(_p(F), 64, _p(2 * F), _p(F + 256), 100, 64, 0, s) == wsf.ERR_OVERLAP
+    # overflowing sizes
+    assert L.ws_fwd(_p(F), 1 << 62, _p(2 * F), _p(3 * F), 4, 64, 0, s) == wsf.ERR_BAD_SHAPE
+    # empty: nothing to do, nothing enqueued
+    assert L.ws_fwd(None, 0, None, None, 0, 64, 0, s) == wsf.OK
+
+
+def test_ws_bwd_rejects(wsf):
+    L = wsf.lib
+    s = None
+    need = L.ws_bwd_workspace_bytes(100, 64, 0, 0)
+    args = dict(x=F, ldx=64, w=2 * F, dy=3 * F, dx=4 * F, lddx=64, gw=5 * F, acc=0, ws=6 * F,
+                wsb=need, bn=0, N=100, D=64, dt=0)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.ws_bwd(_p(a["x"]) if a["x"] else None, a["ldx"], _p(a["w"]) if a["w"] else None,
+                        _p(a["dy"]) if a["dy"] else None, _p(a["dx"]) if a["dx"] else None, a["lddx"],
+                        _p(a["gw"]) if a["gw"] else None, a["acc"], _p(a["ws"]) if a["ws"] else None,
+                        a["wsb"], a["bn"], a["N"], a["D"], a["dt"], s)
+
+    assert call(dt=3) == wsf.ERR_BAD_DTYPE
+    assert call(N=-1) == wsf.ERR_BAD_SHAPE
+    assert call(bn=-2) == wsf.ERR_BAD_ARG
+    assert call(acc=2) == wsf.ERR_BAD_ARG
+    assert call(lddx=10) == wsf.ERR_BAD_STRIDE
+    assert call(ldx=10) == wsf.ERR_BAD_STRIDE
+    for k in ["x", "w", "dy", "dx", "gw"]:
+        assert call(**{k: 0}) == wsf.ERR_NULL_PTR, k
+    assert call(ws=0) == wsf.ERR_WORKSPACE
+    assert call(wsb=need - 1) == wsf.ERR_WORKSPACE
+    assert call(bn=32, wsb=need) == wsf.ERR_WORKSPACE or \
+        L.ws_bwd_workspace_bytes(100, 64, 0, 32) <= need
+    assert call(dx=F + 64) == wsf.ERR_OVERLAP
+    assert call(gw=3 * F) == wsf.ERR_OVERLAP
+    assert call(ws=4 * F + 128) == wsf.ERR_OVERLAP
+    assert call(dx=4 * F + 2) == wsf.ERR_MISALIGNED
+
+
+def test_silu_rejects(wsf):
+    L = wsf.lib
+    s = None
+    assert L.silu_fwd(_p(F), _p(2 * F), _p(3 * F), 100, 5, s) == wsf.ERR_BAD_DTYPE
+    assert L.silu_fwd(_p(F), _p(2 * F), _p(3 * F), -1, 1, s) == wsf.ERR_BAD_SHAPE
+    assert L.silu_fwd(None, _p(2 * F), _p(3 * F), 100, 1, s) == wsf.ERR_NULL_PTR
+    assert L.silu_fwd(_p(F), None, _p(3 * F), 100, 1, s) == wsf.ERR_NULL_PTR
+    assert L.silu_fwd(_p(F), _p(2 * F), _p(F + 10), 100, 1, s) == wsf.ERR_OVERLAP
+    assert L.silu_fwd(_p(F + 1), _p(2 * F), _p(3 * F), 100, 1, s) == wsf.ERR_MISALIGNED
+    assert L.silu_fwd(None, None, None, 0, 1, s) == wsf.OK
+    need = L.silu_bwd_workspace_bytes(100, 1)
+    ok = dict(dy=F, x=2 * F, w=3 * F, dx=4 * F, dw=5 * F, acc=0, ws=6 * F, wsb=need, n=100, dt=1)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        P = lambda v: _p(v) if v else None  # noqa: E731
+        return L.silu_bwd(P(a["dy"]), P(a["x"]), P(a["w"]), P(a["dx"]), P(a["dw"]), a["acc"],
+                          P(a["ws"]), a["wsb"], a["n"], a["dt"], s)
+
+    assert call(dt=-1) == wsf.ERR_BAD_DTYPE
+    assert call(n=-5) == wsf.ERR_BAD_SHAPE
+    assert call(acc=3) == wsf.ERR_BAD_ARG
+    for k in ["dy", "x", "w", "dx", "dw"]:
+        assert call(**{k: 0}) == wsf.ERR_NULL_PTR, k
+    assert call(ws=0) == wsf.ERR_WORKSPACE
+    assert call(wsb=need - 4) == wsf.ERR_WORKSPACE
+    assert call(dx=2 * F + 100) == wsf.ERR_OVERLAP
+    assert call(dw=6 * F + 8) == wsf.ERR_OVERLAP
+    assert call(x=2 * F + 1) == wsf.ERR_MISALIGNED
