@@ -23,6 +23,7 @@
 //    the grad_w partials.
 // No atomics anywhere: every sum has a fixed operand order.
 #include <algorithm>
+#include <type_traits>
 
 #include "wsf_device.cuh"
 #include "wsf_internal.h"
@@ -65,6 +66,13 @@ int64_t ws_tiles(int64_t N, int64_t D, int dtype, int64_t block_n) {
     if (p > cap) p = cap;
     return p < 1 ? 1 : p;
 }
+
+// The forward sums use compensated accumulation (Acc2) when the output is
+// binary32, whose stated tolerance (1e-6 relative) is below the error of a
+// plain binary32 sum of tens of thousands of terms; 16-bit outputs round far
+// above that error and use plain fp32 accumulation.
+template <typename T>
+constexpr bool kCompensated = std::is_same<T, float>::value;
 
 // Load the lane's CPL chunks of w (V fp32 values each) into registers.
 template <int LPR, int CPL, int V>
@@ -117,15 +125,28 @@ __global__ void __launch_bounds__(NT, MINB)
         float acc[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            float a = 0.f;
+            if constexpr (kCompensated<T>) {
+                Acc2 a = acc2_zero();
 #pragma unroll
-            for (int k = 0; k < CPL; k++) {
-                float f[V];
-                E::widen(xr[u][k], f);
+                for (int k = 0; k < CPL; k++) {
+                    float f[V];
+                    E::widen(xr[u][k], f);
 #pragma unroll
-                for (int v = 0; v < V; v++) a = fmaf(f[v], wr[k][v], a);
+                    for (int v = 0; v < V; v++) acc2_fma(a, f[v], wr[k][v]);
+                }
+                a = group_sum2<LPR>(a);
+                acc[u] = a.hi + a.lo;
+            } else {
+                float a = 0.f;
+#pragma unroll
+                for (int k = 0; k < CPL; k++) {
+                    float f[V];
+                    E::widen(xr[u][k], f);
+#pragma unroll
+                    for (int v = 0; v < V; v++) a = fmaf(f[v], wr[k][v], a);
+                }
+                acc[u] = group_sum<LPR>(a);
             }
-            acc[u] = group_sum<LPR>(a);
         }
         // every lane of a group holds all U row sums; lane l stores rows u = l, l+LPR, ...
         for (int u = l; u < U; u += LPR) {
@@ -142,12 +163,12 @@ __global__ void __launch_bounds__(NT)
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int NW = NT / 32;
-    __shared__ float red[NW][R];
+    __shared__ Acc2 red[NW][R];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int64_t r0 = (int64_t)blockIdx.x * R; r0 < N; r0 += (int64_t)gridDim.x * R) {
-        float acc[R];
+        Acc2 acc[R];  // lo stays 0 unless the storage type is binary32
 #pragma unroll
-        for (int r = 0; r < R; r++) acc[r] = 0.f;
+        for (int r = 0; r < R; r++) acc[r] = acc2_zero();
         for (int64_t c0 = threadIdx.x; c0 < Dv; c0 += (int64_t)NT * UJ) {
             Raw16 xr[UJ][R];
             float wv[UJ][V];
@@ -172,20 +193,30 @@ __global__ void __launch_bounds__(NT)
                     float f[V];
                     E::widen(xr[j][r], f);
 #pragma unroll
-                    for (int v = 0; v < V; v++) acc[r] = fmaf(f[v], wv[j][v], acc[r]);
+                    for (int v = 0; v < V; v++) {
+                        if constexpr (kCompensated<T>)
+                            acc2_fma(acc[r], f[v], wv[j][v]);
+                        else
+                            acc[r].hi = fmaf(f[v], wv[j][v], acc[r].hi);
+                    }
                 }
         }
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            const float s = group_sum<32>(acc[r]);
+            Acc2 s;
+            if constexpr (kCompensated<T>) {
+                s = group_sum2<32>(acc[r]);
+            } else {
+                s = Acc2{group_sum<32>(acc[r].hi), 0.f};
+            }
             if (lane == 0) red[wid][r] = s;
         }
         __syncthreads();
         if (threadIdx.x < R && r0 + threadIdx.x < N) {
-            float s = red[0][threadIdx.x];
+            Acc2 s = red[0][threadIdx.x];
 #pragma unroll
-            for (int q = 1; q < NW; q++) s += red[q][threadIdx.x];
-            E::store1(y + r0 + threadIdx.x, s);
+            for (int q = 1; q < NW; q++) s = acc2_add(s, red[q][threadIdx.x]);
+            E::store1(y + r0 + threadIdx.x, s.hi + s.lo);
         }
         __syncthreads();
     }
@@ -201,10 +232,21 @@ __global__ void __launch_bounds__(NT)
     const int64_t warp = ((int64_t)blockIdx.x * NT + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * NT) >> 5;
     for (int64_t row = warp; row < N; row += nwarps) {
-        float a = 0.f;
-        for (int64_t d = lane; d < D; d += 32) a = fmaf(E::load1(x + row * ldx + d), __ldg(w + d), a);
-        a = group_sum<32>(a);
-        if (lane == 0) E::store1(y + row, a);
+        Acc2 a = acc2_zero();
+        for (int64_t d = lane; d < D; d += 32) {
+            if constexpr (kCompensated<T>)
+                acc2_fma(a, E::load1(x + row * ldx + d), __ldg(w + d));
+            else
+                a.hi = fmaf(E::load1(x + row * ldx + d), __ldg(w + d), a.hi);
+        }
+        float v;
+        if constexpr (kCompensated<T>) {
+            a = group_sum2<32>(a);
+            v = a.hi + a.lo;
+        } else {
+            v = group_sum<32>(a.hi);
+        }
+        if (lane == 0) E::store1(y + row, v);
     }
 }
 

@@ -142,6 +142,53 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Compensated fp32 dot-product accumulation (the "Dot2" scheme of Ogita,
+// Rump and Oishi, "Accurate sum and dot product", SIAM J. Sci. Comput. 26,
+// 2005): each product is split exactly into p + ep with an FMA, each addition
+// into its rounded sum and exact error (Knuth's TwoSum); the errors are
+// collected in `lo`.  The result hi + lo is as accurate as if computed in
+// twice the working precision, then rounded.  Used where a binary32 output
+// must stay within 1e-6 of the exact sum over up to 65,536 terms.
+struct Acc2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ Acc2 acc2_zero() { return Acc2{0.f, 0.f}; }
+
+// The _rn intrinsics are never contracted into fused multiply-adds, which
+// would break the exactness of the splits.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+__device__ __forceinline__ void acc2_fma(Acc2& a, float x, float w) {
+    const float p = __fmul_rn(x, w);
+    const float ep = fmaf(x, w, -p);
+    float s, e;
+    two_sum(a.hi, p, s, e);
+    a.hi = s;
+    a.lo += e + ep;
+}
+
+__device__ __forceinline__ Acc2 acc2_add(Acc2 a, Acc2 b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    return Acc2{s, a.lo + b.lo + e};
+}
+
+template <int Width>
+__device__ __forceinline__ Acc2 group_sum2(Acc2 v) {
+#pragma unroll
+    for (int off = Width / 2; off > 0; off >>= 1) {
+        Acc2 o{__shfl_xor_sync(FULL_MASK, v.hi, off), __shfl_xor_sync(FULL_MASK, v.lo, off)};
+        v = acc2_add(v, o);
+    }
+    return v;
+}
+
 // Pick a[i] for a runtime i without dynamic register indexing.
 template <int K>
 __device__ __forceinline__ float select(const float (&a)[K], int i) {

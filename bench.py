@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark: forward + backward of the weighted sum and the scaled SiLU.
+
+One step is one pass of the whole hot path over the synthetic workloads:
+
+    silu_fwd(c2)  ws_fwd(c3) ws_fwd(c4) ws_fwd(c5)       forwards
+    ws_bwd(c5)    ws_bwd(c4) ws_bwd(c3) silu_bwd(c2)     backwards, reverse order
+
+(c2: scaled SiLU, fp16 x[8192,4096]; c3: bf16 x[1048576,1024];
+c4: fp16 x[16777216,64]; c5: fp32 x[4096,65536]).  Every input is larger
+than L2 or is separated from its reuse by gigabytes of other traffic, as in a
+real network where a layer's backward runs long after its forward.
+
+The metric is effective HBM bandwidth: the algorithmic bytes the method must
+move (fwd: read x and w, write y; bwd: read x, dy and w, write dx and the
+parameter gradient) divided by device time.  `value` is measured with CUDA
+events around K steps on resident inputs; `e2e` runs the same step through
+the public API with host buffers, the host<->device copies included.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+       [--workload all|c2|c3|c4|c5]
+Under torchrun each rank runs its own replica of the workload (weak scaling,
+no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd effective HBM GB/s and % of GB300 peak; elements/s per op"
+ORDER_FWD = ["c2", "c3", "c4", "c5"]
+ORDER_BWD = ["c5", "c4", "c3", "c2"]
+KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2}
+
+
+# ------------------------------------------------------------------ byte model
+def elt_size(dt: str) -> int:
+    return 4 if dt == "f32" else 2
+
+
+def op_bytes(wl, op: str, rows: int | None = None) -> int:
+    """Algorithmic bytes of one op on workload wl (optionally on `rows` rows)."""
+    N = wl.N if rows is None else rows
+    es = elt_size(wl.dtype)
+    if wl.op == "ws":
+        D = wl.D
+        if op == "fwd":
+            return N * D * es + D * 4 + N * es
+        return 2 * N * D * es + N * es + 2 * D * 4
+    n = N * wl.D
+    return 2 * n * es + 4 if op == "fwd" else 3 * n * es + 8
+
+
+def op_elems(wl, rows: int | None = None) -> int:
+    return (wl.N if rows is None else rows) * wl.D
+
+
+def steps_ops(names):
+    fwd = [(n, "fwd") for n in ORDER_FWD if n in names]
+    bwd = [(n, "bwd") for n in ORDER_BWD if n in names]
+    return fwd + bwd
+
+
+def op_name(wl, op):
+    return f"{wl.op}_{op}"
+
+
+# ------------------------------------------------------------------ helpers
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(v: float, device=None) -> float:
+    """Maximum of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU (oracle) leg
+def oracle_sample(names, frac: float):
+    """Host inputs for a bounded sample of each workload: the first
+    max(1, round(N·frac)) rows (for the scaled SiLU, rows of the [8192, 4096]
+    tensor)."""
+    import torch
+    import inputgen
+    from inputgen.workloads import WORKLOADS
+    samples = []
+    for n in names:
+        wl = WORKLOADS[n]
+        rows = max(1, int(round(wl.N * frac)))
+        x = inputgen.make((rows, wl.D), wl.dtype, wl.x.kind, wl.x.a, wl.x.b, 0, 0)
+        if wl.op == "ws":
+            w = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1)
+            dy = inputgen.make((rows,), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
+        else:
+            w = torch.tensor([wl.w_scalar], dtype=torch.float32)
+            dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
+        samples.append((wl, rows, x, w, dy))
+    return samples
+
+
+def oracle_step(samples):
+    import oracle
+    nbytes = 0
+    for wl, rows, x, w, dy in samples:
+        if wl.op == "ws":
+            oracle.ws_fwd(x, w)
+            oracle.ws_bwd(x, w, dy)
+        else:
+            oracle.silu_fwd(x.reshape(-1), wl.w_scalar)
+            oracle.silu_bwd(dy.reshape(-1), x.reshape(-1), wl.w_scalar)
+        nbytes += op_bytes(wl, "fwd", rows) + op_bytes(wl, "bwd", rows)
+    return nbytes
+
+
+def sample_desc(samples):
+    return ", ".join(f"{wl.name}: first {rows} of {wl.N} rows" for wl, rows, *_ in samples)
+
+
+def calibrated_fraction(names, budget_s: float, max_frac: float = 1 / 16):
+    """Largest row fraction (<= max_frac) whose oracle step takes about budget_s."""
+    f0 = 1 / 4096
+    s = oracle_sample(names, f0)
+    t = time.perf_counter()
+    oracle_step(s)
+    dt = max(time.perf_counter() - t, 1e-4)
+    return max(f0, min(max_frac, f0 * budget_s / dt))
+
+
+def cpu_baseline(names):
+    import oracle
+    oracle.build()
+    frac = calibrated_fraction(names, budget_s=10.0)
+    samples = oracle_sample(names, frac)
+    t = time.perf_counter()
+    nbytes = oracle_step(samples)
+    dt = time.perf_counter() - t
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": sample_desc(samples) + f"; {dt:.1f} s of single-threaded fp64 CPU work"}
+
+
+def run_reference(args, names):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    frac = calibrated_fraction(names, budget_s=budget)
+    samples = oracle_sample(names, frac)
+    for _ in range(args.warmup):
+        oracle_step(samples)
+    nbytes = 0
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        nbytes += oracle_step(samples)
+    dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": workload_label(names), "reference": "fp64 CPU oracle"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample_desc(samples)},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_label(names):
+    return ("weighted sum " + "+".join(n for n in ["c3", "c4", "c5"] if n in names) +
+            (" and " if "c2" in names and len(names) > 1 else "") +
+            ("scaled-SiLU c2" if "c2" in names else "") + ", fwd+bwd")
+
+
+# ------------------------------------------------------------------ GPU leg
+class Buffers:
+    """Device tensors of one workload (inputs resident, outputs, workspace)
+    plus, for e2e, pinned host copies of inputs and outputs."""
+
+    def __init__(self, wl, dev, wsf, host_io: bool):
+        import torch
+        import inputgen
+        self.wl = wl
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+        shape = (wl.N, wl.D)
+        self.hx = inputgen.make(shape, wl.dtype, wl.x.kind, wl.x.a, wl.x.b, 0, 0, pin=host_io)
+        if wl.op == "ws":
+            self.hw = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1, pin=host_io)
+            self.hdy = inputgen.make((wl.N,), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
+                                     pin=host_io)
+        else:
+            self.hw = torch.tensor([wl.w_scalar], dtype=torch.float32)
+            if host_io:
+                self.hw = self.hw.pin_memory()
+            self.hdy = inputgen.make(shape, wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
+                                     pin=host_io)
+        self.x = self.hx.to(dev)
+        self.w = self.hw.to(dev)
+        self.dy = self.hdy.to(dev)
+        if wl.op == "ws":
+            self.y = torch.empty(wl.N, dtype=tdt, device=dev)
+            self.gw = torch.empty(wl.D, dtype=torch.float32, device=dev)
+            nbytes = wsf.ws_bwd_workspace_bytes(wl.N, wl.D, tdt, 0)
+        else:
+            self.y = torch.empty(shape, dtype=tdt, device=dev)
+            self.gw = torch.empty(1, dtype=torch.float32, device=dev)
+            nbytes = wsf.silu_bwd_workspace_bytes(wl.N * wl.D, tdt)
+        self.dx = torch.empty(shape, dtype=tdt, device=dev)
+        self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        if host_io:
+            self.hy = torch.empty(self.y.shape, dtype=tdt, pin_memory=True)
+            self.hdx = torch.empty(shape, dtype=tdt, pin_memory=True)
+            self.hgw = torch.empty(self.gw.shape, dtype=torch.float32, pin_memory=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.hx, self.hw, self.hdy))
+
+    def d2h_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.y, self.dx, self.gw))
+
+    def run(self, wsf, op):
+        if self.wl.op == "ws":
+            if op == "fwd":
+                wsf.ws_fwd(self.x, self.w, y=self.y)
+            else:
+                wsf.ws_bwd(self.x, self.w, self.dy, dx=self.dx, grad_w=self.gw,
+                           workspace=self.ws)
+        else:
+            if op == "fwd":
+                wsf.silu_fwd(self.x, self.w, y=self.y)
+            else:
+                wsf.silu_bwd(self.dy, self.x, self.w, dx=self.dx, dw=self.gw, workspace=self.ws)
+
+
+def run_cuda(args, names):
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import backward_ws_fwd_gb300 as wsf
+    from inputgen.workloads import WORKLOADS
+
+    host_io = not args.no_e2e
+    bufs = {n: Buffers(WORKLOADS[n], dev, wsf, host_io) for n in names}
+    ops = steps_ops(names)
+    step_bytes = sum(op_bytes(WORKLOADS[n], op) for n, op in ops)
+    launches_per_step = sum(KERNELS_PER_OP[op_name(WORKLOADS[n], op)] for n, op in ops)
+
+    def step():
+        for n, op in ops:
+            bufs[n].run(wsf, op)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-op events on the launching (current) stream
+    stream = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+           for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = Clocks(uuid or str(local))
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        e = evs[k]
+        e[0].record(stream)
+        for j, (n, op) in enumerate(ops):
+            bufs[n].run(wsf, op)
+            e[j + 1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    per_op_ms = [sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)) / args.steps
+                 for j in range(len(ops))]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if host_io:
+        e2e_steps = max(1, min(args.steps, 10))
+
+        def e2e_step():
+            for n in names:
+                b = bufs[n]
+                b.x.copy_(b.hx, non_blocking=True)
+                b.w.copy_(b.hw, non_blocking=True)
+                b.dy.copy_(b.hdy, non_blocking=True)
+            step()
+            for n in names:
+                b = bufs[n]
+                b.hy.copy_(b.y, non_blocking=True)
+                b.hdx.copy_(b.dx, non_blocking=True)
+                b.hgw.copy_(b.gw, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b_), dev) / e2e_steps
+        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": sum(bufs[n].h2d_bytes() for n in names),
+               "d2h_bytes_per_step": sum(bufs[n].d2h_bytes() for n in names),
+               "ms_per_step": round(e2e_ms, 3)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = read_peaks()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    per_op = {}
+    for (n, op), ms in zip(ops, per_op_ms):
+        wl = WORKLOADS[n]
+        b = op_bytes(wl, op)
+        per_op[f"{n}.{op}"] = {"ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                               "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                               "elements_per_s": round(op_elems(wl) / (ms * 1e-3), 1)}
+    for n in names:
+        wl = WORKLOADS[n]
+        ms = per_op[f"{n}.fwd"]["ms"] + per_op[f"{n}.bwd"]["ms"]
+        b = op_bytes(wl, "fwd") + op_bytes(wl, "bwd")
+        per_op[f"{n}.fwd+bwd"] = {"ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                                  "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                                  "frac_of_8TBs": round(b / (ms * 1e-3) / 1e9 / 8000.0, 4)}
+    # dominant op: the largest share of the step
+    j = max(range(len(ops)), key=lambda i: per_op_ms[i])
+    dn, dop = ops[j]
+    dwl = WORKLOADS[dn]
+    dbytes = op_bytes(dwl, dop)
+    achieved = dbytes / (per_op_ms[j] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"{op_name(dwl, dop)} ({dn})",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": read_traffic(op_name(dwl, dop), dn),
+                "algorithmic_bytes_per_launch": dbytes,
+                "note": "achieved = algorithmic bytes / mean CUDA-event time of the op "
+                        f"({KERNELS_PER_OP[op_name(dwl, dop)]} kernel(s)) in the timed region"}
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64/Box-Muller, BASELINE workload recipes)"
+                    .replace("BASELINE ", ""),
+            "config": {"workload": workload_label(names),
+                       "step": [f"{n}.{op}" for n, op in ops],
+                       "bytes_per_step": step_bytes,
+                       "frac_of_peak": round(value / world / peak, 4),
+                       "frac_of_8TBs": round(value / world / 8000.0, 4),
+                       "l2": "inputs larger than L2; each fwd and its bwd are separated by "
+                             ">= 1 GB of other traffic"},
+            "roofline": roofline, "per_op": per_op, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(names)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch measured by ncu for this kernel and workload,
+    from profiles/traffic.json, if a capture of the current source exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(f"{kernel}:{workload}")
+        if e and e.get("source_hash") == source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "backward_ws_fwd_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default="all", help="all or a comma list of c2,c3,c4,c5")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    names = ORDER_FWD if args.workload == "all" else [s.strip() for s in args.workload.split(",")]
+    assert all(n in ORDER_FWD for n in names), names
+    if args.warmup < 3 and args.impl == "cuda":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, names)
+    return run_cuda(args, names)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

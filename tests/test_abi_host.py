@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def wsf():
-    from backward_ws_fwd_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._cuda_build_module().build()
     import backward_ws_fwd_gb300 as m
     return m
 
