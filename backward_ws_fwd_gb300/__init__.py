@@ -39,6 +39,9 @@ lib.ws_bwd_workspace_bytes.restype = _sz
 lib.ws_bwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _vp, _sz, _i64, _i64, _i64,
                        _int, _vp]
 lib.ws_bwd.restype = _int
+lib.ws_bwd_noalloc.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _i64, _i64, _i64, _int,
+                               _vp]
+lib.ws_bwd_noalloc.restype = _int
 lib.silu_fwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
 lib.silu_fwd.restype = _int
 lib.silu_bwd_workspace_bytes.argtypes = [_i64, _int]
@@ -135,6 +138,23 @@ def ws_bwd(x, w, dy, dx=None, grad_w=None, accumulate=False, workspace=None, blo
     return dx, grad_w
 
 
+def ws_bwd_noalloc(x, w, dy, dx=None, grad_w=None, accumulate=False, block_n=0, stream=None):
+    """ws_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the partials use the library's fixed 4 MiB scratch array
+    (sizes that need more are rejected).  dx and grad_w must be supplied by
+    such callers; they are allocated here only for convenience when None."""
+    import torch
+    N, D = x.shape
+    if dx is None:
+        dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    if grad_w is None:
+        grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
+    _check(lib.ws_bwd_noalloc(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
+                              _ptr(grad_w), int(bool(accumulate)), block_n, N, D, _dtype_code(x),
+                              _stream(stream)), "ws_bwd_noalloc")
+    return dx, grad_w
+
+
 def silu_fwd(x, w, y=None, stream=None):
     """y = w·x·sigmoid(x).  x contiguous (any shape); w: one float32 on the device."""
     import torch
@@ -166,5 +186,6 @@ def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, strea
     return dx, dw
 
 
-__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "silu_fwd",
+__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
+           "silu_fwd",
            "silu_bwd", "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "F32", "F16", "BF16"]

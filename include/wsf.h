@@ -123,6 +123,32 @@ int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
            int64_t block_n, int64_t N, int64_t D, int dtype, wsf_stream_t stream);
 
 /*
+ * ws_bwd_noalloc — ws_bwd for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that are handed only their input and output buffers, such as a plugin in a
+ * host program that owns all device memory through its own pool, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.  Same arguments, results and errors as ws_bwd, minus the
+ * workspace: the per-tile partials go to a scratch array of
+ * WSF_NOALLOC_SCRATCH_BYTES (4 MiB) that lives in the library's own device
+ * memory, one copy per device that loads the library, held until the
+ * process exits.  The call allocates nothing.
+ *   - Sizes whose ws_bwd_workspace_bytes(N, D, dtype, block_n) exceeds
+ *     WSF_NOALLOC_SCRATCH_BYTES are rejected with WSF_ERR_WORKSPACE before
+ *     anything is enqueued (the five benchmark workloads need at most 2.4 MiB).
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents;
+ *     nothing in it needs clearing, but calls whose kernels overlap on the
+ *     GPU (e.g. issued on two streams) race on it: serialise them.
+ */
+#define WSF_NOALLOC_SCRATCH_BYTES (4u << 20)
+int ws_bwd_noalloc(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                   int64_t lddx, float* grad_w, int accumulate, int64_t block_n, int64_t N,
+                   int64_t D, int dtype, wsf_stream_t stream);
+
+/*
  * silu_fwd — scaled-SiLU forward  [SILU, forward kernel]
  *   s = 1 / (1 + exp(-x)),  y = w · x · s       elementwise over n elements
  * x, y: [n] dtype (contiguous); w: one binary32 value in device memory.

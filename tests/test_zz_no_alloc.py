@@ -1,0 +1,106 @@
+"""ws_bwd_noalloc — the weighted-sum backward for callers that cannot
+allocate device memory (a plugin whose host program owns every byte of device
+memory through its own pool, or a loop that cannot afford cudaMalloc's
+implicit synchronisation).  It keeps its per-tile partials in the library's
+fixed 4 MiB device scratch array instead of a caller workspace.
+
+Checked through the C ABI against the existing ws_bwd entry point, within the
+tolerances the parity tests use, on two calls in a row with different
+workloads (the second call finds the first call's partials still in the
+shared array), and for the rejection of sizes that need more scratch than the
+array holds.  Collected last so that a run stopping at the first failure has
+run every other test first; it also passes alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tolerance import GRAD_TOL, check_elementwise, check_reduction
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+@pytest.fixture(scope="module")
+def wsf():
+    import __graft_entry__
+    __graft_entry__.build()
+    import backward_ws_fwd_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _inputs(N, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((N, D), generator=g).to(dtype)
+    w = (torch.randn(D, generator=g) / D ** 0.5).float()
+    dy = torch.randn(N, generator=g).to(dtype)
+    return x, w, dy
+
+
+def _existing(wsf, xd, wd, dyd, N, D, dt, stream):
+    need = wsf.lib.ws_bwd_workspace_bytes(N, D, dt, 0)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=DEV)
+    dx = torch.empty((N, D), dtype=xd.dtype, device=DEV)
+    gw = torch.empty(D, dtype=torch.float32, device=DEV)
+    rc = wsf.lib.ws_bwd(_p(xd), D, _p(wd), _p(dyd), _p(dx), D, _p(gw), 0, _p(ws), need, 0, N, D,
+                        dt, stream)
+    assert rc == 0, wsf.status_string(rc)
+    return dx, gw
+
+
+def _noalloc(wsf, xd, wd, dyd, N, D, dt, stream):
+    dx = torch.empty((N, D), dtype=xd.dtype, device=DEV)
+    gw = torch.empty(D, dtype=torch.float32, device=DEV)
+    rc = wsf.lib.ws_bwd_noalloc(_p(xd), D, _p(wd), _p(dyd), _p(dx), D, _p(gw), 0, 0, N, D, dt,
+                                stream)
+    assert rc == 0, wsf.status_string(rc)
+    return dx, gw
+
+
+def test_noalloc_matches_ws_bwd_two_calls(wsf):
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # two calls in a row on different workloads: bf16 rows of 1024, then
+    # fp16 tall-skinny rows of 64 (both use the shared scratch array)
+    for N, D, dtype, seed in [(5003, 1024, torch.bfloat16, 1), (70001, 64, torch.float16, 2)]:
+        x, w, dy = _inputs(N, D, dtype, seed)
+        xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+        dt = CODE[dtype]
+        dx_ref, gw_ref = _existing(wsf, xd, wd, dyd, N, D, dt, stream)
+        dx, gw = _noalloc(wsf, xd, wd, dyd, N, D, dt, stream)
+        torch.cuda.synchronize()
+        res = check_elementwise(dx.cpu(), dx_ref.cpu(), dx_ref.cpu().double().numpy())
+        assert res, ("dx", res)
+        S = oracle.ws_bwd(x, w, dy, want_dx=False)["grad_w_abs"]
+        res = check_reduction(gw.cpu(), gw_ref.cpu().double().numpy(), S, N, GRAD_TOL)
+        assert res, ("grad_w", res)
+
+
+def test_noalloc_rejects_sizes_beyond_scratch(wsf):
+    """2048 one-row tiles of 1024 fp32 columns need 8 MiB of partials: more
+    than the 4 MiB array, so the call is refused before anything runs."""
+    N, D = 2048, 1024
+    assert wsf.lib.ws_bwd_workspace_bytes(N, D, 0, 1) > 4 << 20
+    x = torch.zeros((N, D), device=DEV)
+    w = torch.zeros(D, device=DEV)
+    dy = torch.zeros(N, device=DEV)
+    dx = torch.full((N, D), 7.0, device=DEV)
+    gw = torch.full((D,), 7.0, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = wsf.lib.ws_bwd_noalloc(_p(x), D, _p(w), _p(dy), _p(dx), D, _p(gw), 0, 1, N, D, 0, stream)
+    assert rc == wsf.ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((dx == 7.0).all()) and bool((gw == 7.0).all())  # nothing was enqueued
+    # the same sizes with the library's own tiling fit and run
+    rc = wsf.lib.ws_bwd_noalloc(_p(x), D, _p(w), _p(dy), _p(dx), D, _p(gw), 0, 0, N, D, 0, stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert bool((dx == 0).all()) and bool((gw == 0).all())
