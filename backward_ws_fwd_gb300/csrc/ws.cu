@@ -14,16 +14,25 @@
 //    columns and holding their weights in registers; a warp covers 32/LPR
 //    rows per load instruction with U rows per lane in flight; row sums use
 //    an xor butterfly inside the LPR-lane group.
-//  * forward, wide path (rows > 4 KB): a CTA owns R rows and walks the
-//    columns, reusing each w chunk (an L2 hit) for the R rows.
-//  * backward, tile path (16-byte aligned): a 2-D grid of (column slice x row
-//    tile); each thread owns one 16-byte column chunk (its V weights and V
-//    grad_w accumulators in registers) and walks its share of the tile's rows.
+//  * forward, wide path (rows > 4 KB): one CTA per row walks its columns;
+//    the w chunks come from L2.
+//  * backward, staged path (16-byte aligned): a 2-D grid of (row tile x
+//    column slice); each thread owns one 16-byte column chunk (its V weights
+//    and V grad_w accumulators in registers) and walks its share of the
+//    tile's rows.  x is staged S steps ahead into shared memory with
+//    cp.async — each thread copies and later reads only its own chunks — and
+//    each step's slice of dy is staged the same way by a few threads.  The
+//    bytes in flight are then bounded by shared memory, not registers.
+//  * backward, tile path: the same thread layout with register-held loads,
+//    for aligned x/dx whose dy or tile starts are not 16-byte aligned.
 //  * scalar paths (any alignment, any D): element-wise loads, same tiling of
 //    the grad_w partials.
 // No atomics anywhere: every sum has a fixed operand order.
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "wsf_device.cuh"
 #include "wsf_internal.h"
@@ -31,46 +40,47 @@
 namespace wsf {
 
 // Rows [a, b) of row tile p.  block_n > 0 gives tiles of block_n rows (the
-// last one ragged); otherwise the N rows are split into P near-equal tiles.
+// last one ragged).  Otherwise the N rows are split into P near-equal tiles
+// whose boundaries are multiples of 8 rows (the last tile ends at N), so that
+// every tile's slice of dy starts on a 16-byte boundary.
 __host__ __device__ __forceinline__ void tile_rows(int64_t p, int64_t P, int64_t N,
                                                    int64_t block_n, int64_t& a, int64_t& b) {
     if (block_n > 0) {
         a = p * block_n;
         b = (a + block_n < N) ? a + block_n : N;
     } else {
-        a = (p * N) / P;
-        b = ((p + 1) * N) / P;
+        a = ((p * N) / P) & ~(int64_t)7;
+        b = (p + 1 == P) ? N : ((((p + 1) * N) / P) & ~(int64_t)7);
     }
 }
 
 // ---------------------------------------------------------------------------
 // Tiling constants (chosen for 152 SMs; all are compile-time, so the
 // reduction order depends on nothing but the sizes).
-constexpr int kRegMaxChunks = 256;       // forward register path: rows of <= 256 x 16 B
-constexpr int kTileThreads = 256;        // backward tile kernel: threads per CTA
-constexpr int kTileMinBlocks = 4;        // ... and CTAs resident per SM
-constexpr int64_t kTileSlots = kTileMinBlocks * kDesignSMs;  // 608: one full wave
+constexpr int kRegMaxChunks = 256;        // forward register path: rows of <= 256 x 16 B
+constexpr int kSliceChunks = 256;         // backward: 16-byte chunks per column slice
+constexpr int64_t kTileSlots = 6 * kDesignSMs;  // 912 CTAs per backward launch at most
 constexpr int64_t kRowsPerTileMin = 64;
 
 // P = number of row tiles.  A row of D elements is cut into column slices of
-// kTileThreads 16-byte chunks; P is the largest tile count that keeps
-// slices x P within one wave of kTileSlots CTAs, at least kRowsPerTileMin
-// rows per tile, and at least 1.
+// kSliceChunks 16-byte chunks; P is the largest tile count that keeps
+// slices x P within kTileSlots CTAs, at least kRowsPerTileMin rows per tile,
+// and at least 1.
 int64_t ws_tiles(int64_t N, int64_t D, int dtype, int64_t block_n) {
     if (N <= 0 || D <= 0) return 0;
     if (block_n > 0) return (N + block_n - 1) / block_n;
     const int64_t chunks = (D * elt_bytes(dtype) + 15) / 16;
-    const int64_t slices = (chunks + kTileThreads - 1) / kTileThreads;
+    const int64_t slices = (chunks + kSliceChunks - 1) / kSliceChunks;
     int64_t p = (N + kRowsPerTileMin - 1) / kRowsPerTileMin;
     const int64_t cap = kTileSlots / slices;
     if (p > cap) p = cap;
     return p < 1 ? 1 : p;
 }
 
-// The forward sums use compensated accumulation (Acc2) when the output is
-// binary32, whose stated tolerance (1e-6 relative) is below the error of a
-// plain binary32 sum of tens of thousands of terms; 16-bit outputs round far
-// above that error and use plain fp32 accumulation.
+// The forward sums use compensated accumulation when the output is binary32,
+// whose stated tolerance (1e-6 relative) is below the error of a plain
+// binary32 sum of tens of thousands of terms; 16-bit outputs round far above
+// that error and use plain fp32 accumulation.
 template <typename T>
 constexpr bool kCompensated = std::is_same<T, float>::value;
 
@@ -156,67 +166,68 @@ __global__ void __launch_bounds__(NT, MINB)
     }
 }
 
-template <typename T, int R, int UJ, int NT>
+// Wide rows: one CTA per row (grid-stride over rows).  Each thread sums the
+// products of its chunks c0, c0 + NT, ... in order; for binary32 outputs the
+// running sum is compensated (Kahan: the rounding error of every addition is
+// carried in a second register), then the threads are combined with
+// double-float additions (xor butterfly in each warp, warps in index order).
+template <typename T, int UJ, int NT>
 __global__ void __launch_bounds__(NT)
     ws_fwd_wide(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                 T* __restrict__ y, int64_t N, int64_t Dv) {
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int NW = NT / 32;
-    __shared__ Acc2 red[NW][R];
+    __shared__ Acc2 red[NW];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int64_t r0 = (int64_t)blockIdx.x * R; r0 < N; r0 += (int64_t)gridDim.x * R) {
-        Acc2 acc[R];  // lo stays 0 unless the storage type is binary32
-#pragma unroll
-        for (int r = 0; r < R; r++) acc[r] = acc2_zero();
+    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+        const T* xrow = x + row * ldx;
+        float s = 0.f, comp = 0.f;
         for (int64_t c0 = threadIdx.x; c0 < Dv; c0 += (int64_t)NT * UJ) {
-            Raw16 xr[UJ][R];
+            Raw16 xr[UJ];
             float wv[UJ][V];
 #pragma unroll
             for (int j = 0; j < UJ; j++) {
                 const int64_t c = c0 + (int64_t)j * NT;
+                const bool ok = c < Dv;
 #pragma unroll
                 for (int q = 0; q < V / 4; q++) {
-                    Raw16 rw = (c < Dv) ? ld_keep(w + c * V + 4 * q) : raw_zero();
+                    Raw16 rw = ok ? ld_keep(w + c * V + 4 * q) : raw_zero();
 #pragma unroll
                     for (int i = 0; i < 4; i++) wv[j][4 * q + i] = __uint_as_float(rw.u[i]);
                 }
-#pragma unroll
-                for (int r = 0; r < R; r++)
-                    xr[j][r] = (c < Dv && r0 + r < N) ? ld_stream(x + (r0 + r) * ldx + c * V)
-                                                      : raw_zero();
+                xr[j] = ok ? ld_stream(xrow + c * V) : raw_zero();
             }
 #pragma unroll
-            for (int j = 0; j < UJ; j++)
+            for (int j = 0; j < UJ; j++) {
+                float f[V];
+                E::widen(xr[j], f);
 #pragma unroll
-                for (int r = 0; r < R; r++) {
-                    float f[V];
-                    E::widen(xr[j][r], f);
-#pragma unroll
-                    for (int v = 0; v < V; v++) {
-                        if constexpr (kCompensated<T>)
-                            acc2_fma(acc[r], f[v], wv[j][v]);
-                        else
-                            acc[r].hi = fmaf(f[v], wv[j][v], acc[r].hi);
+                for (int v = 0; v < V; v++) {
+                    if constexpr (kCompensated<T>) {
+                        const float yk = __fsub_rn(__fmul_rn(f[v], wv[j][v]), comp);
+                        const float t = __fadd_rn(s, yk);
+                        comp = __fsub_rn(__fsub_rn(t, s), yk);
+                        s = t;
+                    } else {
+                        s = fmaf(f[v], wv[j][v], s);
                     }
                 }
-        }
-#pragma unroll
-        for (int r = 0; r < R; r++) {
-            Acc2 s;
-            if constexpr (kCompensated<T>) {
-                s = group_sum2<32>(acc[r]);
-            } else {
-                s = Acc2{group_sum<32>(acc[r].hi), 0.f};
             }
-            if (lane == 0) red[wid][r] = s;
         }
+        Acc2 a{s, -comp};
+        if constexpr (kCompensated<T>) {
+            a = group_sum2<32>(a);
+        } else {
+            a.hi = group_sum<32>(a.hi);
+        }
+        if (lane == 0) red[wid] = a;
         __syncthreads();
-        if (threadIdx.x < R && r0 + threadIdx.x < N) {
-            Acc2 s = red[0][threadIdx.x];
+        if (threadIdx.x == 0) {
+            Acc2 t = red[0];
 #pragma unroll
-            for (int q = 1; q < NW; q++) s = acc2_add(s, red[q][threadIdx.x]);
-            E::store1(y + r0 + threadIdx.x, s.hi + s.lo);
+            for (int q = 1; q < NW; q++) t = acc2_add(t, red[q]);
+            E::store1(y + row, t.hi + t.lo);
         }
         __syncthreads();
     }
@@ -254,15 +265,141 @@ __global__ void __launch_bounds__(NT)
 // Backward, stage 1: dx and the per-tile partial rows of grad_w
 // ===========================================================================
 
-// Vector path.  blockIdx.x = row tile p; column slices of LPRC 16-byte
-// chunks are taken by blockIdx.y, blockIdx.y + gridDim.y, ...  The CTA's NT threads form G = NT / LPRC row groups of
-// LPRC threads; thread (g, l) owns chunk c = slice·LPRC + l (V columns) and
-// handles rows ra + g, ra + g + G, ... of the tile, U of them in flight, in
-// ascending order.  It keeps V weights and V accumulators in registers.  At
-// the end the G row groups are added in index order through shared memory.
-// Rows of up to NT chunks (4 KB) fit one slice; wider rows use several.
+// Write the CTA's partial row for columns [slice·LPRC·V, ...): G == 1 writes
+// each thread's V sums directly; otherwise the G row groups are added in
+// index order through shared memory `red` (G·LPRC·V floats).
+template <int LPRC, int G, int V, int NT>
+__device__ __forceinline__ void write_partial(const float (&acc)[V], float* __restrict__ out,
+                                              int g, int l, bool cok, int64_t ncols,
+                                              float* red) {
+    if constexpr (G == 1) {
+        if (cok) {
+#pragma unroll
+            for (int q = 0; q < V / 4; q++) {
+                Raw16 r;
+#pragma unroll
+                for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(acc[4 * q + i]);
+                *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = r;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; v++) red[(g * LPRC + l) * V + v] = acc[v];
+        __syncthreads();
+        for (int j = threadIdx.x; j < ncols; j += NT) {
+            float s = red[j];
+#pragma unroll
+            for (int q = 1; q < G; q++) s += red[q * LPRC * V + j];
+            out[j] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// Staged path.  blockIdx.x = row tile p, blockIdx.y = column slice.  The
+// CTA's NT threads form G = NT / LPRC row groups of LPRC threads; thread
+// (g, l) owns chunk c = slice·LPRC + l (V columns).  Step k covers rows
+// ra + k·SR .. ra + (k+1)·SR - 1 (SR = G·U); thread (g, l) handles rows
+// ra + k·SR + u·G + g, u < U.  Its x chunks for step k + S - 1 are copied
+// into its own shared slots while it computes step k; the step's dy slice
+// (SR values, 16-byte aligned) is copied in 16-byte pieces by the first
+// threads, so each step starts with a CTA barrier.
+template <typename T, int LPRC, int U, int S, int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+    ws_bwd_staged(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                  const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
+                  float* __restrict__ partial, int64_t N, int64_t Dv, int64_t D,
+                  int64_t block_n, int64_t P) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    constexpr int G = NT / LPRC;
+    constexpr int SR = G * U;                 // rows per step
+    constexpr int DYB = SR * (int)sizeof(T);  // dy bytes per step
+    static_assert(DYB % 16 == 0, "dy step must be whole 16-byte copies");
+    extern __shared__ __align__(16) unsigned char smem[];
+    Raw16* xs = reinterpret_cast<Raw16*>(smem);                                // [S][U][NT]
+    T* dys = reinterpret_cast<T*>(smem + (size_t)S * U * NT * sizeof(Raw16));  // [S][SR]
+
+    const int tid = threadIdx.x;
+    const int g = tid / LPRC, l = tid % LPRC;
+    int64_t ra, rb;
+    tile_rows(blockIdx.x, P, N, block_n, ra, rb);
+    const int64_t c = (int64_t)blockIdx.y * LPRC + l;
+    const bool cok = c < Dv;
+
+    float wv[V];
+#pragma unroll
+    for (int q = 0; q < V / 4; q++) {
+        Raw16 r = cok ? ld_keep(w + c * V + 4 * q) : raw_zero();
+#pragma unroll
+        for (int i = 0; i < 4; i++) wv[4 * q + i] = __uint_as_float(r.u[i]);
+    }
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; v++) acc[v] = 0.f;
+
+    const int64_t nsteps = (rb - ra + SR - 1) / SR;
+    auto issue = [&](int64_t k) {
+        if (k < nsteps) {
+            const int slot = (int)(k % S);
+            const int64_t r0 = ra + k * SR;
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t row = r0 + u * G + g;
+                const bool ok = row < rb && cok;
+                cp_async16(&xs[(slot * U + u) * NT + tid],
+                           ok ? (const void*)(x + row * ldx + c * V) : (const void*)x, ok ? 16 : 0);
+            }
+            for (int j = tid; j < DYB / 16; j += NT) {
+                const int64_t first = r0 + j * (16 / (int)sizeof(T));
+                const int64_t rem = (N - first) * (int64_t)sizeof(T);
+                const int bytes = rem >= 16 ? 16 : (rem > 0 ? (int)rem : 0);
+                cp_async16(reinterpret_cast<unsigned char*>(dys) + slot * DYB + j * 16,
+                           bytes > 0 ? (const void*)(dy + first) : (const void*)dy, bytes);
+            }
+        }
+        cp_async_commit();  // empty groups past the end keep the group count uniform
+    };
+
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) issue(k);
+    for (int64_t k = 0; k < nsteps; k++) {
+        cp_async_wait<S - 2>();  // this thread's copies for step k have landed
+        __syncthreads();         // ... and every thread's (dy), and step k-1 is consumed
+        issue(k + S - 1);        // refills the slot of step k-1
+        const int slot = (int)(k % S);
+        const int64_t r0 = ra + k * SR;
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t row = r0 + u * G + g;
+            const bool ok = row < rb;
+            const float gv = ok ? E::widen1(dys[slot * SR + u * G + g]) : 0.f;
+            const Raw16 xr = xs[(slot * U + u) * NT + tid];
+            if (ok && cok) {
+                float f[V];
+#pragma unroll
+                for (int v = 0; v < V; v++) f[v] = gv * wv[v];
+                st_stream(dx + row * lddx + c * V, E::narrow(f));
+            }
+            float f[V];
+            E::widen(xr, f);
+#pragma unroll
+            for (int v = 0; v < V; v++) acc[v] = fmaf(f[v], gv, acc[v]);
+        }
+    }
+    cp_async_wait<0>();  // no copy may still target shared memory when the CTA ends
+    __syncthreads();
+    const int64_t col0 = (int64_t)blockIdx.y * LPRC * V;
+    const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
+    write_partial<LPRC, G, V, NT>(acc, partial + (int64_t)blockIdx.x * D + col0, g, l, cok, ncols,
+                                  reinterpret_cast<float*>(smem));
+}
+
+// Tile path: the staged kernel's thread layout with register-held loads (U
+// rows in flight per thread); column slices are taken by blockIdx.y,
+// blockIdx.y + gridDim.y, ...
 template <typename T, int LPRC, int U, int NT>
-__global__ void __launch_bounds__(NT, kTileMinBlocks)
+__global__ void __launch_bounds__(NT)
     ws_bwd_tile(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                 const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
                 float* __restrict__ partial, int64_t N, int64_t Dv, int64_t D, int64_t block_n,
@@ -270,6 +407,7 @@ __global__ void __launch_bounds__(NT, kTileMinBlocks)
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int G = NT / LPRC;
+    __shared__ float red[G > 1 ? G * LPRC * V : 1];
     const int g = threadIdx.x / LPRC, l = threadIdx.x % LPRC;
     int64_t ra, rb;
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
@@ -277,71 +415,46 @@ __global__ void __launch_bounds__(NT, kTileMinBlocks)
     for (int64_t slice = blockIdx.y; slice < nslices; slice += gridDim.y) {
         const int64_t c = slice * LPRC + l;
         const bool cok = c < Dv;
-
         float wv[V];
-    #pragma unroll
+#pragma unroll
         for (int q = 0; q < V / 4; q++) {
             Raw16 r = cok ? ld_keep(w + c * V + 4 * q) : raw_zero();
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < 4; i++) wv[4 * q + i] = __uint_as_float(r.u[i]);
         }
         float acc[V];
-    #pragma unroll
+#pragma unroll
         for (int v = 0; v < V; v++) acc[v] = 0.f;
-
         for (int64_t base = ra + g; base < rb; base += (int64_t)G * U) {
             Raw16 xr[U];
             float gv[U];
-    #pragma unroll
+#pragma unroll
             for (int u = 0; u < U; u++) {
                 const int64_t row = base + (int64_t)u * G;
                 const bool ok = row < rb;
                 gv[u] = ok ? E::load1(dy + row) : 0.f;
                 xr[u] = (ok && cok) ? ld_stream(x + row * ldx + c * V) : raw_zero();
             }
-    #pragma unroll
+#pragma unroll
             for (int u = 0; u < U; u++) {
                 const int64_t row = base + (int64_t)u * G;
                 if (row < rb && cok) {
                     float f[V];
-    #pragma unroll
+#pragma unroll
                     for (int v = 0; v < V; v++) f[v] = gv[u] * wv[v];
                     st_stream(dx + row * lddx + c * V, E::narrow(f));
                 }
                 float f[V];
                 E::widen(xr[u], f);
-    #pragma unroll
+#pragma unroll
                 for (int v = 0; v < V; v++) acc[v] = fmaf(f[v], gv[u], acc[v]);
             }
         }
-
-        float* out = partial + (int64_t)blockIdx.x * D + slice * LPRC * V;
-        if constexpr (G == 1) {
-            if (cok) {
-    #pragma unroll
-                for (int q = 0; q < V / 4; q++) {
-                    Raw16 r;
-    #pragma unroll
-                    for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(acc[4 * q + i]);
-                    *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = r;
-                }
-            }
-        } else {
-            __shared__ float red[G][LPRC * V];
-    #pragma unroll
-            for (int v = 0; v < V; v++) red[g][l * V + v] = acc[v];
-            __syncthreads();
-            const int64_t ncols = (D - slice * LPRC * V) < LPRC * V ? D - slice * LPRC * V
-                                                                     : LPRC * V;
-            for (int j = threadIdx.x; j < ncols; j += NT) {
-                float s = red[0][j];
-    #pragma unroll
-                for (int q = 1; q < G; q++) s += red[q][j];
-                out[j] = s;
-            }
-            __syncthreads();  // red[] is reused by the next slice
-        }
-    }  // slices
+        const int64_t col0 = slice * LPRC * V;
+        const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
+        write_partial<LPRC, G, V, NT>(acc, partial + (int64_t)blockIdx.x * D + col0, g, l, cok,
+                                      ncols, red);
+    }
 }
 
 // Scalar path: blockIdx.x = row tile; a thread owns columns
@@ -403,23 +516,40 @@ static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; 
 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-static inline int next_pow2(int v) {
+static inline int next_pow2(int64_t v) {
     int p = 1;
     while (p < v) p <<= 1;
     return p;
 }
 
-template <typename T, int LPR, int CPL, int U>
-static cudaError_t fwd_reg(const T* x, int64_t ldx, const float* w, T* y, int64_t N, int Dv,
-                           cudaStream_t s) {
-    constexpr int NT = 256;
-    constexpr int rows_per_cta = (NT / 32) * (32 / LPR) * U;
-    constexpr int MINB = CPL * Elt<T>::V <= 16 ? 4 : 2;
-    const int64_t grid = std::min<int64_t>(cdiv(N, rows_per_cta), MINB * kDesignSMs);
-    return launch(ws_fwd_reg<T, LPR, CPL, U, NT, MINB>, dim3((unsigned)grid), dim3(NT), 0, s, false, x,
-                  ldx, w, y, N, Dv);
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+static cudaError_t allow_smem(const void* kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& d : done)
+        if (d.first == kernel && d.second == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.emplace_back(kernel, dev);
+    return e;
 }
 
+template <typename T, int LPR, int CPL, int U, int NT, int MINB>
+static cudaError_t fwd_reg(const T* x, int64_t ldx, const float* w, T* y, int64_t N, int Dv,
+                           cudaStream_t s) {
+    constexpr int rows_per_cta = (NT / 32) * (32 / LPR) * U;
+    const int64_t grid = std::min<int64_t>(cdiv(N, rows_per_cta), (int64_t)MINB * kDesignSMs);
+    return launch(ws_fwd_reg<T, LPR, CPL, U, NT, MINB>, dim3((unsigned)grid), dim3(NT), 0, s,
+                  false, x, ldx, w, y, N, Dv);
+}
+
+// Register-path shapes (measured on GB300): rows of <= 32 chunks use 128
+// threads, 4 rows per lane in flight and 8 CTAs per SM; rows of 128 chunks
+// one row per lane at 4 CTAs per SM.
 template <typename T>
 static cudaError_t ws_fwd_t(const T* x, int64_t ldx, const float* w, T* y, int64_t N, int64_t D,
                             cudaStream_t s) {
@@ -430,23 +560,23 @@ static cudaError_t ws_fwd_t(const T* x, int64_t ldx, const float* w, T* y, int64
         const int dv = (int)Dv;
         if (dv <= 32) {
             switch (next_pow2(dv)) {
-                case 1: return fwd_reg<T, 1, 1, 8>(x, ldx, w, y, N, dv, s);
-                case 2: return fwd_reg<T, 2, 1, 8>(x, ldx, w, y, N, dv, s);
-                case 4: return fwd_reg<T, 4, 1, 8>(x, ldx, w, y, N, dv, s);
-                case 8: return fwd_reg<T, 8, 1, 8>(x, ldx, w, y, N, dv, s);
-                case 16: return fwd_reg<T, 16, 1, 8>(x, ldx, w, y, N, dv, s);
-                default: return fwd_reg<T, 32, 1, 8>(x, ldx, w, y, N, dv, s);
+                case 1: return fwd_reg<T, 1, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
+                case 2: return fwd_reg<T, 2, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
+                case 4: return fwd_reg<T, 4, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
+                case 8: return fwd_reg<T, 8, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
+                case 16: return fwd_reg<T, 16, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
+                default: return fwd_reg<T, 32, 1, 4, 128, 8>(x, ldx, w, y, N, dv, s);
             }
         }
-        if (dv <= 64) return fwd_reg<T, 32, 2, 4>(x, ldx, w, y, N, dv, s);
-        if (dv <= 128) return fwd_reg<T, 32, 4, 2>(x, ldx, w, y, N, dv, s);
-        return fwd_reg<T, 32, 8, 1>(x, ldx, w, y, N, dv, s);
+        if (dv <= 64) return fwd_reg<T, 32, 2, 2, 256, 4>(x, ldx, w, y, N, dv, s);
+        if (dv <= 128) return fwd_reg<T, 32, 4, 1, 256, 4>(x, ldx, w, y, N, dv, s);
+        return fwd_reg<T, 32, 8, 1, 256, 2>(x, ldx, w, y, N, dv, s);
     }
     if (vec) {
-        constexpr int NT = 256, R = 4, UJ = 2;
-        const int64_t grid = std::min<int64_t>(cdiv(N, R), 64 * kDesignSMs);
-        return launch(ws_fwd_wide<T, R, UJ, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x,
-                      ldx, w, y, N, Dv);
+        constexpr int NT = 512, UJ = 4;
+        const int64_t grid = std::min<int64_t>(N, 64 * kDesignSMs);
+        return launch(ws_fwd_wide<T, UJ, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, ldx,
+                      w, y, N, Dv);
     }
     constexpr int NT = 256;
     const int64_t grid = std::min<int64_t>(cdiv(N, NT / 32), 8 * kDesignSMs);
@@ -464,14 +594,70 @@ cudaError_t launch_ws_fwd(const void* x, int64_t ldx, const float* w, void* y, i
     }
 }
 
-template <typename T, int LPRC, int U>
-static cudaError_t bwd_tile(const T* x, int64_t ldx, const float* w, const T* dy, T* dx,
-                            int64_t lddx, float* partial, int64_t N, int64_t Dv, int64_t D,
-                            int64_t block_n, int64_t P, cudaStream_t s) {
-    constexpr int NT = kTileThreads;
-    const int64_t slices = std::min<int64_t>(cdiv(Dv, LPRC), 65535);
-    return launch(ws_bwd_tile<T, LPRC, U, NT>, dim3((unsigned)P, (unsigned)slices),
-                  dim3(NT), 0, s, false, x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P);
+template <typename T>
+struct BwdArgs {
+    const T* x;
+    int64_t ldx;
+    const float* w;
+    const T* dy;
+    T* dx;
+    int64_t lddx;
+    float* partial;
+    int64_t N, Dv, D, block_n, P;
+};
+
+template <typename T, int LPRC, int U, int S, int NT, int MINB>
+static cudaError_t bwd_staged(const BwdArgs<T>& a, cudaStream_t s) {
+    const size_t smem =
+        (size_t)S * U * NT * sizeof(Raw16) + (size_t)S * (NT / LPRC) * U * sizeof(T);
+    auto kernel = ws_bwd_staged<T, LPRC, U, S, NT, MINB>;
+    cudaError_t e = allow_smem((const void*)kernel, smem);
+    if (e != cudaSuccess) return e;
+    return launch(kernel, dim3((unsigned)a.P, (unsigned)cdiv(a.Dv, LPRC)), dim3(NT), smem, s,
+                  false, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
+                  a.block_n, a.P);
+}
+
+template <typename T, int LPRC>
+static cudaError_t bwd_tile(const BwdArgs<T>& a, cudaStream_t s) {
+    constexpr int NT = LPRC < 128 ? 128 : LPRC, U = 4;
+    const int64_t slices = std::min<int64_t>(cdiv(a.Dv, LPRC), 65535);
+    return launch(ws_bwd_tile<T, LPRC, U, NT>, dim3((unsigned)a.P, (unsigned)slices), dim3(NT), 0,
+                  s, false, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
+                  a.block_n, a.P);
+}
+
+// Staged-path shapes (measured on GB300): rows of <= 64 chunks use 128
+// threads, 8 rows per thread per step and 3 steps in flight; rows of 128
+// chunks 128 threads and 4 steps; wider rows 256-chunk slices with 16 bytes
+// of dy per step.
+template <typename T>
+static cudaError_t bwd_vec(const BwdArgs<T>& a, int lprc, bool staged, cudaStream_t s) {
+    constexpr int UW = 16 / (int)sizeof(T);
+    if (staged) {
+        switch (lprc) {
+            case 1: return bwd_staged<T, 1, 8, 3, 128, 6>(a, s);
+            case 2: return bwd_staged<T, 2, 8, 3, 128, 6>(a, s);
+            case 4: return bwd_staged<T, 4, 8, 3, 128, 6>(a, s);
+            case 8: return bwd_staged<T, 8, 8, 3, 128, 6>(a, s);
+            case 16: return bwd_staged<T, 16, 8, 3, 128, 6>(a, s);
+            case 32: return bwd_staged<T, 32, 8, 3, 128, 6>(a, s);
+            case 64: return bwd_staged<T, 64, 8, 3, 128, 6>(a, s);
+            case 128: return bwd_staged<T, 128, 8, 4, 128, 6>(a, s);
+            default: return bwd_staged<T, 256, UW, 3, 256, 4>(a, s);
+        }
+    }
+    switch (lprc) {
+        case 1: return bwd_tile<T, 1>(a, s);
+        case 2: return bwd_tile<T, 2>(a, s);
+        case 4: return bwd_tile<T, 4>(a, s);
+        case 8: return bwd_tile<T, 8>(a, s);
+        case 16: return bwd_tile<T, 16>(a, s);
+        case 32: return bwd_tile<T, 32>(a, s);
+        case 64: return bwd_tile<T, 64>(a, s);
+        case 128: return bwd_tile<T, 128>(a, s);
+        default: return bwd_tile<T, 256>(a, s);
+    }
 }
 
 template <typename T>
@@ -482,26 +668,21 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
     const int64_t P = ws_tiles(N, D, dtype, block_n);
     cudaError_t e = cudaSuccess;
     if (P > 0) {
+        const int64_t Dv = D / V;
         const bool vec = D % V == 0 && ldx % V == 0 && lddx % V == 0 && aligned16(x) &&
                          aligned16(w) && aligned16(dx) && aligned16(partial);
-        const int64_t Dv = D / V;
         if (vec) {
-            switch (Dv <= kRegMaxChunks ? next_pow2((int)Dv) : kRegMaxChunks) {
-                case 1: e = bwd_tile<T, 1, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 2: e = bwd_tile<T, 2, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 4: e = bwd_tile<T, 4, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 8: e = bwd_tile<T, 8, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 16: e = bwd_tile<T, 16, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 32: e = bwd_tile<T, 32, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 64: e = bwd_tile<T, 64, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                case 128: e = bwd_tile<T, 128, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-                default: e = bwd_tile<T, 256, 4>(x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P, s); break;
-            }
+            const int lprc = Dv <= kSliceChunks ? next_pow2(Dv) : kSliceChunks;
+            // staged path: every step's dy slice must start on a 16-byte boundary
+            const bool staged = aligned16(dy) && (block_n * (int64_t)sizeof(T)) % 16 == 0 &&
+                                cdiv(Dv, lprc) <= 65535;
+            BwdArgs<T> a{x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P};
+            e = bwd_vec<T>(a, lprc, staged, s);
         } else {
             constexpr int NT = 128;
             const int64_t slices = std::min<int64_t>(cdiv(D, NT), 65535);
-            e = launch(ws_bwd_scalar<T, NT>, dim3((unsigned)P, (unsigned)slices), dim3(NT), 0,
-                       s, false, x, ldx, w, dy, dx, lddx, partial, N, D, block_n, P);
+            e = launch(ws_bwd_scalar<T, NT>, dim3((unsigned)P, (unsigned)slices), dim3(NT), 0, s,
+                       false, x, ldx, w, dy, dx, lddx, partial, N, D, block_n, P);
         }
         if (e != cudaSuccess) return e;
     }

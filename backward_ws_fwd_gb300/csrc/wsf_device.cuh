@@ -55,6 +55,25 @@ __device__ __forceinline__ void st_stream(void* p, const Raw16& r) {
                  : "memory");
 }
 
+// Asynchronous 16-byte global -> shared copy (cp.async, bypassing L1, with a
+// 256-byte L2 prefetch).  Only the first src_bytes (0..16) are read; the
+// rest of the 16 shared bytes are zero-filled.  A thread waits for its own
+// copies with cp_async_wait<N>() (at most N most recent groups pending); no
+// other synchronisation is involved, so nothing here can wait forever.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Storage-type traits: V elements per 16 bytes, widening, narrowing.
 template <typename T>
@@ -73,6 +92,7 @@ struct Elt<float> {
         for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(f[i]);
         return r;
     }
+    __device__ __forceinline__ static float widen1(float v) { return v; }
     __device__ __forceinline__ static float load1(const float* p) { return __ldg(p); }
     __device__ __forceinline__ static void store1(float* p, float v) { *p = v; }
 };
@@ -99,6 +119,7 @@ struct Elt<__half> {
         }
         return r;
     }
+    __device__ __forceinline__ static float widen1(__half v) { return __half2float(v); }
     __device__ __forceinline__ static float load1(const __half* p) { return __half2float(__ldg(p)); }
     __device__ __forceinline__ static void store1(__half* p, float v) { *p = __float2half_rn(v); }
 };
@@ -123,6 +144,7 @@ struct Elt<__nv_bfloat16> {
         }
         return r;
     }
+    __device__ __forceinline__ static float widen1(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ __forceinline__ static float load1(const __nv_bfloat16* p) {
         return __bfloat162float(__ldg(p));
     }

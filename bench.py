@@ -227,7 +227,8 @@ def run_reference(args, names):
             "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": workload_label(names), "reference": "fp64 CPU oracle"},
+            "config": {"workload": workload_label(names) + (f" (rows x {args.scale})"
+                                                             if args.scale != 1.0 else ""), "reference": "fp64 CPU oracle"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": sample_desc(samples)},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -316,9 +317,9 @@ def run_cuda(args, names):
     if world > 1:
         dist.barrier()
     import backward_ws_fwd_gb300 as wsf
-    from inputgen.workloads import WORKLOADS
 
     host_io = not args.no_e2e
+    WORKLOADS = scaled_workloads(args.scale)
     bufs = {n: Buffers(WORKLOADS[n], dev, wsf, host_io) for n in names}
     ops = steps_ops(names)
     step_bytes = sum(op_bytes(WORKLOADS[n], op) for n, op in ops)
@@ -442,7 +443,8 @@ def run_cuda(args, names):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded SplitMix64/Box-Muller, BASELINE workload recipes)"
                     .replace("BASELINE ", ""),
-            "config": {"workload": workload_label(names),
+            "config": {"workload": workload_label(names) + (f" (rows x {args.scale})"
+                                                             if args.scale != 1.0 else ""),
                        "step": [f"{n}.{op}" for n, op in ops],
                        "bytes_per_step": step_bytes,
                        "frac_of_peak": round(value / world / peak, 4),
@@ -457,6 +459,15 @@ def run_cuda(args, names):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def scaled_workloads(scale: float):
+    """The workload table with every row count multiplied by `scale`."""
+    import dataclasses
+    from inputgen.workloads import WORKLOADS
+    if scale == 1.0:
+        return WORKLOADS
+    return {k: dataclasses.replace(v, N=max(1, int(round(v.N * scale)))) for k, v in WORKLOADS.items()}
 
 
 def read_traffic(kernel: str, workload: str):
@@ -492,6 +503,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="all", help="all or a comma list of c2,c3,c4,c5")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="multiply every workload's row count (profiling on small cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

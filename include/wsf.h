@@ -135,7 +135,7 @@ int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
  * process exits.  The call allocates nothing.
  *   - Sizes whose ws_bwd_workspace_bytes(N, D, dtype, block_n) exceeds
  *     WSF_NOALLOC_SCRATCH_BYTES are rejected with WSF_ERR_WORKSPACE before
- *     anything is enqueued (the five benchmark workloads need at most 2.4 MiB).
+ *     anything is enqueued (the five benchmark workloads need at most 3.6 MiB).
  *   - The first call on a device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with the device current); make that first call
  *     before any stream capture.

@@ -54,9 +54,9 @@ def test_workspace_queries(wsf):
                      (7, 5, wsf.F32), (1, 1, wsf.F16)]:
         b = q(N, D, dt, 0)
         assert b % 256 == 0 and b >= 4 * D and b <= max(4 * D * N, 256) + 255
-        # at most 608 tiles and at most one tile per 64 rows
+        # at most 912 tiles and at most one tile per 64 rows
         P = b // (4 * D)
-        assert P <= 608 and (P <= max(1, -(-N // 64)) or b - 4 * D * max(1, -(-N // 64)) < 256)
+        assert P <= 912 and (P <= max(1, -(-N // 64)) or b - 4 * D * max(1, -(-N // 64)) < 256)
     s = wsf.lib.silu_bwd_workspace_bytes
     assert s(0, wsf.F16) == 0 and s(1, wsf.F16) == 256 and s(-1, wsf.F16) == wsf.SIZE_MAX
     assert s(8192 * 4096, wsf.F16) == 1216 * 4 // 256 * 256 + (256 if 1216 * 4 % 256 else 0)

@@ -57,18 +57,19 @@ def make_ws(N, D, dt, seed_shift=0, xdist=(NORMAL, 0.0, 1.0)):
     return x, w, dy
 
 
-def run_ws(wsf, x, w, dy, ld_pad=0, misalign=0, block_n=0):
+def run_ws(wsf, x, w, dy, ld_pad=0, misalign=0, block_n=0, dy_misalign=None):
     """Place inputs on the device (optionally with a row stride of D + ld_pad
-    and pointers shifted by `misalign` elements), run forward and backward
-    with guarded outputs; returns host results."""
+    and pointers shifted by `misalign` elements; dy alone by `dy_misalign`),
+    run forward and backward with guarded outputs; returns host results."""
     N, D = x.shape
     dt = x.dtype
     ld = D + ld_pad
+    dmis = misalign if dy_misalign is None else dy_misalign
     xb = torch.zeros(N * ld + misalign + 8, dtype=dt, device=DEV)
     xd = xb[misalign:misalign + N * ld].view(N, ld)[:, :D]
     xd.copy_(x.to(DEV))
-    dyb = torch.zeros(N + misalign + 8, dtype=dt, device=DEV)
-    dyd = dyb[misalign:misalign + N]
+    dyb = torch.zeros(N + dmis + 8, dtype=dt, device=DEV)
+    dyd = dyb[dmis:dmis + N]
     dyd.copy_(dy.to(DEV))
     wd = w.to(DEV)
     y, ychk = guarded((N,), dt)
@@ -119,6 +120,16 @@ def test_ws_parity_shapes(wsf, dt, N, D):
 def test_ws_parity_strides_alignment(wsf, dt, N, D, ld_pad, misalign):
     x, w, dy = make_ws(N, D, dt)
     y, dx, gw = run_ws(wsf, x, w, dy, ld_pad=ld_pad, misalign=misalign)
+    assert_ws_parity(x, w, dy, y, dx, gw)
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D", [(37, 64), (1000, 8), (77, 1024), (9, 2056), (5, 8200)])
+def test_ws_parity_register_tile_path(wsf, dt, N, D):
+    """x and dx 16-byte aligned but dy not: the backward uses the register-load
+    tile kernel instead of the cp.async-staged one."""
+    x, w, dy = make_ws(N, D, dt)
+    y, dx, gw = run_ws(wsf, x, w, dy, dy_misalign=1)
     assert_ws_parity(x, w, dy, y, dx, gw)
 
 
