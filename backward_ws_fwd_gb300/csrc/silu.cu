@@ -18,7 +18,14 @@
 // cancellation near the minimum of silu (x ≈ −1.2785, where silu' = 0) down
 // to the error of exp: (1+x) is exact for x in [−2, −1/2] and (1+x) + t is
 // an exact difference there.
+//
+// For 16-bit storage the exponential and the reciprocal use the hardware
+// approximations (__expf, __fdividef; relative error ~1e-6 for |x| <= 20,
+// far below the 2^-11 half-unit of a 16-bit result) — the full-precision
+// versions made these kernels instruction-bound.  binary32 storage keeps
+// expf and an IEEE division.
 #include <algorithm>
+#include <type_traits>
 
 #include "wsf_device.cuh"
 #include "wsf_internal.h"
@@ -39,16 +46,33 @@ struct SiluTerms {
     float dsilu;  // d(x·s)/dx
 };
 
+// exp(-a) and 1/d, exact-rounding library versions or hardware approximations
+template <bool Fast>
+__device__ __forceinline__ float exp_neg(float a) {
+    if constexpr (Fast) return __expf(-a);
+    else return expf(-a);
+}
+template <bool Fast>
+__device__ __forceinline__ float recip(float d) {
+    if constexpr (Fast) return __fdividef(1.0f, d);
+    else return 1.0f / d;
+}
+
+template <typename T>
+constexpr bool kFastMath = !std::is_same<T, float>::value;
+
+template <bool Fast>
 __device__ __forceinline__ float silu_only(float x) {
-    const float t = expf(-fabsf(x));
-    const float r = 1.0f / (1.0f + t);
+    const float t = exp_neg<Fast>(fabsf(x));
+    const float r = recip<Fast>(1.0f + t);
     const float s = (x >= 0.f) ? r : t * r;
     return x * s;
 }
 
+template <bool Fast>
 __device__ __forceinline__ SiluTerms silu_terms(float x) {
-    const float t = expf(-fabsf(x));
-    const float r = 1.0f / (1.0f + t);
+    const float t = exp_neg<Fast>(fabsf(x));
+    const float r = recip<Fast>(1.0f + t);
     SiluTerms o;
     if (x >= 0.f) {
         o.silu = x * r;
@@ -69,6 +93,7 @@ __global__ void __launch_bounds__(NT)
                  int64_t n) {
     using E = Elt<T>;
     constexpr int V = E::V;
+    pdl_wait();
     const float wv = __ldg(w);
     const int64_t nv = n / V;
     for (int64_t base = (int64_t)blockIdx.x * NT * U; base < nv; base += (int64_t)gridDim.x * NT * U) {
@@ -85,15 +110,16 @@ __global__ void __launch_bounds__(NT)
                 float f[V];
                 E::widen(xr[u], f);
 #pragma unroll
-                for (int v = 0; v < V; v++) f[v] = wv * silu_only(f[v]);
+                for (int v = 0; v < V; v++) f[v] = wv * silu_only<kFastMath<T>>(f[v]);
                 st_stream(y + i * V, E::narrow(f));
             }
         }
     }
     if (blockIdx.x == 0) {
         const int64_t k = nv * V + threadIdx.x;
-        if (k < n) E::store1(y + k, wv * silu_only(E::load1(x + k)));
+        if (k < n) E::store1(y + k, wv * silu_only<kFastMath<T>>(E::load1(x + k)));
     }
+    pdl_trigger();
 }
 
 template <typename T, int NT>
@@ -101,9 +127,11 @@ __global__ void __launch_bounds__(NT)
     silu_fwd_scalar(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
                     int64_t n) {
     using E = Elt<T>;
+    pdl_wait();
     const float wv = __ldg(w);
     for (int64_t k = (int64_t)blockIdx.x * NT + threadIdx.x; k < n; k += (int64_t)gridDim.x * NT)
-        E::store1(y + k, wv * silu_only(E::load1(x + k)));
+        E::store1(y + k, wv * silu_only<kFastMath<T>>(E::load1(x + k)));
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -132,6 +160,7 @@ __global__ void __launch_bounds__(NT)
                  T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
     using E = Elt<T>;
     constexpr int V = E::V;
+    pdl_wait();
     const float wv = __ldg(w);
     const int64_t nv = n / V;
     const int64_t p = blockIdx.x;
@@ -154,7 +183,7 @@ __global__ void __launch_bounds__(NT)
             E::widen(gr[u], gf);
 #pragma unroll
             for (int v = 0; v < V; v++) {
-                const SiluTerms st = silu_terms(xf[v]);
+                const SiluTerms st = silu_terms<kFastMath<T>>(xf[v]);
                 acc = fmaf(gf[v], st.silu, acc);
                 xf[v] = (gf[v] * wv) * st.dsilu;
             }
@@ -165,11 +194,12 @@ __global__ void __launch_bounds__(NT)
         const int64_t k = nv * V + threadIdx.x;
         if (k < n) {
             const float xv = E::load1(x + k), gv = E::load1(dy + k);
-            const SiluTerms st = silu_terms(xv);
+            const SiluTerms st = silu_terms<kFastMath<T>>(xv);
             acc = fmaf(gv, st.silu, acc);
             E::store1(dx + k, (gv * wv) * st.dsilu);
         }
     }
+    pdl_trigger();
     block_sum_store<NT>(acc, part + p);
 }
 
@@ -178,16 +208,18 @@ __global__ void __launch_bounds__(NT)
     silu_bwd_scalar(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
                     T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
     using E = Elt<T>;
+    pdl_wait();
     const float wv = __ldg(w);
     const int64_t p = blockIdx.x;
     const int64_t kb = (p * n) / P, ke = ((p + 1) * n) / P;
     float acc = 0.f;
     for (int64_t k = kb + threadIdx.x; k < ke; k += NT) {
         const float xv = E::load1(x + k), gv = E::load1(dy + k);
-        const SiluTerms st = silu_terms(xv);
+        const SiluTerms st = silu_terms<kFastMath<T>>(xv);
         acc = fmaf(gv, st.silu, acc);
         E::store1(dx + k, (gv * wv) * st.dsilu);
     }
+    pdl_trigger();
     block_sum_store<NT>(acc, part + p);
 }
 
@@ -197,11 +229,13 @@ template <int NT>
 __global__ void __launch_bounds__(NT)
     silu_bwd_reduce(const float* __restrict__ part, int64_t P, float* __restrict__ dw,
                     int accumulate) {
+    pdl_wait();
     float s = 0.f;
     for (int64_t i = threadIdx.x; i < P; i += NT) s += part[i];
     __shared__ float total;
     block_sum_store<NT>(s, &total);
     if (threadIdx.x == 0) *dw = accumulate ? *dw + total : total;
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -214,12 +248,12 @@ static cudaError_t silu_fwd_t(const T* x, const float* w, T* y, int64_t n, cudaS
     if (aligned16(x) && aligned16(y)) {
         constexpr int NT = 256, U = 4;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(cdiv(n / V, NT * U), 8 * kDesignSMs));
-        return launch(silu_fwd_vec<T, U, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, w, y,
+        return launch(silu_fwd_vec<T, U, NT>, dim3((unsigned)grid), dim3(NT), 0, s, true, x, w, y,
                       n);
     }
     constexpr int NT = 256;
     const int64_t grid = std::min<int64_t>(cdiv(n, NT), 8 * kDesignSMs);
-    return launch(silu_fwd_scalar<T, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, w, y, n);
+    return launch(silu_fwd_scalar<T, NT>, dim3((unsigned)grid), dim3(NT), 0, s, true, x, w, y, n);
 }
 
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
@@ -239,17 +273,17 @@ static cudaError_t silu_bwd_t(const T* dy, const T* x, const float* w, T* dx, fl
     if (P > 0) {
         if (aligned16(dy) && aligned16(x) && aligned16(dx)) {
             constexpr int NT = 256, U = 2;
-            e = launch(silu_bwd_vec<T, U, NT>, dim3((unsigned)P), dim3(NT), 0, s, false, dy, x, w,
+            e = launch(silu_bwd_vec<T, U, NT>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
                        dx, part, n, P);
         } else {
             constexpr int NT = 256;
-            e = launch(silu_bwd_scalar<T, NT>, dim3((unsigned)P), dim3(NT), 0, s, false, dy, x, w,
+            e = launch(silu_bwd_scalar<T, NT>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
                        dx, part, n, P);
         }
         if (e != cudaSuccess) return e;
     }
     constexpr int NT = 1024;
-    return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, false, (const float*)part, P, dw,
+    return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, true, (const float*)part, P, dw,
                   accumulate);
 }
 

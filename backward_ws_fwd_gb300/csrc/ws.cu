@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(NT, MINB)
     const int lane = threadIdx.x & 31;
     const int g = lane / LPR, l = lane % LPR;
 
+    pdl_wait();
     float wr[CPL][V];
     load_w<LPR, CPL, V>(w, l, Dv, wr);
 
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(NT, MINB)
             if (row < N) E::store1(y + row, select<U>(acc, u));
         }
     }
+    pdl_trigger();
 }
 
 // Wide rows: one CTA per row (grid-stride over rows).  Each thread sums the
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(NT)
     constexpr int NW = NT / 32;
     __shared__ Acc2 red[NW];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    pdl_wait();
     for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
         const T* xrow = x + row * ldx;
         float s = 0.f, comp = 0.f;
@@ -231,6 +234,7 @@ __global__ void __launch_bounds__(NT)
         }
         __syncthreads();
     }
+    pdl_trigger();
 }
 
 // One warp per row, element-wise loads: any alignment, any D (D == 0 gives 0).
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(NT)
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * NT + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * NT) >> 5;
+    pdl_wait();
     for (int64_t row = warp; row < N; row += nwarps) {
         Acc2 a = acc2_zero();
         for (int64_t d = lane; d < D; d += 32) {
@@ -259,6 +264,7 @@ __global__ void __launch_bounds__(NT)
         }
         if (lane == 0) E::store1(y + row, v);
     }
+    pdl_trigger();
 }
 
 // ===========================================================================
@@ -326,6 +332,7 @@ __global__ void __launch_bounds__(NT, MINB)
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
     const int64_t c = (int64_t)blockIdx.y * LPRC + l;
     const bool cok = c < Dv;
+    pdl_wait();
 
     float wv[V];
 #pragma unroll
@@ -388,6 +395,7 @@ __global__ void __launch_bounds__(NT, MINB)
         }
     }
     cp_async_wait<0>();  // no copy may still target shared memory when the CTA ends
+    pdl_trigger();
     __syncthreads();
     const int64_t col0 = (int64_t)blockIdx.y * LPRC * V;
     const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
@@ -412,6 +420,7 @@ __global__ void __launch_bounds__(NT)
     int64_t ra, rb;
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
     const int64_t nslices = (Dv + LPRC - 1) / LPRC;
+    pdl_wait();
     for (int64_t slice = blockIdx.y; slice < nslices; slice += gridDim.y) {
         const int64_t c = slice * LPRC + l;
         const bool cok = c < Dv;
@@ -455,6 +464,7 @@ __global__ void __launch_bounds__(NT)
         write_partial<LPRC, G, V, NT>(acc, partial + (int64_t)blockIdx.x * D + col0, g, l, cok,
                                       ncols, red);
     }
+    pdl_trigger();
 }
 
 // Scalar path: blockIdx.x = row tile; a thread owns columns
@@ -467,6 +477,7 @@ __global__ void __launch_bounds__(NT)
     using E = Elt<T>;
     int64_t ra, rb;
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
+    pdl_wait();
     for (int64_t col = (int64_t)blockIdx.y * NT + threadIdx.x; col < D;
          col += (int64_t)gridDim.y * NT) {
         const float wv = __ldg(w + col);
@@ -478,12 +489,14 @@ __global__ void __launch_bounds__(NT)
         }
         partial[(int64_t)blockIdx.x * D + col] = acc;
     }
+    pdl_trigger();
 }
 
 // ===========================================================================
 // Backward, stage 2: grad_w[d] = (accumulate ? grad_w[d] : 0) + Σ_p partial[p,d]
 // Thread (tx, ty) sums p = ty, ty + RY, ... in ascending order; the RY
-// stripe sums are then combined by a fixed halving tree.
+// stripe sums are then combined by a fixed halving tree.  RY is 32 for rows
+// of up to 4096 columns and 8 above; either way the order is fixed by D.
 // ===========================================================================
 template <int RY>
 __global__ void __launch_bounds__(32 * RY)
@@ -492,9 +505,12 @@ __global__ void __launch_bounds__(32 * RY)
     __shared__ float sm[RY][33];
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int64_t col = (int64_t)blockIdx.x * 32 + tx;
+    pdl_wait();
     float s = 0.f;
-    if (col < D)
+    if (col < D) {
+#pragma unroll 8
         for (int64_t p = ty; p < P; p += RY) s += partial[p * D + col];
+    }
     sm[ty][tx] = s;
     __syncthreads();
 #pragma unroll
@@ -506,6 +522,7 @@ __global__ void __launch_bounds__(32 * RY)
         const float v = sm[0][tx];
         grad_w[col] = accumulate ? grad_w[col] + v : v;
     }
+    pdl_trigger();
 }
 
 // ===========================================================================
@@ -544,7 +561,7 @@ static cudaError_t fwd_reg(const T* x, int64_t ldx, const float* w, T* y, int64_
     constexpr int rows_per_cta = (NT / 32) * (32 / LPR) * U;
     const int64_t grid = std::min<int64_t>(cdiv(N, rows_per_cta), (int64_t)MINB * kDesignSMs);
     return launch(ws_fwd_reg<T, LPR, CPL, U, NT, MINB>, dim3((unsigned)grid), dim3(NT), 0, s,
-                  false, x, ldx, w, y, N, Dv);
+                  true, x, ldx, w, y, N, Dv);
 }
 
 // Register-path shapes (measured on GB300): rows of <= 32 chunks use 128
@@ -575,12 +592,12 @@ static cudaError_t ws_fwd_t(const T* x, int64_t ldx, const float* w, T* y, int64
     if (vec) {
         constexpr int NT = 512, UJ = 4;
         const int64_t grid = std::min<int64_t>(N, 64 * kDesignSMs);
-        return launch(ws_fwd_wide<T, UJ, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, ldx,
+        return launch(ws_fwd_wide<T, UJ, NT>, dim3((unsigned)grid), dim3(NT), 0, s, true, x, ldx,
                       w, y, N, Dv);
     }
     constexpr int NT = 256;
     const int64_t grid = std::min<int64_t>(cdiv(N, NT / 32), 8 * kDesignSMs);
-    return launch(ws_fwd_scalar<T, NT>, dim3((unsigned)grid), dim3(NT), 0, s, false, x, ldx, w, y,
+    return launch(ws_fwd_scalar<T, NT>, dim3((unsigned)grid), dim3(NT), 0, s, true, x, ldx, w, y,
                   N, D);
 }
 
@@ -614,7 +631,7 @@ static cudaError_t bwd_staged(const BwdArgs<T>& a, cudaStream_t s) {
     cudaError_t e = allow_smem((const void*)kernel, smem);
     if (e != cudaSuccess) return e;
     return launch(kernel, dim3((unsigned)a.P, (unsigned)cdiv(a.Dv, LPRC)), dim3(NT), smem, s,
-                  false, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
+                  true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
                   a.block_n, a.P);
 }
 
@@ -623,7 +640,7 @@ static cudaError_t bwd_tile(const BwdArgs<T>& a, cudaStream_t s) {
     constexpr int NT = LPRC < 128 ? 128 : LPRC, U = 4;
     const int64_t slices = std::min<int64_t>(cdiv(a.Dv, LPRC), 65535);
     return launch(ws_bwd_tile<T, LPRC, U, NT>, dim3((unsigned)a.P, (unsigned)slices), dim3(NT), 0,
-                  s, false, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
+                  s, true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
                   a.block_n, a.P);
 }
 
@@ -682,14 +699,19 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
             constexpr int NT = 128;
             const int64_t slices = std::min<int64_t>(cdiv(D, NT), 65535);
             e = launch(ws_bwd_scalar<T, NT>, dim3((unsigned)P, (unsigned)slices), dim3(NT), 0, s,
-                       false, x, ldx, w, dy, dx, lddx, partial, N, D, block_n, P);
+                       true, x, ldx, w, dy, dx, lddx, partial, N, D, block_n, P);
         }
         if (e != cudaSuccess) return e;
     }
     if (D > 0) {
-        constexpr int RY = 16;
-        e = launch(ws_bwd_reduce<RY>, dim3((unsigned)cdiv(D, 32)), dim3(32, RY), 0, s, false,
-                   (const float*)partial, P, D, grad_w, accumulate);
+        // narrow rows: 32 stripes of tiles per 32-column tile, so that a
+        // handful of CTAs still keep many loads in flight
+        if (D <= 4096)
+            e = launch(ws_bwd_reduce<32>, dim3((unsigned)cdiv(D, 32)), dim3(32, 32), 0, s, true,
+                       (const float*)partial, P, D, grad_w, accumulate);
+        else
+            e = launch(ws_bwd_reduce<8>, dim3((unsigned)cdiv(D, 32)), dim3(32, 8), 0, s, true,
+                       (const float*)partial, P, D, grad_w, accumulate);
     }
     return e;
 }

@@ -18,6 +18,19 @@ constexpr unsigned FULL_MASK = 0xffffffffu;
 constexpr int kDesignSMs = 152;
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may be scheduled while the previous kernel on the stream drains;
+// each one therefore calls pdl_wait() before its first global memory access
+// (read or write), which blocks until the previous grid has completed and its
+// writes are visible.  pdl_trigger() tells the hardware that this CTA's main
+// work is done, so the next kernel may begin launching.  Both are no-ops when
+// a kernel is launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // 16-byte vector of raw storage.
 struct alignas(16) Raw16 {
     uint32_t u[4];

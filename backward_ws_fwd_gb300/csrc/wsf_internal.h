@@ -34,8 +34,9 @@ cudaError_t launch_silu_bwd(const void* dy, const void* x, const float* w, void*
 
 // Launch through cudaLaunchKernelEx so that the status returned is this
 // launch's own.  `pdl` lets the kernel start while the previous kernel on
-// the stream drains; such a kernel must wait (griddepcontrol.wait) before
-// touching that kernel's outputs.
+// the stream drains; every kernel of the library begins with
+// griddepcontrol.wait, so nothing it reads or writes is touched before the
+// previous kernel has finished.
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                    bool pdl, Args&&... args) {
