@@ -1,0 +1,78 @@
+"""Host-side checks of bench.py: the algorithmic byte model of each op, and
+the max-over-ranks timing reduction run as two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from inputgen.workloads import WORKLOADS
+
+# algorithmic bytes per op (read x and w, write y / read x, dy, w, write dx
+# and the parameter gradient), as in the measurement plan's table
+EXPECTED = {
+    "c1": (26_256, 52_112),
+    "c2": (134_217_732, 201_326_600),
+    "c3": (2_149_584_896, 4_297_072_640),
+    "c4": (2_181_038_336, 4_328_522_240),
+    "c5": (1_074_020_352, 2_148_024_320),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EXPECTED))
+def test_byte_model(name):
+    wl = WORKLOADS[name]
+    assert (bench.op_bytes(wl, "fwd"), bench.op_bytes(wl, "bwd")) == EXPECTED[name]
+
+
+def test_step_composition():
+    ops = bench.steps_ops(bench.ORDER_FWD)
+    assert ops[:4] == [("c2", "fwd"), ("c3", "fwd"), ("c4", "fwd"), ("c5", "fwd")]
+    assert ops[4:] == [("c5", "bwd"), ("c4", "bwd"), ("c3", "bwd"), ("c2", "bwd")]
+    total = sum(bench.op_bytes(WORKLOADS[n], op) for n, op in ops)
+    assert total == sum(sum(EXPECTED[n]) for n in ["c2", "c3", "c4", "c5"])
+    assert sum(bench.KERNELS_PER_OP[bench.op_name(WORKLOADS[n], op)] for n, op in ops) == 12
+
+
+def test_scaled_workloads():
+    s = bench.scaled_workloads(0.125)
+    assert s["c4"].N == (1 << 24) // 8 and s["c4"].D == 64 and s["c1"].N == 12
+    assert bench.scaled_workloads(1.0) is WORKLOADS
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        assert bench.dist_info() == (rank, world, rank)
+        v = bench.max_over_ranks(10.0 * (rank + 1), device="cpu")
+        out[rank] = v
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 20.0, 1: 20.0}
+
+
+def test_max_over_ranks_single_process():
+    assert bench.max_over_ranks(3.5) == 3.5
