@@ -42,6 +42,10 @@ lib.ws_bwd.restype = _int
 lib.ws_bwd_noalloc.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _i64, _i64, _i64, _int,
                                _vp]
 lib.ws_bwd_noalloc.restype = _int
+lib.ws_bwd_atomic.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _i64, _i64, _int, _vp]
+lib.ws_bwd_atomic.restype = _int
+lib.silu_bwd_atomic.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _i64, _int, _vp]
+lib.silu_bwd_atomic.restype = _int
 lib.silu_fwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
 lib.silu_fwd.restype = _int
 lib.silu_bwd_workspace_bytes.argtypes = [_i64, _int]
@@ -155,6 +159,35 @@ def ws_bwd_noalloc(x, w, dy, dx=None, grad_w=None, accumulate=False, block_n=0, 
     return dx, grad_w
 
 
+def ws_bwd_atomic(x, w, dy, dx=None, grad_w=None, accumulate=False, stream=None):
+    """ws_bwd with grad_w summed by atomic additions (run-to-run bits may
+    differ); the measured comparison for the deterministic two-pass form."""
+    import torch
+    N, D = x.shape
+    if dx is None:
+        dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    if grad_w is None:
+        grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
+    _check(lib.ws_bwd_atomic(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
+                             _ptr(grad_w), int(bool(accumulate)), N, D, _dtype_code(x),
+                             _stream(stream)), "ws_bwd_atomic")
+    return dx, grad_w
+
+
+def silu_bwd_atomic(dy, x, w, dx=None, dw=None, accumulate=False, stream=None):
+    """silu_bwd with dw summed by one atomic addition per block (the pages'
+    own scheme); run-to-run bits may differ."""
+    import torch
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib.silu_bwd_atomic(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), ctypes.c_void_p(dw.data_ptr()),
+                               int(bool(accumulate)), x.numel(), _dtype_code(x), _stream(stream)),
+           "silu_bwd_atomic")
+    return dx, dw
+
+
 def silu_fwd(x, w, y=None, stream=None):
     """y = w·x·sigmoid(x).  x contiguous (any shape); w: one float32 on the device."""
     import torch
@@ -187,5 +220,5 @@ def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, strea
 
 
 __all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
-           "silu_fwd",
+           "ws_bwd_atomic", "silu_bwd_atomic", "silu_fwd",
            "silu_bwd", "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "F32", "F16", "BF16"]

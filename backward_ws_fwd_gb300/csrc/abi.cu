@@ -181,4 +181,51 @@ int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,
                                             dtype, (cudaStream_t)stream));
 }
 
+int ws_bwd_atomic(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                  int64_t lddx, float* grad_w, int accumulate, int64_t N, int64_t D, int dtype,
+                  wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldx < D || lddx < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = mat ? extent_bytes(N, D, ldx, es) : 0;
+    const int64_t dxb = mat ? extent_bytes(N, D, lddx, es) : 0;
+    int64_t dyb, wb;
+    if (xb < 0 || dxb < 0 || !mul_ok(N, es, &dyb) || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
+    if ((mat && (!x || !dy || !dx || !w)) || (D > 0 && !grad_w)) return WSF_ERR_NULL_PTR;
+    if (D == 0) return WSF_OK;
+    if (mat && !wsf::ws_bwd_atomic_supported(x, ldx, w, dy, dx, lddx, grad_w, D, dtype))
+        return WSF_ERR_MISALIGNED;
+    const Span sdx = span(dx, dxb), sg = span(grad_w, wb);
+    const Span sx = span(x, xb), sdy = span(dy, mat ? dyb : 0), sw = span(w, mat ? wb : 0);
+    if (overlap(sdx, sx) || overlap(sdx, sdy) || overlap(sdx, sw) || overlap(sg, sx) ||
+        overlap(sg, sdy) || overlap(sg, sw) || overlap(sdx, sg))
+        return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_ws_bwd_atomic(x, ldx, w, dy, dx, lddx, grad_w, accumulate, N, D,
+                                                 dtype, (cudaStream_t)stream));
+}
+
+int silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                    int accumulate, int64_t n, int dtype, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (n < 0) return WSF_ERR_BAD_SHAPE;
+    if (accumulate != 0 && accumulate != 1) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    int64_t b;
+    if (!mul_ok(n, es, &b)) return WSF_ERR_BAD_SHAPE;
+    if (!dw || (n > 0 && (!x || !dy || !dx || !w))) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(w, 4) ||
+        !aligned_to(dw, 4))
+        return WSF_ERR_MISALIGNED;
+    const Span sdx = span(dx, b), sdw = span(dw, 4);
+    const Span sx = span(x, b), sdy = span(dy, b), sw = span(w, n > 0 ? 4 : 0);
+    if (overlap(sdx, sx) || overlap(sdx, sdy) || overlap(sdx, sw) || overlap(sdw, sx) ||
+        overlap(sdw, sdy) || overlap(sdw, sw) || overlap(sdx, sdw))
+        return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_silu_bwd_atomic(dy, x, w, dx, dw, accumulate, n, dtype,
+                                                   (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(NT)
 // block also the n mod V tail elements); each thread accumulates dy·silu(x)
 // over its elements in order, then the block combines: xor butterfly inside
 // each warp, warps added in index order.
-template <int NT>
+// With ATOMIC the block's sum is added into *out with one atomic addition
+// (the page's own scheme, kept as a measured comparison: the order of the
+// blocks' additions, and so the bits of dw, depend on scheduling).
+template <int NT, bool ATOMIC = false>
 __device__ __forceinline__ void block_sum_store(float acc, float* out) {
     constexpr int NW = NT / 32;
     __shared__ float red[NW];
@@ -150,11 +153,14 @@ __device__ __forceinline__ void block_sum_store(float acc, float* out) {
         float s = red[0];
 #pragma unroll
         for (int q = 1; q < NW; q++) s += red[q];
-        *out = s;
+        if constexpr (ATOMIC)
+            atomicAdd(out, s);
+        else
+            *out = s;
     }
 }
 
-template <typename T, int U, int NT>
+template <typename T, int U, int NT, bool ATOMIC = false>
 __global__ void __launch_bounds__(NT)
     silu_bwd_vec(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
                  T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
@@ -200,10 +206,10 @@ __global__ void __launch_bounds__(NT)
         }
     }
     pdl_trigger();
-    block_sum_store<NT>(acc, part + p);
+    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p);
 }
 
-template <typename T, int NT>
+template <typename T, int NT, bool ATOMIC = false>
 __global__ void __launch_bounds__(NT)
     silu_bwd_scalar(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
                     T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(NT)
         E::store1(dx + k, (gv * wv) * st.dsilu);
     }
     pdl_trigger();
-    block_sum_store<NT>(acc, part + p);
+    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p);
 }
 
 // Backward, stage 2: one block; thread t sums part[t], part[t + NT], ... in
@@ -285,6 +291,46 @@ static cudaError_t silu_bwd_t(const T* dy, const T* x, const float* w, T* dx, fl
     constexpr int NT = 1024;
     return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, true, (const float*)part, P, dw,
                   accumulate);
+}
+
+__global__ void __launch_bounds__(32) zero_one_f32(float* __restrict__ p) {
+    pdl_wait();
+    if (threadIdx.x == 0) *p = 0.f;
+    pdl_trigger();
+}
+
+template <typename T>
+static cudaError_t silu_bwd_atomic_t(const T* dy, const T* x, const float* w, T* dx, float* dw,
+                                     int accumulate, int64_t n, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (!accumulate) {
+        e = launch(zero_one_f32, dim3(1), dim3(32), 0, s, true, dw);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t P = silu_tiles(n);
+    if (P == 0) return e;
+    constexpr int NT = 256;
+    if (aligned16(dy) && aligned16(x) && aligned16(dx))
+        return launch(silu_bwd_vec<T, 2, NT, true>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x,
+                      w, dx, dw, n, P);
+    return launch(silu_bwd_scalar<T, NT, true>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
+                  dx, dw, n, P);
+}
+
+cudaError_t launch_silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx,
+                                   float* dw, int accumulate, int64_t n, int dtype,
+                                   cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return silu_bwd_atomic_t((const float*)dy, (const float*)x, w, (float*)dx, dw,
+                                     accumulate, n, s);
+        case 1:
+            return silu_bwd_atomic_t((const __half*)dy, (const __half*)x, w, (__half*)dx, dw,
+                                     accumulate, n, s);
+        default:
+            return silu_bwd_atomic_t((const __nv_bfloat16*)dy, (const __nv_bfloat16*)x, w,
+                                     (__nv_bfloat16*)dx, dw, accumulate, n, s);
+    }
 }
 
 cudaError_t launch_silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,

@@ -273,8 +273,11 @@ __global__ void __launch_bounds__(NT)
 
 // Write the CTA's partial row for columns [slice·LPRC·V, ...): G == 1 writes
 // each thread's V sums directly; otherwise the G row groups are added in
-// index order through shared memory `red` (G·LPRC·V floats).
-template <int LPRC, int G, int V, int NT>
+// index order through shared memory `red` (G·LPRC·V floats).  With ATOMIC the
+// row is instead added into grad_w with atomic additions (the measured
+// comparison variant: the order of the additions, and so the bits of the
+// result, then depend on scheduling).
+template <int LPRC, int G, int V, int NT, bool ATOMIC = false>
 __device__ __forceinline__ void write_partial(const float (&acc)[V], float* __restrict__ out,
                                               int g, int l, bool cok, int64_t ncols,
                                               float* red) {
@@ -282,10 +285,15 @@ __device__ __forceinline__ void write_partial(const float (&acc)[V], float* __re
         if (cok) {
 #pragma unroll
             for (int q = 0; q < V / 4; q++) {
-                Raw16 r;
+                if constexpr (ATOMIC) {
+                    atomicAdd(reinterpret_cast<float4*>(out + l * V + 4 * q),
+                              make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+                } else {
+                    Raw16 r;
 #pragma unroll
-                for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(acc[4 * q + i]);
-                *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = r;
+                    for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(acc[4 * q + i]);
+                    *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = r;
+                }
             }
         }
     } else {
@@ -296,7 +304,10 @@ __device__ __forceinline__ void write_partial(const float (&acc)[V], float* __re
             float s = red[j];
 #pragma unroll
             for (int q = 1; q < G; q++) s += red[q * LPRC * V + j];
-            out[j] = s;
+            if constexpr (ATOMIC)
+                atomicAdd(out + j, s);
+            else
+                out[j] = s;
         }
         __syncthreads();
     }
@@ -310,7 +321,7 @@ __device__ __forceinline__ void write_partial(const float (&acc)[V], float* __re
 // into its own shared slots while it computes step k; the step's dy slice
 // (SR values, 16-byte aligned) is copied in 16-byte pieces by the first
 // threads, so each step starts with a CTA barrier.
-template <typename T, int LPRC, int U, int S, int NT, int MINB>
+template <typename T, int LPRC, int U, int S, int NT, int MINB, bool ATOMIC = false>
 __global__ void __launch_bounds__(NT, MINB)
     ws_bwd_staged(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                   const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
@@ -399,8 +410,10 @@ __global__ void __launch_bounds__(NT, MINB)
     __syncthreads();
     const int64_t col0 = (int64_t)blockIdx.y * LPRC * V;
     const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
-    write_partial<LPRC, G, V, NT>(acc, partial + (int64_t)blockIdx.x * D + col0, g, l, cok, ncols,
-                                  reinterpret_cast<float*>(smem));
+    // ATOMIC: `partial` is grad_w itself and every tile adds into the same row
+    float* out = partial + (ATOMIC ? 0 : (int64_t)blockIdx.x * D) + col0;
+    write_partial<LPRC, G, V, NT, ATOMIC>(acc, out, g, l, cok, ncols,
+                                          reinterpret_cast<float*>(smem));
 }
 
 // Tile path: the staged kernel's thread layout with register-held loads (U
@@ -623,11 +636,11 @@ struct BwdArgs {
     int64_t N, Dv, D, block_n, P;
 };
 
-template <typename T, int LPRC, int U, int S, int NT, int MINB>
+template <typename T, int LPRC, int U, int S, int NT, int MINB, bool ATOMIC = false>
 static cudaError_t bwd_staged(const BwdArgs<T>& a, cudaStream_t s) {
     const size_t smem =
         (size_t)S * U * NT * sizeof(Raw16) + (size_t)S * (NT / LPRC) * U * sizeof(T);
-    auto kernel = ws_bwd_staged<T, LPRC, U, S, NT, MINB>;
+    auto kernel = ws_bwd_staged<T, LPRC, U, S, NT, MINB, ATOMIC>;
     cudaError_t e = allow_smem((const void*)kernel, smem);
     if (e != cudaSuccess) return e;
     return launch(kernel, dim3((unsigned)a.P, (unsigned)cdiv(a.Dv, LPRC)), dim3(NT), smem, s,
@@ -648,22 +661,25 @@ static cudaError_t bwd_tile(const BwdArgs<T>& a, cudaStream_t s) {
 // threads, 8 rows per thread per step and 3 steps in flight; rows of 128
 // chunks 128 threads and 4 steps; wider rows 256-chunk slices with 16 bytes
 // of dy per step.
+template <typename T, bool ATOMIC = false>
+static cudaError_t bwd_staged_any(const BwdArgs<T>& a, int lprc, cudaStream_t s) {
+    constexpr int UW = 16 / (int)sizeof(T);
+    switch (lprc) {
+        case 1: return bwd_staged<T, 1, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 2: return bwd_staged<T, 2, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 4: return bwd_staged<T, 4, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 8: return bwd_staged<T, 8, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 16: return bwd_staged<T, 16, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 32: return bwd_staged<T, 32, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 64: return bwd_staged<T, 64, 8, 3, 128, 6, ATOMIC>(a, s);
+        case 128: return bwd_staged<T, 128, 8, 4, 128, 6, ATOMIC>(a, s);
+        default: return bwd_staged<T, 256, UW, 3, 256, 4, ATOMIC>(a, s);
+    }
+}
+
 template <typename T>
 static cudaError_t bwd_vec(const BwdArgs<T>& a, int lprc, bool staged, cudaStream_t s) {
-    constexpr int UW = 16 / (int)sizeof(T);
-    if (staged) {
-        switch (lprc) {
-            case 1: return bwd_staged<T, 1, 8, 3, 128, 6>(a, s);
-            case 2: return bwd_staged<T, 2, 8, 3, 128, 6>(a, s);
-            case 4: return bwd_staged<T, 4, 8, 3, 128, 6>(a, s);
-            case 8: return bwd_staged<T, 8, 8, 3, 128, 6>(a, s);
-            case 16: return bwd_staged<T, 16, 8, 3, 128, 6>(a, s);
-            case 32: return bwd_staged<T, 32, 8, 3, 128, 6>(a, s);
-            case 64: return bwd_staged<T, 64, 8, 3, 128, 6>(a, s);
-            case 128: return bwd_staged<T, 128, 8, 4, 128, 6>(a, s);
-            default: return bwd_staged<T, 256, UW, 3, 256, 4>(a, s);
-        }
-    }
+    if (staged) return bwd_staged_any<T>(a, lprc, s);
     switch (lprc) {
         case 1: return bwd_tile<T, 1>(a, s);
         case 2: return bwd_tile<T, 2>(a, s);
@@ -714,6 +730,62 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
                        (const float*)partial, P, D, grad_w, accumulate);
     }
     return e;
+}
+
+// ---------------------------------------------------------------------------
+// Atomic comparison variant: zero grad_w (unless accumulating), then the
+// staged stage-1 kernel adds each tile's partial row into grad_w with atomic
+// additions.  One launch pair, no workspace, no fixed order.
+__global__ void __launch_bounds__(256) zero_f32(float* __restrict__ p, int64_t n) {
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+        p[i] = 0.f;
+    pdl_trigger();
+}
+
+bool ws_bwd_atomic_supported(const void* x, int64_t ldx, const float* w, const void* dy,
+                             const void* dx, int64_t lddx, const float* grad_w, int64_t D,
+                             int dtype) {
+    const int V = 16 / elt_bytes(dtype);
+    const int64_t Dv = D / V;
+    return D % V == 0 && ldx % V == 0 && lddx % V == 0 && aligned16(x) && aligned16(w) &&
+           aligned16(dx) && aligned16(dy) && aligned16(grad_w) &&
+           cdiv(Dv, Dv <= kSliceChunks ? next_pow2(Dv) : kSliceChunks) <= 65535;
+}
+
+template <typename T>
+static cudaError_t ws_bwd_atomic_t(const T* x, int64_t ldx, const float* w, const T* dy, T* dx,
+                                   int64_t lddx, float* grad_w, int accumulate, int64_t N,
+                                   int64_t D, int dtype, cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    cudaError_t e = cudaSuccess;
+    if (!accumulate) {
+        e = launch(zero_f32, dim3((unsigned)std::min<int64_t>(cdiv(D, 256), 1024)), dim3(256), 0,
+                   s, true, grad_w, D);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t P = ws_tiles(N, D, dtype, 0);
+    if (P == 0) return e;
+    const int64_t Dv = D / V;
+    const int lprc = Dv <= kSliceChunks ? next_pow2(Dv) : kSliceChunks;
+    BwdArgs<T> a{x, ldx, w, dy, dx, lddx, grad_w, N, Dv, D, 0, P};
+    return bwd_staged_any<T, true>(a, lprc, s);
+}
+
+cudaError_t launch_ws_bwd_atomic(const void* x, int64_t ldx, const float* w, const void* dy,
+                                 void* dx, int64_t lddx, float* grad_w, int accumulate, int64_t N,
+                                 int64_t D, int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return ws_bwd_atomic_t((const float*)x, ldx, w, (const float*)dy, (float*)dx, lddx,
+                                   grad_w, accumulate, N, D, dtype, s);
+        case 1:
+            return ws_bwd_atomic_t((const __half*)x, ldx, w, (const __half*)dy, (__half*)dx, lddx,
+                                   grad_w, accumulate, N, D, dtype, s);
+        default:
+            return ws_bwd_atomic_t((const __nv_bfloat16*)x, ldx, w, (const __nv_bfloat16*)dy,
+                                   (__nv_bfloat16*)dx, lddx, grad_w, accumulate, N, D, dtype, s);
+    }
 }
 
 cudaError_t launch_ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,

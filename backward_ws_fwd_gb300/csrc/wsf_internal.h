@@ -26,6 +26,16 @@ cudaError_t launch_ws_bwd(const void* x, int64_t ldx, const float* w, const void
                           int64_t lddx, float* grad_w, int accumulate, float* partial,
                           int64_t block_n, int64_t N, int64_t D, int dtype, cudaStream_t s);
 
+// Atomic comparison variants (grad_w / dw summed with atomic additions).
+bool ws_bwd_atomic_supported(const void* x, int64_t ldx, const float* w, const void* dy,
+                             const void* dx, int64_t lddx, const float* grad_w, int64_t D,
+                             int dtype);
+cudaError_t launch_ws_bwd_atomic(const void* x, int64_t ldx, const float* w, const void* dy,
+                                 void* dx, int64_t lddx, float* grad_w, int accumulate, int64_t N,
+                                 int64_t D, int dtype, cudaStream_t s);
+cudaError_t launch_silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx,
+                                   float* dw, int accumulate, int64_t n, int dtype, cudaStream_t s);
+
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);
 

@@ -513,6 +513,65 @@ def scaled_workloads(scale: float):
     return {k: dataclasses.replace(v, N=max(1, int(round(v.N * scale)))) for k, v in WORKLOADS.items()}
 
 
+def run_compare_atomic(args, names):
+    """Measured comparison of the deterministic two-pass backward with the
+    atomic-add variant (the pages' own scheme): mean backward time over K
+    launches each, and how many distinct bit patterns grad_w / dw takes over
+    the same K runs.  Prints one JSON line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import backward_ws_fwd_gb300 as wsf
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    WL = scaled_workloads(args.scale)
+    out = {}
+    for n in names:
+        b = Buffers(WL[n], dev, wsf, host_io=False)
+        wl = b.wl
+
+        def two():
+            b.run(wsf, "bwd")
+            return b.gw
+
+        def atom():
+            if wl.op == "ws":
+                wsf.ws_bwd_atomic(b.x, b.w, b.dy, dx=b.dx, grad_w=b.gw)
+            else:
+                wsf.silu_bwd_atomic(b.dy, b.x, b.w, dx=b.dx, dw=b.gw)
+            return b.gw
+
+        res = {}
+        for label, fn in (("two_pass", two), ("atomic", atom)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            pats = set()
+            ms = []
+            for _ in range(args.steps):
+                a = torch.cuda.Event(enable_timing=True)
+                c = torch.cuda.Event(enable_timing=True)
+                a.record()
+                g = fn()
+                c.record()
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(c))
+                pats.add(bytes(g.view(torch.int32).cpu().numpy()))
+            mean = sum(ms) / len(ms)
+            res[label] = {"ms": round(mean, 4),
+                          "GB/s": round(op_bytes(wl, "bwd") / (mean * 1e-3) / 1e9, 1),
+                          "distinct_gradient_bit_patterns": len(pats)}
+        res["atomic_speedup"] = round(res["two_pass"]["ms"] / res["atomic"]["ms"], 4)
+        out[n] = res
+        del b
+        torch.cuda.empty_cache()
+    print(json.dumps({"comparison": "backward: deterministic two-pass vs atomic-add parameter "
+                                    "gradient", "runs_per_variant": args.steps,
+                      "note": "each run timed alone with events (sync between runs)",
+                      "per_workload": out}), flush=True)
+    return 0
+
+
 def read_traffic(kernel: str, workload: str):
     """DRAM bytes per launch measured by ncu for this kernel and workload,
     from profiles/traffic.json, if a capture of the current source exists."""
@@ -548,6 +607,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="all", help="all or a comma list of c2,c3,c4,c5")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="multiply every workload's row count (profiling on small cases)")
+    ap.add_argument("--compare-atomic", action="store_true",
+                    help="measure the atomic-add backward variants against the two-pass ones")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -557,6 +618,8 @@ def main(argv=None):
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         return run_reference(args, names)
+    if args.compare_atomic:
+        return run_compare_atomic(args, names)
     return run_cuda(args, names)
 
 

@@ -176,6 +176,29 @@ size_t silu_bwd_workspace_bytes(int64_t n, int dtype);
 int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw, int accumulate,
              void* workspace, size_t workspace_bytes, int64_t n, int dtype, wsf_stream_t stream);
 
+/*
+ * Atomic comparison variants  [SILU, backward kernel: per-block sums added
+ * into one fp32 cell with an atomic add; § The backward grid is not the
+ * forward grid: "atomics (small, non-critical)" versus the two-pass partials
+ * buffer; VJP §02 The kernel consequence: "atomicAdd, split-K, or a separate
+ * reduction pass"; §06: atomic adds are nondeterministic by default].
+ *
+ * Same results as ws_bwd / silu_bwd up to fp32 rounding, but the parameter
+ * gradient is summed with atomic additions in whatever order the blocks
+ * finish, so its bits may differ from run to run; they exist to measure what
+ * the deterministic two-pass form costs.  No workspace: grad_w / dw is
+ * zeroed first (unless accumulate == 1) and every row tile adds its partial
+ * into it.  ws_bwd_atomic supports only the 16-byte-aligned layout of the
+ * staged path (x, dx, w, dy, grad_w 16-byte aligned; D, ldx, lddx multiples
+ * of 16 bytes) and returns WSF_ERR_MISALIGNED otherwise.  Other arguments and
+ * errors as for ws_bwd / silu_bwd.
+ */
+int ws_bwd_atomic(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                  int64_t lddx, float* grad_w, int accumulate, int64_t N, int64_t D, int dtype,
+                  wsf_stream_t stream);
+int silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                    int accumulate, int64_t n, int dtype, wsf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -152,3 +152,35 @@ def test_silu_rejects(wsf):
     assert call(dx=2 * F + 100) == wsf.ERR_OVERLAP
     assert call(dw=6 * F + 8) == wsf.ERR_OVERLAP
     assert call(x=2 * F + 1) == wsf.ERR_MISALIGNED
+
+
+def test_atomic_variants_reject(wsf):
+    L = wsf.lib
+    s = None
+    ok = dict(x=F, ldx=64, w=2 * F, dy=3 * F, dx=4 * F, lddx=64, gw=5 * F, acc=0, N=100, D=64, dt=1)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        P = lambda v: _p(v) if v else None  # noqa: E731
+        return L.ws_bwd_atomic(P(a["x"]), a["ldx"], P(a["w"]), P(a["dy"]), P(a["dx"]), a["lddx"],
+                               P(a["gw"]), a["acc"], a["N"], a["D"], a["dt"], s)
+
+    assert call(dt=4) == wsf.ERR_BAD_DTYPE
+    assert call(N=-1) == wsf.ERR_BAD_SHAPE
+    assert call(acc=5) == wsf.ERR_BAD_ARG
+    assert call(ldx=3) == wsf.ERR_BAD_STRIDE
+    assert call(gw=0) == wsf.ERR_NULL_PTR
+    assert call(dy=3 * F + 2) == wsf.ERR_MISALIGNED  # staged layout only
+    assert call(D=60, ldx=60, lddx=60) == wsf.ERR_MISALIGNED
+    assert call(dx=F + 16) == wsf.ERR_OVERLAP
+    sa = lambda **kw: L.silu_bwd_atomic(*(  # noqa: E731
+        [_p(kw.get("dy", F)), _p(kw.get("x", 2 * F)), _p(kw.get("w", 3 * F)),
+         _p(kw.get("dx", 4 * F)) if kw.get("dx", 4 * F) else None,
+         _p(kw.get("dw", 5 * F)) if kw.get("dw", 5 * F) else None,
+         kw.get("acc", 0), kw.get("n", 100), kw.get("dt", 1), s]))
+    assert sa(dt=9) == wsf.ERR_BAD_DTYPE
+    assert sa(n=-3) == wsf.ERR_BAD_SHAPE
+    assert sa(acc=2) == wsf.ERR_BAD_ARG
+    assert sa(dw=0) == wsf.ERR_NULL_PTR
+    assert sa(dx=2 * F + 50) == wsf.ERR_OVERLAP
