@@ -61,6 +61,10 @@ def lib():
         L.orc_silu_fwd.restype = _int
         L.orc_silu_bwd.argtypes = [_vp, _vp, _dbl, _i64, _int, _vp, _vp, _vp, _vp, _vp]
         L.orc_silu_bwd.restype = _int
+        L.orc_softmax_fwd.argtypes = [_vp, _i64, _i64, _i64, _int, _vp, _vp]
+        L.orc_softmax_fwd.restype = _int
+        L.orc_softmax_bwd.argtypes = [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _vp]
+        L.orc_softmax_bwd.restype = _int
         _lib = L
     return _lib
 
@@ -174,3 +178,32 @@ def silu_bwd(dy, x, w: float, *, want_dx=True, want_dw=True):
                               _ptr(dwa) if want_dw else None), "silu_bwd")
     out.update(dx_exact=dxe, dx_scale=dxs, dx=dx, dw=float(dw[0]), dw_abs=float(dwa[0]))
     return out
+
+
+# ---------------------------------------------------------------- softmax
+def softmax_fwd(x):
+    """x: host tensor [N, D] (unit inner stride).  Returns (y_exact fp64
+    [N, D], y_out tensor [N, D] in x's dtype)."""
+    import torch
+    assert x.dim() == 2 and x.stride(1) == 1
+    N, D = x.shape
+    ye = np.empty((N, D), np.float64)
+    yo = torch.empty((N, D), dtype=x.dtype)
+    _check(lib().orc_softmax_fwd(_ptr(x), x.stride(0) if N > 0 else D, N, D,
+                                 DTYPE_CODE[_dt_of(x)], _ptr(ye), _ptr(yo)), "softmax_fwd")
+    return ye, yo
+
+
+def softmax_bwd(y, dy):
+    """y, dy: contiguous host tensors [N, D].  Returns dict dx_exact,
+    dx_scale (fp64 [N, D]), dx (tensor), s (fp64 [N])."""
+    import torch
+    assert y.is_contiguous() and dy.is_contiguous() and y.dtype == dy.dtype
+    N, D = y.shape
+    dxe = np.empty((N, D), np.float64)
+    dxs = np.empty((N, D), np.float64)
+    dx = torch.empty((N, D), dtype=y.dtype)
+    s = np.empty(N, np.float64)
+    _check(lib().orc_softmax_bwd(_ptr(y), _ptr(dy), N, D, DTYPE_CODE[_dt_of(y)], _ptr(dxe),
+                                 _ptr(dxs), _ptr(dx), _ptr(s)), "softmax_bwd")
+    return {"dx_exact": dxe, "dx_scale": dxs, "dx": dx, "s": s}

@@ -323,3 +323,67 @@ int orc_silu_bwd(const void* dy, const void* x, double w, int64_t n, int dt, dou
     free(ta);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Softmax over rows  ["Backprop for kernel writers", §04 The duality:  */
+/* softmax backward collapses the dense Jacobian to one row scalar]:    */
+/*   y[i,j]  = exp(x[i,j] - m_i) / Σ_k exp(x[i,k] - m_i),  m_i = max_k x */
+/*   dx[i,j] = y[i,j] · (dy[i,j] - s_i),  s_i = Σ_k dy[i,k] · y[i,k]     */
+/* ------------------------------------------------------------------ */
+
+/* x [N, D] (row stride ldx), storage dt.  Outputs (any may be NULL):
+ * y_exact [N*D] contiguous fp64, y_out [N, D] contiguous in dt. */
+int orc_softmax_fwd(const void* x, int64_t ldx, int64_t N, int64_t D, int dt, double* y_exact,
+                    void* y_out) {
+    if (!x || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* e = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    if (!e) return -2;
+    for (int64_t i = 0; i < N; i++) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < D; j++) {
+            const double v = decode(x, i * ldx + j, dt);
+            if (v > m) m = v;
+        }
+        for (int64_t j = 0; j < D; j++) e[j] = exp(decode(x, i * ldx + j, dt) - m);
+        const double S = orc_pairwise_sum(e, D);
+        for (int64_t j = 0; j < D; j++) {
+            const double y = e[j] / S;
+            if (y_exact) y_exact[i * D + j] = y;
+            if (y_out) store(y_out, i * D + j, dt, y);
+        }
+    }
+    free(e);
+    return 0;
+}
+
+/* y, dy [N, D] contiguous in dt (y is the forward's stored output).
+ * Outputs (any may be NULL): dx_exact, dx_scale = |y|·(|dy| + Σ_k |dy_k·y_k|)
+ * (the magnitude of the two cancelling terms), dx_out (dt), s_exact [N]. */
+int orc_softmax_bwd(const void* y, const void* dy, int64_t N, int64_t D, int dt, double* dx_exact,
+                    double* dx_scale, void* dx_out, double* s_exact) {
+    if (!y || !dy || N < 0 || D < 0 || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* t = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    double* ta = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+    if (!t || !ta) { free(t); free(ta); return -2; }
+    for (int64_t i = 0; i < N; i++) {
+        for (int64_t j = 0; j < D; j++) {
+            t[j] = decode(dy, i * D + j, dt) * decode(y, i * D + j, dt);
+            ta[j] = fabs(t[j]);
+        }
+        const double s = orc_pairwise_sum(t, D);
+        const double sa = orc_pairwise_sum(ta, D);
+        if (s_exact) s_exact[i] = s;
+        for (int64_t j = 0; j < D; j++) {
+            const double yv = decode(y, i * D + j, dt), g = decode(dy, i * D + j, dt);
+            const double dx = yv * (g - s);
+            if (dx_exact) dx_exact[i * D + j] = dx;
+            if (dx_scale) dx_scale[i * D + j] = fabs(yv) * (fabs(g) + sa);
+            if (dx_out) store(dx_out, i * D + j, dt, dx);
+        }
+    }
+    free(t);
+    free(ta);
+    return 0;
+}
