@@ -46,6 +46,10 @@ lib.ws_bwd_atomic.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _int, _i64, _
 lib.ws_bwd_atomic.restype = _int
 lib.silu_bwd_atomic.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _i64, _int, _vp]
 lib.silu_bwd_atomic.restype = _int
+lib.softmax_fwd.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]
+lib.softmax_fwd.restype = _int
+lib.softmax_bwd.argtypes = [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]
+lib.softmax_bwd.restype = _int
 lib.silu_fwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
 lib.silu_fwd.restype = _int
 lib.silu_bwd_workspace_bytes.argtypes = [_i64, _int]
@@ -188,6 +192,28 @@ def silu_bwd_atomic(dy, x, w, dx=None, dw=None, accumulate=False, stream=None):
     return dx, dw
 
 
+def softmax_fwd(x, y=None, stream=None):
+    """Row softmax of x [N, D] (unit inner stride); y has x's type."""
+    import torch
+    N, D = x.shape
+    if y is None:
+        y = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    _check(lib.softmax_fwd(_ptr(x), x.stride(0), _ptr(y), y.stride(0), N, D, _dtype_code(x),
+                           _stream(stream)), "softmax_fwd")
+    return y
+
+
+def softmax_bwd(y, dy, dx=None, stream=None):
+    """dx = y ⊙ (dy − Σ_j dy·y) per row, from the forward's output y."""
+    import torch
+    N, D = y.shape
+    if dx is None:
+        dx = torch.empty((N, D), dtype=y.dtype, device=y.device)
+    _check(lib.softmax_bwd(_ptr(y), y.stride(0), _ptr(dy), dy.stride(0), _ptr(dx), dx.stride(0),
+                           N, D, _dtype_code(y), _stream(stream)), "softmax_bwd")
+    return dx
+
+
 def silu_fwd(x, w, y=None, stream=None):
     """y = w·x·sigmoid(x).  x contiguous (any shape); w: one float32 on the device."""
     import torch
@@ -220,5 +246,5 @@ def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, strea
 
 
 __all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
-           "ws_bwd_atomic", "silu_bwd_atomic", "silu_fwd",
+           "ws_bwd_atomic", "silu_bwd_atomic", "softmax_fwd", "softmax_bwd", "silu_fwd",
            "silu_bwd", "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "F32", "F16", "BF16"]

@@ -228,4 +228,41 @@ int silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx, flo
                                                    (cudaStream_t)stream));
 }
 
+int softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t N, int64_t D, int dtype,
+                wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldx < D || ldy < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = mat ? extent_bytes(N, D, ldx, es) : 0;
+    const int64_t yb = mat ? extent_bytes(N, D, ldy, es) : 0;
+    if (xb < 0 || yb < 0) return WSF_ERR_BAD_SHAPE;
+    if (mat && (!x || !y)) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(y, es)) return WSF_ERR_MISALIGNED;
+    if (!mat) return WSF_OK;
+    if (overlap(span(y, yb), span(x, xb))) return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_softmax_fwd(x, ldx, y, ldy, N, D, dtype, (cudaStream_t)stream));
+}
+
+int softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* dx, int64_t lddx,
+                int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldy < D || lddy < D || lddx < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t yb = mat ? extent_bytes(N, D, ldy, es) : 0;
+    const int64_t gb = mat ? extent_bytes(N, D, lddy, es) : 0;
+    const int64_t xb = mat ? extent_bytes(N, D, lddx, es) : 0;
+    if (yb < 0 || gb < 0 || xb < 0) return WSF_ERR_BAD_SHAPE;
+    if (mat && (!y || !dy || !dx)) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(y, es) || !aligned_to(dy, es) || !aligned_to(dx, es)) return WSF_ERR_MISALIGNED;
+    if (!mat) return WSF_OK;
+    const Span sdx = span(dx, xb);
+    if (overlap(sdx, span(y, yb)) || overlap(sdx, span(dy, gb))) return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_softmax_bwd(y, ldy, dy, lddy, dx, lddx, N, D, dtype,
+                                               (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -1,0 +1,529 @@
+// softmax.cu — row softmax forward and backward for sm_103a.
+//
+// "Backprop for kernel writers", §04 The duality: the softmax backward is a
+// row-scalar collapse, dx = y ⊙ (dy − Σ_j dy_j·y_j), computed from the saved
+// output y ("you need y, not x"), so the dense Jacobian is never formed; the
+// stability shift of the forward (x − max x) adds nothing to the backward.
+//
+// Forward:  y[i,j] = exp(x[i,j] − m_i) / Σ_k exp(x[i,k] − m_i),  m_i = max_k x[i,k]
+// Backward: dx[i,j] = y[i,j] · (dy[i,j] − s_i),  s_i = Σ_k dy[i,k]·y[i,k]
+//
+// Row path (16-byte aligned rows of up to 2048 chunks): a row is held in
+// registers by a group of TPR threads (CPT 16-byte chunks each); the row max
+// and the row sums are combined with xor butterflies inside a warp and, for
+// groups wider than a warp, through shared memory in warp order.  x (or y and
+// dy) is read once and y (dx) written once.  Wide or unaligned rows take a
+// multi-pass path with one CTA per row.  Sums of binary32 rows are
+// compensated and their exponents taken of exactly split differences.
+#include <algorithm>
+#include <type_traits>
+
+#include "wsf_device.cuh"
+#include "wsf_internal.h"
+
+namespace wsf {
+
+template <typename T>
+constexpr bool kSoftmaxFast = !std::is_same<T, float>::value;
+
+// exp(a − b).  For binary32 storage the difference is split exactly into
+// s + e (TwoSum) and exp(s)·(1 + e) is returned, so the rounding of a − b
+// (up to |a − b|·2^-24 in the exponent) does not reach the result; 16-bit
+// storage uses the hardware exponential of the rounded difference.
+template <bool Fast>
+__device__ __forceinline__ float exp_diff(float a, float b) {
+    if constexpr (Fast) {
+        return __expf(a - b);
+    } else {
+        float d, e;
+        two_sum(a, -b, d, e);
+        const float r = expf(d);
+        return fmaf(r, e, r);
+    }
+}
+
+// Reductions over a group of TPR threads (aligned, consecutive).  Groups of
+// more than 32 threads combine per-warp results through `red` (NT/32 floats)
+// in warp order; every thread of the CTA must call these together.
+template <int TPR>
+__device__ __forceinline__ float group_max(float v, float* red) {
+    constexpr int W = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int off = W / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
+    if constexpr (TPR > 32) {
+        const int wid = threadIdx.x >> 5, first = (threadIdx.x / TPR) * (TPR / 32);
+        if ((threadIdx.x & 31) == 0) red[wid] = v;
+        __syncthreads();
+        v = red[first];
+#pragma unroll
+        for (int q = 1; q < TPR / 32; q++) v = fmaxf(v, red[first + q]);
+        __syncthreads();
+    }
+    return v;
+}
+
+// Plain fp32 group sum with the same combination order as group_sum_acc2
+// (xor butterfly in each warp, warps in index order), for 16-bit storage.
+template <int TPR>
+__device__ __forceinline__ float group_sum_plain(float v, float* red) {
+    constexpr int W = TPR < 32 ? TPR : 32;
+    v = group_sum<W>(v);
+    if constexpr (TPR > 32) {
+        const int wid = threadIdx.x >> 5, first = (threadIdx.x / TPR) * (TPR / 32);
+        if ((threadIdx.x & 31) == 0) red[wid] = v;
+        __syncthreads();
+        v = red[first];
+#pragma unroll
+        for (int q = 1; q < TPR / 32; q++) v += red[first + q];
+        __syncthreads();
+    }
+    return v;
+}
+
+template <int TPR>
+__device__ __forceinline__ Acc2 group_sum_acc2(Acc2 v, Acc2* red) {
+    constexpr int W = TPR < 32 ? TPR : 32;
+    v = group_sum2<W>(v);
+    if constexpr (TPR > 32) {
+        const int wid = threadIdx.x >> 5, first = (threadIdx.x / TPR) * (TPR / 32);
+        if ((threadIdx.x & 31) == 0) red[wid] = v;
+        __syncthreads();
+        v = red[first];
+#pragma unroll
+        for (int q = 1; q < TPR / 32; q++) v = acc2_add(v, red[first + q]);
+        __syncthreads();
+    }
+    return v;
+}
+
+
+// 16-bit rows: the maximum of a 16-byte chunk taken on packed pairs (exact),
+// and e^(x − m) as 2^(x·log2(e) − m·log2(e)) with the argument formed by one
+// FMA and the hardware base-2 exponential.
+template <typename T>
+__device__ __forceinline__ float chunk_max16(const Raw16& r) {
+    if constexpr (std::is_same<T, __half>::value) {
+        __half2 m;
+        memcpy(&m, &r.u[0], 4);
+#pragma unroll
+        for (int i = 1; i < 4; i++) {
+            __half2 h;
+            memcpy(&h, &r.u[i], 4);
+            m = __hmax2(m, h);
+        }
+        return fmaxf(__low2float(m), __high2float(m));
+    } else {
+        __nv_bfloat162 m;
+        memcpy(&m, &r.u[0], 4);
+#pragma unroll
+        for (int i = 1; i < 4; i++) {
+            __nv_bfloat162 h;
+            memcpy(&h, &r.u[i], 4);
+            m = __hmax2(m, h);
+        }
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float exp2_approx(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Compensated (binary32) or plain (16-bit) running sum.
+template <bool Comp>
+__device__ __forceinline__ void add_to(Acc2& a, float v) {
+    if constexpr (Comp) {
+        float s, e;
+        two_sum(a.hi, v, s, e);
+        a.hi = s;
+        a.lo += e;
+    } else {
+        a.hi += v;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row path.  Each CTA takes R = NT / TPR rows per iteration (grid-stride
+// over iterations k = 0, 1, ...).  Every thread copies its own chunks of the
+// rows of iteration k + S - 1 into private shared-memory slots with cp.async
+// while it computes iteration k, so S - 1 iterations' loads are in flight
+// without holding registers; only the row reductions synchronise threads.
+template <int TPR, int CPT, int NT, int S>
+struct RowStage {
+    static constexpr size_t bytes(int arrays) { return (size_t)arrays * S * CPT * NT * 16; }
+};
+
+template <typename T, int TPR, int CPT, int NT>
+__device__ __forceinline__ void stage_row(Raw16* slots, const T* __restrict__ p, int64_t ld,
+                                          int64_t row, int64_t N, int Dv, int l) {
+    constexpr int V = Elt<T>::V;
+#pragma unroll
+    for (int k = 0; k < CPT; k++) {
+        const int c = l + k * TPR;
+        const bool ok = row < N && c < Dv;
+        cp_async16(&slots[k * NT + threadIdx.x],
+                   ok ? (const void*)(p + row * ld + (int64_t)c * V) : (const void*)p, ok ? 16 : 0);
+    }
+}
+
+template <typename T, int TPR, int CPT, int NT, int S>
+__global__ void __launch_bounds__(NT)
+    softmax_fwd_rows(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
+                     int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    constexpr int R = NT / TPR;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* slots = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    __shared__ float redm[NT / 32];
+    __shared__ Acc2 reds[NT / 32];
+    const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
+    pdl_wait();
+    const int64_t first = (int64_t)blockIdx.x * R + g, stride = (int64_t)gridDim.x * R;
+    const int64_t iters = ((int64_t)blockIdx.x * R < N) ? (N - (int64_t)blockIdx.x * R + stride - 1) / stride : 0;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) stage_row<T, TPR, CPT, NT>(slots + k * CPT * NT, x, ldx, first + k * stride, N, Dv, l);
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters)
+            stage_row<T, TPR, CPT, NT>(slots + (nk % S) * CPT * NT, x, ldx, first + nk * stride, N, Dv, l);
+        cp_async_commit();
+        const int64_t row = first + k * stride;
+        const bool rok = row < N;
+        const Raw16* cur = slots + (k % S) * CPT * NT;
+        if constexpr (!kComp) {
+            // 16-bit storage: packed max, one FMA + ex2 per element, plain sums
+            float m = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < CPT; c++)
+                if (rok && l + c * TPR < Dv) m = fmaxf(m, chunk_max16<T>(cur[c * NT + threadIdx.x]));
+            m = group_max<TPR>(m, redm);
+            const float ms = m * kLog2e;
+            float f[CPT][V];
+            float st = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                E::widen(cur[c * NT + threadIdx.x], f[c]);
+                const bool ok = rok && l + c * TPR < Dv;
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    f[c][v] = ok ? exp2_approx(fmaf(f[c][v], kLog2e, -ms)) : 0.f;
+                    st += f[c][v];
+                }
+            }
+            const float inv = 1.0f / group_sum_plain<TPR>(st, redm);
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                if (rok && l + c * TPR < Dv) {
+                    float o[V];
+#pragma unroll
+                    for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
+                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                }
+            }
+            continue;
+        }
+        float f[CPT][V];
+        bool cok[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            cok[c] = rok && l + c * TPR < Dv;
+            E::widen(cur[c * NT + threadIdx.x], f[c]);
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+            if (cok[c])
+#pragma unroll
+                for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
+        m = group_max<TPR>(m, redm);
+        Acc2 s = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+#pragma unroll
+            for (int v = 0; v < V; v++) {
+                f[c][v] = cok[c] ? exp_diff<kSoftmaxFast<T>>(f[c][v], m) : 0.f;
+                add_to<kComp>(s, f[c][v]);
+            }
+        }
+        s = group_sum_acc2<TPR>(s, reds);
+        const float inv = 1.0f / (s.hi + s.lo);
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (cok[c]) {
+                float o[V];
+#pragma unroll
+                for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
+                st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+            }
+        }
+    }
+    cp_async_wait<0>();
+    pdl_trigger();
+}
+
+template <typename T, int TPR, int CPT, int NT, int S>
+__global__ void __launch_bounds__(NT)
+    softmax_bwd_rows(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy, int64_t lddy,
+                     T* __restrict__ dx, int64_t lddx, int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    constexpr int R = NT / TPR;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* ys = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    Raw16* gs = ys + S * CPT * NT;                    // [S][CPT][NT]
+    __shared__ Acc2 reds[NT / 32];
+    __shared__ float redf[NT / 32];
+    const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
+    pdl_wait();
+    const int64_t first = (int64_t)blockIdx.x * R + g, stride = (int64_t)gridDim.x * R;
+    const int64_t iters = ((int64_t)blockIdx.x * R < N) ? (N - (int64_t)blockIdx.x * R + stride - 1) / stride : 0;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) {
+            stage_row<T, TPR, CPT, NT>(ys + k * CPT * NT, y, ldy, first + k * stride, N, Dv, l);
+            stage_row<T, TPR, CPT, NT>(gs + k * CPT * NT, dy, lddy, first + k * stride, N, Dv, l);
+        }
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters) {
+            stage_row<T, TPR, CPT, NT>(ys + (nk % S) * CPT * NT, y, ldy, first + nk * stride, N, Dv, l);
+            stage_row<T, TPR, CPT, NT>(gs + (nk % S) * CPT * NT, dy, lddy, first + nk * stride, N, Dv, l);
+        }
+        cp_async_commit();
+        const int64_t row = first + k * stride;
+        const bool rok = row < N;
+        const Raw16* cy = ys + (k % S) * CPT * NT;
+        const Raw16* cg = gs + (k % S) * CPT * NT;
+        float fy[CPT][V], fg[CPT][V];
+        bool cok[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            cok[c] = rok && l + c * TPR < Dv;
+            E::widen(cy[c * NT + threadIdx.x], fy[c]);
+            E::widen(cg[c * NT + threadIdx.x], fg[c]);
+        }
+        Acc2 s = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+#pragma unroll
+            for (int v = 0; v < V; v++) {
+                if constexpr (kComp)
+                    acc2_fma(s, fg[c][v], fy[c][v]);
+                else
+                    s.hi = fmaf(fg[c][v], fy[c][v], s.hi);
+            }
+        float sv;
+        if constexpr (kComp) {
+            s = group_sum_acc2<TPR>(s, reds);
+            sv = s.hi + s.lo;
+        } else {
+            sv = group_sum_plain<TPR>(s.hi, redf);
+        }
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (cok[c]) {
+                float o[V];
+#pragma unroll
+                for (int v = 0; v < V; v++) o[v] = fy[c][v] * (fg[c][v] - sv);
+                st_stream(dx + row * lddx + (int64_t)(l + c * TPR) * V, E::narrow(o));
+            }
+        }
+    }
+    cp_async_wait<0>();
+    pdl_trigger();
+}
+
+// Wide path: one CTA per row (grid-stride), element-wise loads, three passes
+// over the row (max, sum of exponentials, write), each reduction combining the
+// threads in a fixed order.
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT)
+    softmax_fwd_wide(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
+                     int64_t N, int64_t D) {
+    using E = Elt<T>;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    __shared__ float redm[NT / 32];
+    __shared__ Acc2 reds[NT / 32];
+    pdl_wait();
+    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+        const T* xr = x + row * ldx;
+        float m = -INFINITY;
+        for (int64_t j = threadIdx.x; j < D; j += NT) m = fmaxf(m, E::load1(xr + j));
+        m = group_max<NT>(m, redm);
+        Acc2 s = acc2_zero();
+        for (int64_t j = threadIdx.x; j < D; j += NT)
+            add_to<kComp>(s, exp_diff<kSoftmaxFast<T>>(E::load1(xr + j), m));
+        s = group_sum_acc2<NT>(s, reds);
+        const float inv = 1.0f / (s.hi + s.lo);
+        for (int64_t j = threadIdx.x; j < D; j += NT)
+            E::store1(y + row * ldy + j, exp_diff<kSoftmaxFast<T>>(E::load1(xr + j), m) * inv);
+    }
+    pdl_trigger();
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT)
+    softmax_bwd_wide(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy, int64_t lddy,
+                     T* __restrict__ dx, int64_t lddx, int64_t N, int64_t D) {
+    using E = Elt<T>;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    __shared__ Acc2 red[NT / 32];
+    pdl_wait();
+    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+        Acc2 s = acc2_zero();
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float a = E::load1(dy + row * lddy + j), b = E::load1(y + row * ldy + j);
+            if constexpr (kComp)
+                acc2_fma(s, a, b);
+            else
+                s.hi = fmaf(a, b, s.hi);
+        }
+        s = group_sum_acc2<NT>(s, red);
+        const float sv = s.hi + s.lo;
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float yv = E::load1(y + row * ldy + j);
+            E::store1(dx + row * lddx + j, yv * (E::load1(dy + row * lddy + j) - sv));
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static inline int next_pow2(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+constexpr int kSoftmaxRowChunks = 2048;  // rows of up to 32 KB stay in registers
+
+// Raise a kernel's dynamic shared-memory limit (idempotent, cheap); done from
+// 32 KB up because the kernels' static shared memory counts against the
+// default 48 KB too.
+static cudaError_t allow_smem_sm(const void* kernel, size_t bytes) {
+    if (bytes < 32 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Row-path shapes: TPR threads per row, CPT chunks per thread, 256-thread
+// CTAs; S stages of staged rows (fewer for wide rows to bound shared memory).
+template <int TPR, int CPT, int S, typename F>
+static cudaError_t with_rows(int64_t N, F&& go) {
+    constexpr int NT = 256;
+    constexpr int R = NT / TPR;
+    const int64_t grid = std::min<int64_t>(cdiv(N, R), 8 * kDesignSMs);
+    return go(std::integral_constant<int, TPR>{}, std::integral_constant<int, CPT>{},
+              std::integral_constant<int, S>{}, dim3((unsigned)grid), dim3(NT));
+}
+
+// Measured on GB300 for rows of 512 chunks (4096 bf16): forward 128 threads x
+// 4 chunks, backward 64 x 8, two stages; other widths follow the same idea.
+template <bool Fwd, typename F>
+static cudaError_t dispatch_rows(int64_t Dv, int64_t N, F&& go) {
+    if (Dv <= 32) {
+        switch (next_pow2(Dv)) {
+            case 1: return with_rows<1, 1, 4>(N, go);
+            case 2: return with_rows<2, 1, 4>(N, go);
+            case 4: return with_rows<4, 1, 4>(N, go);
+            case 8: return with_rows<8, 1, 4>(N, go);
+            case 16: return with_rows<16, 1, 4>(N, go);
+            default: return with_rows<32, 1, 4>(N, go);
+        }
+    }
+    if (Dv <= 64) return with_rows<32, 2, 4>(N, go);
+    if (Dv <= 128) return with_rows<32, 4, 3>(N, go);
+    if (Dv <= 256) return with_rows<32, 8, 2>(N, go);
+    if (Dv <= 512) {
+        if constexpr (Fwd) return with_rows<128, 4, 2>(N, go);
+        else return with_rows<64, 8, 2>(N, go);
+    }
+    if (Dv <= 1024) return with_rows<128, 8, 2>(N, go);
+    return with_rows<256, 8, 2>(N, go);
+}
+
+template <typename T>
+static cudaError_t softmax_fwd_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N, int64_t D,
+                                 cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    const int64_t Dv = D / V;
+    if (D % V == 0 && ldx % V == 0 && ldy % V == 0 && aligned16(x) && aligned16(y) &&
+        Dv <= kSoftmaxRowChunks) {
+        return dispatch_rows<true>(Dv, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
+            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+            constexpr int S = decltype(st)::value;
+            auto k = softmax_fwd_rows<T, TPR, CPT, 256, S>;
+            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(1);
+            cudaError_t e = allow_smem_sm((const void*)k, smem);
+            if (e != cudaSuccess) return e;
+            return launch(k, grid, block, smem, s, true, x, ldx, y, ldy, N, (int)Dv);
+        });
+    }
+    constexpr int NT = 256;
+    return launch(softmax_fwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
+                  dim3(NT), 0, s, true, x, ldx, y, ldy, N, D);
+}
+
+template <typename T>
+static cudaError_t softmax_bwd_t(const T* y, int64_t ldy, const T* dy, int64_t lddy, T* dx,
+                                 int64_t lddx, int64_t N, int64_t D, cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    const int64_t Dv = D / V;
+    if (D % V == 0 && ldy % V == 0 && lddy % V == 0 && lddx % V == 0 && aligned16(y) &&
+        aligned16(dy) && aligned16(dx) && Dv <= kSoftmaxRowChunks) {
+        return dispatch_rows<false>(Dv, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
+            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+            constexpr int S = decltype(st)::value;
+            auto k = softmax_bwd_rows<T, TPR, CPT, 256, S>;
+            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(2);
+            cudaError_t e = allow_smem_sm((const void*)k, smem);
+            if (e != cudaSuccess) return e;
+            return launch(k, grid, block, smem, s, true, y, ldy, dy, lddy, dx, lddx, N, (int)Dv);
+        });
+    }
+    constexpr int NT = 256;
+    return launch(softmax_bwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
+                  dim3(NT), 0, s, true, y, ldy, dy, lddy, dx, lddx, N, D);
+}
+
+cudaError_t launch_softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t N,
+                               int64_t D, int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case 0: return softmax_fwd_t((const float*)x, ldx, (float*)y, ldy, N, D, s);
+        case 1: return softmax_fwd_t((const __half*)x, ldx, (__half*)y, ldy, N, D, s);
+        default:
+            return softmax_fwd_t((const __nv_bfloat16*)x, ldx, (__nv_bfloat16*)y, ldy, N, D, s);
+    }
+}
+
+cudaError_t launch_softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* dx,
+                               int64_t lddx, int64_t N, int64_t D, int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return softmax_bwd_t((const float*)y, ldy, (const float*)dy, lddy, (float*)dx, lddx, N,
+                                 D, s);
+        case 1:
+            return softmax_bwd_t((const __half*)y, ldy, (const __half*)dy, lddy, (__half*)dx, lddx,
+                                 N, D, s);
+        default:
+            return softmax_bwd_t((const __nv_bfloat16*)y, ldy, (const __nv_bfloat16*)dy, lddy,
+                                 (__nv_bfloat16*)dx, lddx, N, D, s);
+    }
+}
+
+}  // namespace wsf

@@ -554,7 +554,7 @@ static inline int next_pow2(int64_t v) {
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 static cudaError_t allow_smem(const void* kernel, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes < 32 * 1024) return cudaSuccess;  // static shared memory counts against 48 KB too
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

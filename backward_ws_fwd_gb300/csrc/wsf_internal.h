@@ -36,6 +36,11 @@ cudaError_t launch_ws_bwd_atomic(const void* x, int64_t ldx, const float* w, con
 cudaError_t launch_silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx,
                                    float* dw, int accumulate, int64_t n, int dtype, cudaStream_t s);
 
+cudaError_t launch_softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t N,
+                               int64_t D, int dtype, cudaStream_t s);
+cudaError_t launch_softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* dx,
+                               int64_t lddx, int64_t N, int64_t D, int dtype, cudaStream_t s);
+
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);
 

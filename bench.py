@@ -39,7 +39,9 @@ if ROOT not in sys.path:
 METRIC = "fwd+bwd effective HBM GB/s and % of GB300 peak; elements/s per op"
 ORDER_FWD = ["c2", "c3", "c4", "c5"]
 ORDER_BWD = ["c5", "c4", "c3", "c2"]
-KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2}
+KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2, "softmax_fwd": 1,
+                  "softmax_bwd": 1}
+EXTRA = ["s1"]  # measured only when named with --workload
 
 
 # ------------------------------------------------------------------ byte model
@@ -57,6 +59,8 @@ def op_bytes(wl, op: str, rows: int | None = None) -> int:
             return N * D * es + D * 4 + N * es
         return 2 * N * D * es + N * es + 2 * D * 4
     n = N * wl.D
+    if wl.op == "softmax":
+        return 2 * n * es if op == "fwd" else 3 * n * es
     return 2 * n * es + 4 if op == "fwd" else 3 * n * es + 8
 
 
@@ -65,8 +69,8 @@ def op_elems(wl, rows: int | None = None) -> int:
 
 
 def steps_ops(names):
-    fwd = [(n, "fwd") for n in ORDER_FWD if n in names]
-    bwd = [(n, "bwd") for n in ORDER_BWD if n in names]
+    fwd = [(n, "fwd") for n in ORDER_FWD + EXTRA if n in names]
+    bwd = [(n, "bwd") for n in ORDER_BWD + EXTRA if n in names]
     return fwd + bwd
 
 
@@ -158,6 +162,9 @@ def oracle_sample(names, frac: float):
         if wl.op == "ws":
             w = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1)
             dy = inputgen.make((rows,), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
+        elif wl.op == "softmax":
+            w = None
+            dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
         else:
             w = torch.tensor([wl.w_scalar], dtype=torch.float32)
             dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
@@ -172,6 +179,9 @@ def oracle_step(samples):
         if wl.op == "ws":
             oracle.ws_fwd(x, w)
             oracle.ws_bwd(x, w, dy)
+        elif wl.op == "softmax":
+            _, y = oracle.softmax_fwd(x)
+            oracle.softmax_bwd(y, dy)
         else:
             oracle.silu_fwd(x.reshape(-1), wl.w_scalar)
             oracle.silu_bwd(dy.reshape(-1), x.reshape(-1), wl.w_scalar)
@@ -238,6 +248,8 @@ def run_reference(args, names):
 
 
 def workload_label(names):
+    if names == ["s1"]:
+        return "row softmax s1 (bf16 x[65536,4096]), fwd+bwd"
     return ("weighted sum " + "+".join(n for n in ["c3", "c4", "c5"] if n in names) +
             (" and " if "c2" in names and len(names) > 1 else "") +
             ("scaled-SiLU c2" if "c2" in names else "") + ", fwd+bwd")
@@ -259,6 +271,10 @@ class Buffers:
             self.hw = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1, pin=host_io)
             self.hdy = inputgen.make((wl.N,), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
                                      pin=host_io)
+        elif wl.op == "softmax":
+            self.hw = torch.zeros(1, dtype=torch.float32)
+            self.hdy = inputgen.make(shape, wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
+                                     pin=host_io)
         else:
             self.hw = torch.tensor([wl.w_scalar], dtype=torch.float32)
             if host_io:
@@ -272,6 +288,10 @@ class Buffers:
             self.y = torch.empty(wl.N, dtype=tdt, device=dev)
             self.gw = torch.empty(wl.D, dtype=torch.float32, device=dev)
             nbytes = wsf.ws_bwd_workspace_bytes(wl.N, wl.D, tdt, 0)
+        elif wl.op == "softmax":
+            self.y = torch.empty(shape, dtype=tdt, device=dev)
+            self.gw = torch.zeros(1, dtype=torch.float32, device=dev)
+            nbytes = 0
         else:
             self.y = torch.empty(shape, dtype=tdt, device=dev)
             self.gw = torch.empty(1, dtype=torch.float32, device=dev)
@@ -293,7 +313,10 @@ class Buffers:
         """Forward and backward of rows [r0, r1) (for the scaled SiLU, rows of
         the [N, D] view), the parameter gradient accumulated when asked."""
         x, dy, y, dx = self.x[r0:r1], self.dy[r0:r1], self.y[r0:r1], self.dx[r0:r1]
-        if self.wl.op == "ws":
+        if self.wl.op == "softmax":
+            wsf.softmax_fwd(x, y=y, stream=stream)
+            wsf.softmax_bwd(y, dy, dx=dx, stream=stream)
+        elif self.wl.op == "ws":
             wsf.ws_fwd(x, self.w, y=y, stream=stream)
             wsf.ws_bwd(x, self.w, dy, dx=dx, grad_w=self.gw, accumulate=accumulate,
                        workspace=self.ws, stream=stream)
@@ -303,7 +326,12 @@ class Buffers:
                          workspace=self.ws, stream=stream)
 
     def run(self, wsf, op):
-        if self.wl.op == "ws":
+        if self.wl.op == "softmax":
+            if op == "fwd":
+                wsf.softmax_fwd(self.x, y=self.y)
+            else:
+                wsf.softmax_bwd(self.y, self.dy, dx=self.dx)
+        elif self.wl.op == "ws":
             if op == "fwd":
                 wsf.ws_fwd(self.x, self.w, y=self.y)
             else:
@@ -613,7 +641,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     names = ORDER_FWD if args.workload == "all" else [s.strip() for s in args.workload.split(",")]
-    assert all(n in ORDER_FWD for n in names), names
+    assert all(n in ORDER_FWD + EXTRA for n in names), names
     if args.warmup < 3 and args.impl == "cuda":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

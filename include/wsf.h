@@ -177,6 +177,25 @@ int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,
              void* workspace, size_t workspace_bytes, int64_t n, int dtype, wsf_stream_t stream);
 
 /*
+ * softmax_fwd / softmax_bwd — row softmax and its vector-Jacobian product
+ * ["Backprop for kernel writers", §04 The duality: the backward collapses the
+ * dense Jacobian diag(y) − y·yᵀ to one row scalar and needs the output y, not
+ * x; the forward's max shift contributes nothing to it]:
+ *   y[i,j]  = exp(x[i,j] − m_i) / Σ_k exp(x[i,k] − m_i),  m_i = max_k x[i,k]
+ *   dx[i,j] = y[i,j] · (dy[i,j] − s_i),   s_i = Σ_k dy[i,k]·y[i,k]
+ * x, y, dy, dx: [N, D] in dtype, row strides ldx, ldy, lddy, lddx (>= D).
+ * fp32 arithmetic (for binary32 storage the row sums are compensated and
+ * x − max is split exactly before the exponential), each output rounded once.
+ * Rows of up to 32 KB are read once and written once; wider or unaligned rows
+ * read their inputs two or three times.  N == 0 or D == 0 does nothing.
+ * Errors as for ws_fwd.
+ */
+int softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t N, int64_t D, int dtype,
+                wsf_stream_t stream);
+int softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* dx, int64_t lddx,
+                int64_t N, int64_t D, int dtype, wsf_stream_t stream);
+
+/*
  * Atomic comparison variants  [SILU, backward kernel: per-block sums added
  * into one fp32 cell with an atomic add; § The backward grid is not the
  * forward grid: "atomics (small, non-critical)" versus the two-pass partials

@@ -24,7 +24,7 @@ class Dist:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                  # "ws" (weighted sum) or "silu" (scaled SiLU)
+    op: str                  # "ws" (weighted sum), "silu" (scaled SiLU) or "softmax"
     dtype: str               # storage type of x, dy, y, dx: "f32" | "f16" | "bf16"
     N: int                   # rows (ws) or leading extent (silu)
     D: int                   # features (ws) or trailing extent (silu)
@@ -57,4 +57,9 @@ WORKLOADS = {
     "c5": Workload("c5", "ws", "f32", 4096, 65536, x=Dist(NORMAL, 0.0, 1.0),
                    w=Dist(NORMAL, 0.0, 1.0 / 256.0), dy=Dist(NORMAL, 0.0, 1.0),
                    note="wide weighted sum, fp32 x[4096,65536], w ~N(0,1/256)"),
+    # measurement case of the softmax backward (rows of 4096, as in the
+    # softmax example of the VJP essay); not part of the default benchmark step
+    "s1": Workload("s1", "softmax", "bf16", 65536, 4096, x=Dist(NORMAL, 0.0, 2.0),
+                   dy=Dist(NORMAL, 0.0, 1.0),
+                   note="row softmax, bf16 x[65536,4096] ~N(0,2), dy ~N(0,1)"),
 }

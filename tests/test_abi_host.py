@@ -184,3 +184,20 @@ def test_atomic_variants_reject(wsf):
     assert sa(acc=2) == wsf.ERR_BAD_ARG
     assert sa(dw=0) == wsf.ERR_NULL_PTR
     assert sa(dx=2 * F + 50) == wsf.ERR_OVERLAP
+
+
+def test_softmax_rejects(wsf):
+    L = wsf.lib
+    s = None
+    assert L.softmax_fwd(_p(F), 64, _p(2 * F), 64, 10, 64, 7, s) == wsf.ERR_BAD_DTYPE
+    assert L.softmax_fwd(_p(F), 64, _p(2 * F), 64, -1, 64, 1, s) == wsf.ERR_BAD_SHAPE
+    assert L.softmax_fwd(_p(F), 63, _p(2 * F), 64, 10, 64, 1, s) == wsf.ERR_BAD_STRIDE
+    assert L.softmax_fwd(None, 64, _p(2 * F), 64, 10, 64, 1, s) == wsf.ERR_NULL_PTR
+    assert L.softmax_fwd(_p(F), 64, _p(F + 64), 64, 10, 64, 1, s) == wsf.ERR_OVERLAP
+    assert L.softmax_fwd(_p(F + 1), 64, _p(2 * F), 64, 10, 64, 1, s) == wsf.ERR_MISALIGNED
+    assert L.softmax_fwd(None, 0, None, 0, 0, 64, 1, s) == wsf.OK
+    assert L.softmax_bwd(_p(F), 64, _p(2 * F), 64, _p(3 * F), 64, 10, 64, 9, s) == wsf.ERR_BAD_DTYPE
+    assert L.softmax_bwd(_p(F), 64, _p(2 * F), 64, _p(3 * F), 8, 10, 64, 1, s) == wsf.ERR_BAD_STRIDE
+    assert L.softmax_bwd(_p(F), 64, None, 64, _p(3 * F), 64, 10, 64, 1, s) == wsf.ERR_NULL_PTR
+    assert L.softmax_bwd(_p(F), 64, _p(2 * F), 64, _p(2 * F + 2), 64, 10, 64, 1, s) == \
+        wsf.ERR_OVERLAP

@@ -1,0 +1,117 @@
+"""GPU parity of the softmax forward and backward against the fp64 oracle:
+register rows of every width class, the two-pass wide/unaligned path, row
+strides, guard bands, bit reproducibility, and sampled rows at the
+measurement size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from inputgen import NORMAL
+from tolerance import check_elementwise
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DTS = ["f32", "f16", "bf16"]
+
+
+@pytest.fixture(scope="module")
+def wsf():
+    import __graft_entry__
+    __graft_entry__.build()
+    import backward_ws_fwd_gb300 as m
+    return m
+
+
+def _inputs(N, D, dt, seed=0):
+    import inputgen
+    x = inputgen.make((N, D), dt, NORMAL, 0.0, 2.0, seed, 0)
+    dy = inputgen.make((N, D), dt, NORMAL, 0.0, 1.0, seed, 2)
+    return x, dy
+
+
+def _run(wsf, x, dy_host, y_in, pad=0, mis=0):
+    """Run forward on x and backward on (y_in, dy) with row stride D + pad and
+    pointers shifted by `mis` elements; outputs surrounded by guard bytes."""
+    N, D = x.shape
+    ld = D + pad
+
+    def place(t):
+        b = torch.zeros(N * ld + mis + 16, dtype=t.dtype, device=DEV)
+        v = b[mis:mis + N * ld].view(N, ld)[:, :D]
+        v.copy_(t.to(DEV))
+        return v
+
+    def out():
+        b = torch.full((N * ld + mis + 64,), 7.0, dtype=x.dtype, device=DEV)
+        return b, b[mis:mis + N * ld].view(N, ld)[:, :D]
+
+    xd, yd, gd = place(x), place(y_in), place(dy_host)
+    yb, y = out()
+    dxb, dx = out()
+    wsf.softmax_fwd(xd, y=y)
+    wsf.softmax_bwd(yd, gd, dx=dx)
+    torch.cuda.synchronize()
+    for b in (yb, dxb):  # the guard bands and row padding keep their fill
+        mask = torch.ones_like(b, dtype=torch.bool)
+        mask[mis:mis + N * ld].view(N, ld)[:, :D] = False
+        assert bool((b[mask] == 7.0).all())
+    return y.cpu(), dx.cpu()
+
+
+def _check(x, dy, y, dx, yin):
+    ye, yo = oracle.softmax_fwd(x)
+    res = check_elementwise(y, yo, ye)
+    assert res and res.clause2 == 0, ("y", res)
+    r = oracle.softmax_bwd(yin, dy)
+    res = check_elementwise(dx, r["dx"], r["dx_exact"], scale=r["dx_scale"])
+    assert res, ("dx", res)
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D", [(1, 1), (7, 5), (33, 64), (100, 1000), (9, 2048), (5, 4096),
+                                 (3, 8192), (2, 16400), (4, 40000), (1000, 16)])
+def test_softmax_parity(wsf, dt, N, D):
+    x, dy = _inputs(N, D, dt)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("pad,mis", [(8, 0), (3, 0), (0, 1)])
+def test_softmax_strides_alignment(wsf, dt, pad, mis):
+    x, dy = _inputs(37, 1024, dt)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin, pad=pad, mis=mis)
+    _check(x, dy, y, dx, yin)
+
+
+def test_softmax_large_logits_and_reproducible(wsf):
+    x = torch.tensor([[80.0, 0.0, -80.0, 3.0] * 16], dtype=torch.float32).repeat(5, 1)
+    dy = torch.randn(5, 64)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+    xd, yd, gd = x.to(DEV), yin.to(DEV), dy.to(DEV)
+    outs = [(wsf.softmax_fwd(xd), wsf.softmax_bwd(yd, gd)) for _ in range(3)]
+    for a, b in outs[1:]:
+        assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1])
+
+
+@pytest.mark.slow
+def test_softmax_measurement_size_sampled(wsf):
+    import inputgen
+    from inputgen.workloads import WORKLOADS
+    wl = WORKLOADS["s1"]
+    x = inputgen.make((wl.N, wl.D), wl.dtype, wl.x.kind, wl.x.a, wl.x.b, 0, 0, pin=True)
+    dy = inputgen.make((wl.N, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2, pin=True)
+    xd, gd = x.to(DEV), dy.to(DEV)
+    y = wsf.softmax_fwd(xd)
+    dx = wsf.softmax_bwd(y, gd)
+    torch.cuda.synchronize()
+    rows = torch.from_numpy(np.unique(np.concatenate([[0, wl.N - 1],
+                                                      np.random.default_rng(0).choice(wl.N, 254)])))
+    xs, gs = x[rows].contiguous(), dy[rows].contiguous()
+    ys = y[rows.to(DEV)].cpu()
+    _check(xs, gs, ys, dx[rows.to(DEV)].cpu(), ys)
