@@ -65,6 +65,12 @@ def lib():
         L.orc_softmax_fwd.restype = _int
         L.orc_softmax_bwd.argtypes = [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _vp]
         L.orc_softmax_bwd.restype = _int
+        L.orc_norm_fwd.argtypes = [_vp, _i64, _vp, _vp, _dbl, _int, _i64, _i64, _int, _vp, _vp, _vp,
+                                   _vp, _vp]
+        L.orc_norm_fwd.restype = _int
+        L.orc_norm_bwd.argtypes = [_vp, _i64, _vp, _vp, _dbl, _int, _i64, _i64, _int, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp]
+        L.orc_norm_bwd.restype = _int
         _lib = L
     return _lib
 
@@ -207,3 +213,39 @@ def softmax_bwd(y, dy):
     _check(lib().orc_softmax_bwd(_ptr(y), _ptr(dy), N, D, DTYPE_CODE[_dt_of(y)], _ptr(dxe),
                                  _ptr(dxs), _ptr(dx), _ptr(s)), "softmax_bwd")
     return {"dx_exact": dxe, "dx_scale": dxs, "dx": dx, "s": s}
+
+
+# ---------------------------------------------------------------- RMSNorm / LayerNorm
+def norm_fwd(x, w, b=None, eps=1e-5, layer=False):
+    """RMSNorm (layer=False) or LayerNorm (layer=True) of the rows of x [N, D].
+    Returns dict y_exact, y_scale (fp64 [N, D]), y (tensor, x's dtype), r, mu (fp64 [N])."""
+    import torch
+    assert x.dim() == 2 and x.stride(1) == 1 and w.dtype == torch.float32 and w.is_contiguous()
+    N, D = x.shape
+    ye = np.empty((N, D), np.float64)
+    ys = np.empty((N, D), np.float64)
+    yo = torch.empty((N, D), dtype=x.dtype)
+    r = np.empty(N, np.float64)
+    mu = np.empty(N, np.float64)
+    _check(lib().orc_norm_fwd(_ptr(x), x.stride(0) if N > 0 else D, _ptr(w),
+                              _ptr(b) if b is not None else None, float(eps), int(layer), N, D,
+                              DTYPE_CODE[_dt_of(x)], _ptr(ye), _ptr(ys), _ptr(yo), _ptr(r),
+                              _ptr(mu)), "norm_fwd")
+    return {"y_exact": ye, "y_scale": ys, "y": yo, "r": r, "mu": mu}
+
+
+def norm_bwd(x, w, dy, eps=1e-5, layer=False, *, want_dx=True):
+    """Returns dict dx_exact, dx_scale (fp64 [N, D]), dx (tensor), grad_w,
+    grad_w_abs, grad_b, grad_b_abs (fp64 [D]; the b ones for LayerNorm)."""
+    import torch
+    assert x.dim() == 2 and x.stride(1) == 1 and dy.is_contiguous() and dy.dtype == x.dtype
+    N, D = x.shape
+    dxe = np.empty((N, D), np.float64) if want_dx else None
+    dxs = np.empty((N, D), np.float64) if want_dx else None
+    dx = torch.empty((N, D), dtype=x.dtype) if want_dx else None
+    gw, gwa, gb, gba = (np.zeros(D, np.float64) for _ in range(4))
+    _check(lib().orc_norm_bwd(_ptr(x), x.stride(0) if N > 0 else D, _ptr(w), _ptr(dy), float(eps),
+                              int(layer), N, D, DTYPE_CODE[_dt_of(x)], _ptr(dxe), _ptr(dxs),
+                              _ptr(dx), _ptr(gw), _ptr(gwa), _ptr(gb), _ptr(gba)), "norm_bwd")
+    return {"dx_exact": dxe, "dx_scale": dxs, "dx": dx, "grad_w": gw, "grad_w_abs": gwa,
+            "grad_b": gb, "grad_b_abs": gba}

@@ -387,3 +387,160 @@ int orc_softmax_bwd(const void* y, const void* dy, int64_t N, int64_t D, int dt,
     free(ta);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* RMSNorm and LayerNorm over rows, with their backward.  The pages     */
+/* name both ("Backward in Triton", § Save vs recompute: the RMSNorm    */
+/* rstd recompute; § The backward grid ...: RMSNorm's dw sums a length-d */
+/* partial from every row; "Backprop for kernel writers", §04: LayerNorm */
+/* collapses to two row scalars plus batch-axis parameter gradients)    */
+/* but print no formulas; these are the textbook definitions.          */
+/*   RMSNorm:   r = 1/sqrt(mean_j x_j^2 + eps),  y = x·r·w              */
+/*              xh = x·r, g = dy·w,                                      */
+/*              dx = r·(g − xh·mean_j(g·xh)),  dw = Σ_i dy·xh            */
+/*   LayerNorm: mu = mean x, r = 1/sqrt(mean (x−mu)^2 + eps),            */
+/*              xh = (x−mu)·r, y = xh·w + b,                             */
+/*              dx = r·(g − mean g − xh·mean(g·xh)),                     */
+/*              dw = Σ_i dy·xh,  db = Σ_i dy                             */
+/* ------------------------------------------------------------------ */
+
+/* Row statistics: mean (LayerNorm only) and r, both from pairwise sums. */
+static void norm_stats(const void* x, int64_t off, int64_t D, int dt, int ln, double eps,
+                       double* t, double* mu_out, double* r_out) {
+    double mu = 0.0;
+    if (ln) {
+        for (int64_t j = 0; j < D; j++) t[j] = decode(x, off + j, dt);
+        mu = orc_pairwise_sum(t, D) / (double)D;
+    }
+    for (int64_t j = 0; j < D; j++) {
+        const double c = decode(x, off + j, dt) - mu;
+        t[j] = c * c;
+    }
+    *mu_out = mu;
+    *r_out = 1.0 / sqrt(orc_pairwise_sum(t, D) / (double)D + eps);
+}
+
+/* x [N, D] (row stride ldx), w, b [D] binary32 (b unused unless ln).
+ * Outputs (any may be NULL): y_exact [N*D], y_scale [N*D] (magnitude of the
+ * terms: (|x| + |mu|)·r·|w| + |b|), y_out (dt, contiguous), r_out [N], mu_out [N]. */
+int orc_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, double eps, int ln,
+                 int64_t N, int64_t D, int dt, double* y_exact, double* y_scale, void* y_out,
+                 double* r_out, double* mu_out) {
+    if (!x || !w || (ln && !b) || N < 0 || D <= 0 || ldx < D || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* t = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!t) return -2;
+    for (int64_t i = 0; i < N; i++) {
+        double mu, r;
+        norm_stats(x, i * ldx, D, dt, ln, eps, t, &mu, &r);
+        if (r_out) r_out[i] = r;
+        if (mu_out) mu_out[i] = mu;
+        for (int64_t j = 0; j < D; j++) {
+            const double xv = decode(x, i * ldx + j, dt);
+            const double y = (xv - mu) * r * (double)w[j] + (ln ? (double)b[j] : 0.0);
+            if (y_exact) y_exact[i * D + j] = y;
+            if (y_scale)
+                y_scale[i * D + j] = (fabs(xv) + fabs(mu)) * r * fabs((double)w[j]) +
+                                     (ln ? fabs((double)b[j]) : 0.0);
+            if (y_out) store(y_out, i * D + j, dt, y);
+        }
+    }
+    free(t);
+    return 0;
+}
+
+/* Column-wise pairwise sums over rows [a, b) of dy[i,j]·xh[i,j] (into
+ * gw/gwa, signed and absolute) and dy[i,j] (into gb/gba), xh = (x − mu_i)·r_i,
+ * with the split points of orc_pairwise_sum; rows walked in storage order.
+ * scratch: 4·D doubles per recursion level. */
+static void normcol(const void* x, int64_t ldx, const void* dy, int dt, const double* mu,
+                    const double* r, int64_t a, int64_t b, int64_t D, double* gw, double* gwa,
+                    double* gb, double* gba, double* scratch) {
+    const int64_t n = b - a;
+    if (n <= 8) {
+        for (int64_t j = 0; j < D; j++) gw[j] = gwa[j] = gb[j] = gba[j] = 0.0;
+        for (int64_t i = a; i < b; i++)
+            for (int64_t j = 0; j < D; j++) {
+                const double g = decode(dy, i * D + j, dt);
+                const double t = g * ((decode(x, i * ldx + j, dt) - mu[i]) * r[i]);
+                gw[j] += t;
+                gwa[j] += fabs(t);
+                gb[j] += g;
+                gba[j] += fabs(g);
+            }
+        return;
+    }
+    const int64_t h = n / 2;
+    double* rw = scratch;
+    double* rwa = scratch + D;
+    double* rb = scratch + 2 * D;
+    double* rba = scratch + 3 * D;
+    normcol(x, ldx, dy, dt, mu, r, a, a + h, D, gw, gwa, gb, gba, scratch + 4 * D);
+    normcol(x, ldx, dy, dt, mu, r, a + h, b, D, rw, rwa, rb, rba, scratch + 4 * D);
+    for (int64_t j = 0; j < D; j++) {
+        gw[j] += rw[j];
+        gwa[j] += rwa[j];
+        gb[j] += rb[j];
+        gba[j] += rba[j];
+    }
+}
+
+/* x [N, D] (row stride ldx), w [D], dy [N, D] contiguous, storage dt.
+ * Outputs (any may be NULL): dx_exact, dx_scale (|r|·(|g| + mean|g| + |xh|·mean|g·xh|)),
+ * dx_out (dt, contiguous), grad_w / grad_w_abs [D], grad_b / grad_b_abs [D] (ln only). */
+int orc_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, double eps, int ln,
+                 int64_t N, int64_t D, int dt, double* dx_exact, double* dx_scale, void* dx_out,
+                 double* grad_w, double* grad_w_abs, double* grad_b, double* grad_b_abs) {
+    if (!x || !w || !dy || N < 0 || D <= 0 || ldx < D || dt < 0 || dt > 2) return -1;
+    make_tables();
+    double* t = (double*)malloc(sizeof(double) * (size_t)D);
+    double* t2 = (double*)malloc(sizeof(double) * (size_t)D);
+    double* mus = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double* rs = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double* cols = (double*)malloc(sizeof(double) * (size_t)D * 4 * 68);
+    if (!t || !t2 || !mus || !rs || !cols) {
+        free(t); free(t2); free(mus); free(rs); free(cols);
+        return -2;
+    }
+    for (int64_t i = 0; i < N; i++) {
+        double mu, r;
+        norm_stats(x, i * ldx, D, dt, ln, eps, t, &mu, &r);
+        mus[i] = mu;
+        rs[i] = r;
+        if (!dx_exact && !dx_scale && !dx_out) continue;
+        /* mean g, mean g·xh (and their magnitudes for the tolerance scale) */
+        for (int64_t j = 0; j < D; j++) t[j] = decode(dy, i * D + j, dt) * (double)w[j];
+        const double mg = ln ? orc_pairwise_sum(t, D) / (double)D : 0.0;
+        for (int64_t j = 0; j < D; j++) t2[j] = fabs(t[j]);
+        const double mga = ln ? orc_pairwise_sum(t2, D) / (double)D : 0.0;
+        for (int64_t j = 0; j < D; j++) t2[j] = t[j] * ((decode(x, i * ldx + j, dt) - mu) * r);
+        const double mgx = orc_pairwise_sum(t2, D) / (double)D;
+        for (int64_t j = 0; j < D; j++) t2[j] = fabs(t2[j]);
+        const double mgxa = orc_pairwise_sum(t2, D) / (double)D;
+        for (int64_t j = 0; j < D; j++) {
+            const double xh = (decode(x, i * ldx + j, dt) - mu) * r;
+            const double g = t[j];
+            const double dx = r * (g - mg - xh * mgx);
+            if (dx_exact) dx_exact[i * D + j] = dx;
+            if (dx_scale) dx_scale[i * D + j] = fabs(r) * (fabs(g) + mga + fabs(xh) * mgxa);
+            if (dx_out) store(dx_out, i * D + j, dt, dx);
+        }
+    }
+    if (grad_w || grad_w_abs || grad_b || grad_b_abs) {
+        double* gw = (double*)malloc(sizeof(double) * (size_t)D * 4);
+        if (!gw) {
+            free(t); free(t2); free(mus); free(rs); free(cols);
+            return -2;
+        }
+        normcol(x, ldx, dy, dt, mus, rs, 0, N, D, gw, gw + D, gw + 2 * D, gw + 3 * D, cols);
+        for (int64_t j = 0; j < D; j++) {
+            if (grad_w) grad_w[j] = gw[j];
+            if (grad_w_abs) grad_w_abs[j] = gw[D + j];
+            if (ln && grad_b) grad_b[j] = gw[2 * D + j];
+            if (ln && grad_b_abs) grad_b_abs[j] = gw[3 * D + j];
+        }
+        free(gw);
+    }
+    free(t); free(t2); free(mus); free(rs); free(cols);
+    return 0;
+}
