@@ -50,6 +50,21 @@ lib.softmax_fwd.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]
 lib.softmax_fwd.restype = _int
 lib.softmax_bwd.argtypes = [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]
 lib.softmax_bwd.restype = _int
+_f = ctypes.c_float
+lib.rmsnorm_fwd.argtypes = [_vp, _i64, _vp, _f, _vp, _i64, _i64, _i64, _int, _vp]
+lib.rmsnorm_fwd.restype = _int
+lib.layernorm_fwd.argtypes = [_vp, _i64, _vp, _vp, _f, _vp, _i64, _i64, _i64, _int, _vp]
+lib.layernorm_fwd.restype = _int
+lib.rmsnorm_bwd_workspace_bytes.argtypes = [_i64, _i64, _int]
+lib.rmsnorm_bwd_workspace_bytes.restype = _sz
+lib.layernorm_bwd_workspace_bytes.argtypes = [_i64, _i64, _int]
+lib.layernorm_bwd_workspace_bytes.restype = _sz
+lib.rmsnorm_bwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _f, _vp, _i64, _vp, _int, _vp, _sz, _i64,
+                            _i64, _int, _vp]
+lib.rmsnorm_bwd.restype = _int
+lib.layernorm_bwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _f, _vp, _i64, _vp, _vp, _int, _vp, _sz,
+                              _i64, _i64, _int, _vp]
+lib.layernorm_bwd.restype = _int
 lib.silu_fwd.argtypes = [_vp, _vp, _vp, _i64, _int, _vp]
 lib.silu_fwd.restype = _int
 lib.silu_bwd_workspace_bytes.argtypes = [_i64, _int]
@@ -245,6 +260,85 @@ def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, strea
     return dx, dw
 
 
+def norm_bwd_workspace_bytes(N: int, D: int, dtype, layer: bool = False) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code_of_dtype(dtype)
+    fn = lib.layernorm_bwd_workspace_bytes if layer else lib.rmsnorm_bwd_workspace_bytes
+    return fn(N, D, code)
+
+
+def rmsnorm_fwd(x, w, eps=1e-5, y=None, stream=None):
+    """y = x·r·w per row, r = 1/sqrt(mean x² + eps).  x: [N, D] (unit inner
+    stride); w: [D] float32; y has x's type."""
+    import torch
+    N, D = x.shape
+    if y is None:
+        y = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    _check(lib.rmsnorm_fwd(_ptr(x), x.stride(0), _ptr(w), float(eps), _ptr(y), y.stride(0), N, D,
+                           _dtype_code(x), _stream(stream)), "rmsnorm_fwd")
+    return y
+
+
+def layernorm_fwd(x, w, b, eps=1e-5, y=None, stream=None):
+    """y = (x − μ)·r·w + b per row.  w, b: [D] float32."""
+    import torch
+    N, D = x.shape
+    if y is None:
+        y = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    _check(lib.layernorm_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(b), float(eps), _ptr(y),
+                             y.stride(0), N, D, _dtype_code(x), _stream(stream)), "layernorm_fwd")
+    return y
+
+
+def _norm_ws(N, D, code, layer, workspace, device):
+    import torch
+    fn = lib.layernorm_bwd_workspace_bytes if layer else lib.rmsnorm_bwd_workspace_bytes
+    need = fn(N, D, code)
+    if workspace is None and need not in (0, SIZE_MAX):
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return workspace, wbytes
+
+
+def rmsnorm_bwd(x, w, dy, eps=1e-5, dx=None, grad_w=None, accumulate=False, workspace=None,
+                stream=None):
+    """dx = r·(g − x̂·mean(g·x̂)), g = dy·w; grad_w (+)= Σ_rows dy·x̂.  Returns (dx, grad_w)."""
+    import torch
+    N, D = x.shape
+    code = _dtype_code(x)
+    if dx is None:
+        dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    if grad_w is None:
+        grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
+    workspace, wbytes = _norm_ws(N, D, code, False, workspace, x.device)
+    _check(lib.rmsnorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0), float(eps),
+                           _ptr(dx), dx.stride(0), _ptr(grad_w), int(bool(accumulate)),
+                           _ptr(workspace), wbytes, N, D, code, _stream(stream)), "rmsnorm_bwd")
+    return dx, grad_w
+
+
+def layernorm_bwd(x, w, dy, eps=1e-5, dx=None, grad_w=None, grad_b=None, accumulate=False,
+                  workspace=None, stream=None):
+    """dx = r·(g − mean g − x̂·mean(g·x̂)); grad_w (+)= Σ dy·x̂; grad_b (+)= Σ dy.
+    Returns (dx, grad_w, grad_b)."""
+    import torch
+    N, D = x.shape
+    code = _dtype_code(x)
+    if dx is None:
+        dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
+    if grad_w is None:
+        grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
+    if grad_b is None:
+        grad_b = torch.empty(D, dtype=torch.float32, device=x.device)
+    workspace, wbytes = _norm_ws(N, D, code, True, workspace, x.device)
+    _check(lib.layernorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0), float(eps),
+                             _ptr(dx), dx.stride(0), _ptr(grad_w), _ptr(grad_b),
+                             int(bool(accumulate)), _ptr(workspace), wbytes, N, D, code,
+                             _stream(stream)), "layernorm_bwd")
+    return dx, grad_w, grad_b
+
+
 __all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
            "ws_bwd_atomic", "silu_bwd_atomic", "softmax_fwd", "softmax_bwd", "silu_fwd",
-           "silu_bwd", "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "F32", "F16", "BF16"]
+           "silu_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "layernorm_fwd", "layernorm_bwd",
+           "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "norm_bwd_workspace_bytes", "F32",
+           "F16", "BF16"]

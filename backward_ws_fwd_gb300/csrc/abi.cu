@@ -1,7 +1,8 @@
 // abi.cu — the extern "C" entry points declared in include/wsf.h.
 //
 // Every entry point validates its arguments on the host, before anything is
-// enqueued, and maps them to a launcher in ws.cu / silu.cu.  Host-only work
+// enqueued, and maps them to a launcher in ws.cu, silu.cu, softmax.cu or
+// norm.cu.  Host-only work
 // here never touches the device, so argument errors can be checked without
 // a GPU.
 #include <limits.h>
@@ -263,6 +264,122 @@ int softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* 
     if (overlap(sdx, span(y, yb)) || overlap(sdx, span(dy, gb))) return WSF_ERR_OVERLAP;
     return cuda_status(wsf::launch_softmax_bwd(y, ldy, dy, lddy, dx, lddx, N, D, dtype,
                                                (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// RMSNorm / LayerNorm
+namespace {
+
+bool valid_eps(float eps) { return eps >= 0.0f && eps <= 3.0e38f; }  // finite, not negative
+
+size_t norm_ws_bytes(int64_t N, int64_t D, int dtype, int nout) {
+    if (!valid_dtype(dtype) || N < 0 || D < 0) return SIZE_MAX;
+    const int64_t P = wsf::norm_tiles(N, D);
+    int64_t b;
+    if (!mul_ok(P, D, &b) || !mul_ok(b, 4 * nout, &b) || b > INT64_MAX - 255) return SIZE_MAX;
+    return (size_t)((b + 255) / 256 * 256);
+}
+
+int norm_fwd_entry(const void* x, int64_t ldx, const float* w, const float* b, float eps, void* y,
+                   int64_t ldy, int64_t N, int64_t D, int dtype, int layer, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    if (!valid_eps(eps)) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldx < D || ldy < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = mat ? extent_bytes(N, D, ldx, es) : 0;
+    const int64_t yb = mat ? extent_bytes(N, D, ldy, es) : 0;
+    int64_t wb;
+    if (xb < 0 || yb < 0 || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
+    if (mat && (!x || !y || !w || (layer && !b))) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(y, es) || !aligned_to(w, 4) || !aligned_to(b, 4))
+        return WSF_ERR_MISALIGNED;
+    if (!mat) return WSF_OK;
+    const Span sy = span(y, yb);
+    if (overlap(sy, span(x, xb)) || overlap(sy, span(w, wb)) ||
+        (layer && overlap(sy, span(b, wb))))
+        return WSF_ERR_OVERLAP;
+    return cuda_status(wsf::launch_norm_fwd(x, ldx, w, layer ? b : nullptr, eps, y, ldy, N, D,
+                                            dtype, layer, (cudaStream_t)stream));
+}
+
+int norm_bwd_entry(const void* x, int64_t ldx, const float* w, const void* dy, int64_t lddy,
+                   float eps, void* dx, int64_t lddx, float* grad_w, float* grad_b, int accumulate,
+                   void* workspace, size_t workspace_bytes, int64_t N, int64_t D, int dtype,
+                   int layer, wsf_stream_t stream) {
+    if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
+    if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
+    if (!valid_eps(eps) || (accumulate != 0 && accumulate != 1)) return WSF_ERR_BAD_ARG;
+    const int es = elt_bytes(dtype);
+    const bool mat = N > 0 && D > 0;
+    if (mat && (ldx < D || lddy < D || lddx < D)) return WSF_ERR_BAD_STRIDE;
+    const int64_t xb = mat ? extent_bytes(N, D, ldx, es) : 0;
+    const int64_t gb = mat ? extent_bytes(N, D, lddy, es) : 0;
+    const int64_t dxb = mat ? extent_bytes(N, D, lddx, es) : 0;
+    int64_t wb;
+    if (xb < 0 || gb < 0 || dxb < 0 || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
+    if ((mat && (!x || !dy || !dx || !w)) || (D > 0 && (!grad_w || (layer && !grad_b))))
+        return WSF_ERR_NULL_PTR;
+    if (!aligned_to(x, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(w, 4) ||
+        !aligned_to(grad_w, 4) || !aligned_to(grad_b, 4) || !aligned_to(workspace, 4))
+        return WSF_ERR_MISALIGNED;
+    const size_t need = norm_ws_bytes(N, D, dtype, layer ? 2 : 1);
+    if (need == SIZE_MAX) return WSF_ERR_BAD_SHAPE;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return WSF_ERR_WORKSPACE;
+    if (D == 0) return WSF_OK;
+    const Span ins[3] = {span(x, xb), span(dy, gb), span(w, mat ? wb : 0)};
+    const Span outs[4] = {span(dx, dxb), span(grad_w, wb), span(grad_b, layer ? wb : 0),
+                          span(workspace, (int64_t)need)};
+    for (int i = 0; i < 4; i++) {
+        for (int j = 0; j < 3; j++)
+            if (overlap(outs[i], ins[j])) return WSF_ERR_OVERLAP;
+        for (int j = i + 1; j < 4; j++)
+            if (overlap(outs[i], outs[j])) return WSF_ERR_OVERLAP;
+    }
+    return cuda_status(wsf::launch_norm_bwd(x, ldx, w, dy, lddy, eps, dx, lddx, grad_w,
+                                            layer ? grad_b : nullptr, accumulate,
+                                            (float*)workspace, N, D, dtype, layer,
+                                            (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int rmsnorm_fwd(const void* x, int64_t ldx, const float* w, float eps, void* y, int64_t ldy,
+                int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    return norm_fwd_entry(x, ldx, w, nullptr, eps, y, ldy, N, D, dtype, 0, stream);
+}
+
+size_t rmsnorm_bwd_workspace_bytes(int64_t N, int64_t D, int dtype) {
+    return norm_ws_bytes(N, D, dtype, 1);
+}
+
+int rmsnorm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64_t lddy,
+                float eps, void* dx, int64_t lddx, float* grad_w, int accumulate, void* workspace,
+                size_t workspace_bytes, int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    return norm_bwd_entry(x, ldx, w, dy, lddy, eps, dx, lddx, grad_w, nullptr, accumulate,
+                          workspace, workspace_bytes, N, D, dtype, 0, stream);
+}
+
+int layernorm_fwd(const void* x, int64_t ldx, const float* w, const float* b, float eps, void* y,
+                  int64_t ldy, int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    return norm_fwd_entry(x, ldx, w, b, eps, y, ldy, N, D, dtype, 1, stream);
+}
+
+size_t layernorm_bwd_workspace_bytes(int64_t N, int64_t D, int dtype) {
+    return norm_ws_bytes(N, D, dtype, 2);
+}
+
+int layernorm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64_t lddy,
+                  float eps, void* dx, int64_t lddx, float* grad_w, float* grad_b, int accumulate,
+                  void* workspace, size_t workspace_bytes, int64_t N, int64_t D, int dtype,
+                  wsf_stream_t stream) {
+    return norm_bwd_entry(x, ldx, w, dy, lddy, eps, dx, lddx, grad_w, grad_b, accumulate,
+                          workspace, workspace_bytes, N, D, dtype, 1, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,700 @@
+// norm.cu — RMSNorm and LayerNorm forward and backward for sm_103a.
+//
+// "Backward in Triton — autograd.Function and the backward grid", § Save vs
+// recompute (the row statistic rstd is recomputed in the backward from x,
+// not stored) and § The backward grid is not the forward grid (RMSNorm's dw:
+// every row contributes a length-D partial that is summed across the batch,
+// by a separate reduce over a partials buffer); "Backprop for kernel
+// writers", §04 (LayerNorm collapses to two row scalars plus batch-axis
+// parameter gradients).  The pages print no formulas; these are the
+// textbook ones:
+//   RMSNorm:   r = 1/sqrt(mean x² + eps), y = x·r·w;
+//              g = dy·w, dx = r·(g − x̂·mean(g·x̂)) with x̂ = x·r,
+//              dw = Σ_rows dy·x̂
+//   LayerNorm: μ = mean x, r = 1/sqrt(mean (x−μ)² + eps), x̂ = (x−μ)·r,
+//              y = x̂·w + b; dx = r·(g − mean g − x̂·mean(g·x̂)),
+//              dw = Σ_rows dy·x̂, db = Σ_rows dy
+//
+// Row path (16-byte aligned rows of up to 8192 elements).  A row is held by a
+// group of TPR threads, each owning CPT 16-byte chunks (at most 16 elements,
+// so the backward's per-column accumulators stay in registers); the chunks
+// are staged S rows ahead with cp.async into per-thread shared slots.
+// RMSNorm needs one fused group reduction per row; LayerNorm two: Σx, then
+// the sums over d = x − μ.  The mean is carried as μ₀ + c: μ₀ = fl(Σx/D) and
+// c = (Σx − D·μ₀)/D from the remainder of the compensated Σx (hi + lo:
+// fma(−D, μ₀, hi) is exact), and d = (x − μ₀) − c.  With μ₀ alone, its own
+// rounding (up to ulp(μ)/2) would shift every x̂ of a row with a large common
+// offset by the same amount, an error that does not cancel in Σ dy·x̂; and c
+// cannot be taken from Σ(x − μ₀) either, since the rounding of x − μ₀ has
+// one sign across a binade.  Σx is therefore compensated (TwoSum) for every
+// storage type; for binary32 the other row sums are compensated too (Dot2),
+// so that y and dx stay within 1e-6.  In the
+// backward each thread sums dy·x̂ (and dy) for its own columns over the rows
+// of its CTA's row tile; the CTA's row groups are combined in index order into
+// one partial row per tile, and norm_bwd_reduce sums the tiles in a fixed
+// order — the deterministic two-pass form, no atomics.  Other layouts take a
+// multi-pass element-wise path with the same arithmetic.
+#include <algorithm>
+#include <type_traits>
+
+#include "wsf_device.cuh"
+#include "wsf_internal.h"
+
+namespace wsf {
+
+constexpr int64_t kNormTilesMax = 6 * kDesignSMs;  // 912 partial rows at most
+constexpr int64_t kNormRowsPerTileMin = 64;
+constexpr int64_t kNormRowMax = 8192;  // widest row (elements) of the row path
+
+int64_t norm_tiles(int64_t N, int64_t D) {
+    if (N <= 0 || D <= 0) return 0;
+    const int64_t p = (N + kNormRowsPerTileMin - 1) / kNormRowsPerTileMin;
+    return p < kNormTilesMax ? p : kNormTilesMax;
+}
+
+__device__ __forceinline__ void norm_tile_rows(int64_t p, int64_t P, int64_t N, int64_t& a,
+                                               int64_t& b) {
+    a = (p * N) / P;
+    b = ((p + 1) * N) / P;
+}
+
+// ---------------------------------------------------------------------------
+// Row sums: plain fp32 (C = false) or compensated (C = true, value hi + lo).
+template <bool C>
+__device__ __forceinline__ void s_add(Acc2& a, float v) {
+    if constexpr (C) {
+        float s, e;
+        two_sum(a.hi, v, s, e);
+        a.hi = s;
+        a.lo += e;
+    } else {
+        a.hi += v;
+    }
+}
+
+template <bool C>
+__device__ __forceinline__ void s_fma(Acc2& a, float x, float y) {
+    if constexpr (C)
+        acc2_fma(a, x, y);
+    else
+        a.hi = fmaf(x, y, a.hi);
+}
+
+template <bool C>
+__device__ __forceinline__ Acc2 s_comb(Acc2 a, Acc2 b) {
+    if constexpr (C)
+        return acc2_add(a, b);
+    else
+        return Acc2{a.hi + b.hi, 0.f};
+}
+
+__device__ __forceinline__ float s_val(const Acc2& a) { return a.hi + a.lo; }
+
+// Reduce K sums over each aligned group of TPR threads: xor butterfly inside
+// a warp, then (groups wider than a warp) the warps' sums in index order
+// through `red` (K·NT/32 float2).  Every thread of the CTA calls it together;
+// every lane of a group ends with the same bits, on every run.
+template <int TPR, int NT, int K, bool C>
+__device__ __forceinline__ void group_reduce(Acc2 (&v)[K], float2* red) {
+    constexpr int W = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int q = 0; q < K; q++) {
+        if constexpr (C)
+            v[q] = group_sum2<W>(v[q]);
+        else
+            v[q].hi = group_sum<W>(v[q].hi);
+    }
+    if constexpr (TPR > 32) {
+        constexpr int NW = NT / 32, NWG = TPR / 32;
+        const int wid = threadIdx.x >> 5, first = (threadIdx.x / TPR) * NWG;
+        if ((threadIdx.x & 31) == 0)
+#pragma unroll
+            for (int q = 0; q < K; q++) red[q * NW + wid] = make_float2(v[q].hi, v[q].lo);
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < K; q++) {
+            float2 t = red[q * NW + first];
+            Acc2 s{t.x, t.y};
+#pragma unroll
+            for (int i = 1; i < NWG; i++) {
+                t = red[q * NW + first + i];
+                s = s_comb<C>(s, Acc2{t.x, t.y});
+            }
+            v[q] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// 1/sqrt(ms + eps) with ms = Σ/D; each step is correctly rounded (IEEE
+// division and square root: this library is built without fast-math).
+__device__ __forceinline__ float rstd_of(float sum_sq, float d, float eps) {
+    return 1.0f / sqrtf(sum_sq / d + eps);
+}
+
+// The row mean as μ₀ + c from the compensated sum s = Σx (hi + lo): μ₀ is
+// the rounded quotient and c = (Σx − D·μ₀)/D.  hi − D·μ₀ is exact in one fma
+// (a few bits wide, the remainder of a correctly rounded division plus the
+// rounding of hi + lo); adding lo and dividing each round once, relative to c.
+struct Mean {
+    float mu0, c;
+};
+
+__device__ __forceinline__ Mean mean_of(const Acc2& s, float d) {
+    Mean m;
+    m.mu0 = s_val(s) / d;
+    m.c = (fmaf(-d, m.mu0, s.hi) + s.lo) / d;
+    return m;
+}
+
+// Backward row scalars from sums = {Σ d², Σ g·d[, Σ g]}: r, mean(g) (zero for
+// RMSNorm) and mean(g·x̂) = r·Σ g·d / D.
+struct BwdStats {
+    float r, mg, mgx;
+};
+
+template <bool LN, int K>
+__device__ __forceinline__ BwdStats bwd_stats(const Acc2 (&sums)[K], float d, float eps) {
+    BwdStats st;
+    st.r = rstd_of(s_val(sums[0]), d, eps);
+    st.mgx = st.r * (s_val(sums[1]) / d);
+    st.mg = LN ? s_val(sums[K - 1]) / d : 0.f;
+    return st;
+}
+
+template <int TPR, int CPT, int NT>
+__device__ __forceinline__ void stage_chunks(Raw16* slots, const void* base, int64_t ld_bytes,
+                                             int64_t row, int64_t row_end, int Dv, int l) {
+#pragma unroll
+    for (int k = 0; k < CPT; k++) {
+        const int c = l + k * TPR;
+        const bool ok = row < row_end && c < Dv;
+        const char* src =
+            static_cast<const char*>(base) + (ok ? row * ld_bytes + (int64_t)c * 16 : 0);
+        cp_async16(&slots[k * NT + threadIdx.x], src, ok ? 16 : 0);
+    }
+}
+
+template <int TPR, int CPT, int V>
+__device__ __forceinline__ void load_params(const float* __restrict__ p, int Dv, int l,
+                                            float (&out)[CPT][V]) {
+#pragma unroll
+    for (int k = 0; k < CPT; k++) {
+        const int c = l + k * TPR;
+#pragma unroll
+        for (int q = 0; q < V / 4; q++) {
+            const Raw16 r = (c < Dv) ? ld_keep(p + (int64_t)c * V + 4 * q) : raw_zero();
+#pragma unroll
+            for (int i = 0; i < 4; i++) out[k][4 * q + i] = __uint_as_float(r.u[i]);
+        }
+    }
+}
+
+// ===========================================================================
+// Forward, row path: R = NT/TPR rows per CTA iteration, grid-stride.
+// ===========================================================================
+template <typename T, bool LN, int TPR, int CPT, int NT, int S, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+    norm_fwd_rows(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                  const float* __restrict__ b, float eps, T* __restrict__ y, int64_t ldy,
+                  int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    constexpr int R = NT / TPR;
+    constexpr bool C = std::is_same<T, float>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    __shared__ float2 red[NT / 32];
+    const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
+    const float fd = (float)(Dv * V);
+    pdl_wait();
+    float wv[CPT][V], bv[CPT][V];
+    load_params<TPR, CPT, V>(w, Dv, l, wv);
+    if constexpr (LN) load_params<TPR, CPT, V>(b, Dv, l, bv);
+    const int64_t base = (int64_t)blockIdx.x * R, stride = (int64_t)gridDim.x * R;
+    const int64_t iters = base < N ? (N - base + stride - 1) / stride : 0;
+    const int64_t ldb = ldx * (int64_t)sizeof(T);
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters)
+            stage_chunks<TPR, CPT, NT>(xs + k * CPT * NT, x, ldb, base + k * stride + g, N, Dv, l);
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters)
+            stage_chunks<TPR, CPT, NT>(xs + (nk % S) * CPT * NT, x, ldb, base + nk * stride + g, N,
+                                       Dv, l);
+        cp_async_commit();
+        const int64_t row = base + k * stride + g;
+        const Raw16* cur = xs + (k % S) * CPT * NT + threadIdx.x;
+        Mean m{0.f, 0.f};
+        if constexpr (LN) {
+            Acc2 s[1] = {acc2_zero()};
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                float f[V];
+                E::widen(cur[c * NT], f);  // masked chunks are zero-filled
+#pragma unroll
+                for (int v = 0; v < V; v++) s_add<true>(s[0], f[v]);
+            }
+            group_reduce<TPR, NT, 1, true>(s, red);
+            m = mean_of(s[0], fd);
+        }
+        Acc2 ss[1] = {acc2_zero()};  // Σ d², d = (x − μ₀) − c
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * TPR < Dv) {
+                float f[V];
+                E::widen(cur[c * NT], f);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float d = (f[v] - m.mu0) - m.c;
+                    s_fma<C>(ss[0], d, d);
+                }
+            }
+        }
+        group_reduce<TPR, NT, 1, C>(ss, red);
+        const float r = rstd_of(s_val(ss[0]), fd, eps);
+        if (row < N) {
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                if (l + c * TPR < Dv) {
+                    float f[V], o[V];
+                    E::widen(cur[c * NT], f);
+#pragma unroll
+                    for (int v = 0; v < V; v++) {
+                        const float xh = ((f[v] - m.mu0) - m.c) * r;
+                        o[v] = LN ? fmaf(xh, wv[c][v], bv[c][v]) : xh * wv[c][v];
+                    }
+                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    pdl_trigger();
+}
+
+// ===========================================================================
+// Backward stage 1, row path: blockIdx.x = row tile p, rows [ra, rb).
+// ===========================================================================
+template <typename T, bool LN, int TPR, int CPT, int NT, int S, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+    norm_bwd_rows(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                  const T* __restrict__ dy, int64_t lddy, float eps, T* __restrict__ dx,
+                  int64_t lddx, float* __restrict__ part, int64_t N, int Dv, int64_t P) {
+    using E = Elt<T>;
+    constexpr int V = E::V;
+    constexpr int R = NT / TPR;
+    constexpr bool C = std::is_same<T, float>::value;
+    constexpr int K = LN ? 3 : 2;
+    const int64_t D = (int64_t)Dv * V;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
+    __shared__ float2 red[K * (NT / 32)];
+    const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
+    const float fd = (float)D;
+    int64_t ra, rb;
+    norm_tile_rows(blockIdx.x, P, N, ra, rb);
+    pdl_wait();
+    float wv[CPT][V];
+    load_params<TPR, CPT, V>(w, Dv, l, wv);
+    float aw[CPT][V], ab[CPT][V];
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+#pragma unroll
+        for (int v = 0; v < V; v++) aw[c][v] = ab[c][v] = 0.f;
+
+    const int64_t iters = (rb - ra + R - 1) / R;
+    const int64_t ldxb = ldx * (int64_t)sizeof(T), ldgb = lddy * (int64_t)sizeof(T);
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) {
+            stage_chunks<TPR, CPT, NT>(xs + k * CPT * NT, x, ldxb, ra + k * R + g, rb, Dv, l);
+            stage_chunks<TPR, CPT, NT>(gs + k * CPT * NT, dy, ldgb, ra + k * R + g, rb, Dv, l);
+        }
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters) {
+            stage_chunks<TPR, CPT, NT>(xs + (nk % S) * CPT * NT, x, ldxb, ra + nk * R + g, rb, Dv,
+                                       l);
+            stage_chunks<TPR, CPT, NT>(gs + (nk % S) * CPT * NT, dy, ldgb, ra + nk * R + g, rb,
+                                       Dv, l);
+        }
+        cp_async_commit();
+        const int64_t row = ra + k * R + g;
+        const Raw16* cx = xs + (k % S) * CPT * NT + threadIdx.x;
+        const Raw16* cg = gs + (k % S) * CPT * NT + threadIdx.x;
+        Mean m{0.f, 0.f};
+        if constexpr (LN) {
+            Acc2 s[1] = {acc2_zero()};
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                float f[V];
+                E::widen(cx[c * NT], f);  // masked chunks and rows are zero-filled
+#pragma unroll
+                for (int v = 0; v < V; v++) s_add<true>(s[0], f[v]);
+            }
+            group_reduce<TPR, NT, 1, true>(s, red);
+            m = mean_of(s[0], fd);
+        }
+        // sums[0] = Σ d², sums[1] = Σ g·d, and for LayerNorm sums[2] = Σ g;
+        // d = (x − μ₀) − c, g = dy·w
+        Acc2 sums[K];
+#pragma unroll
+        for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * TPR < Dv) {
+                float f[V], gd[V];
+                E::widen(cx[c * NT], f);
+                E::widen(cg[c * NT], gd);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float d = (f[v] - m.mu0) - m.c;
+                    const float gg = gd[v] * wv[c][v];
+                    s_fma<C>(sums[0], d, d);
+                    s_fma<C>(sums[1], gg, d);
+                    if constexpr (LN) s_add<C>(sums[2], gg);
+                }
+            }
+        }
+        group_reduce<TPR, NT, K, C>(sums, red);
+        const BwdStats st = bwd_stats<LN>(sums, fd, eps);
+        if (row < rb) {
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                if (l + c * TPR < Dv) {
+                    float f[V], gd[V], o[V];
+                    E::widen(cx[c * NT], f);
+                    E::widen(cg[c * NT], gd);
+                    const float r = st.r, mg = st.mg, mgx = st.mgx;
+#pragma unroll
+                    for (int v = 0; v < V; v++) {
+                        const float xh = ((f[v] - m.mu0) - m.c) * r;
+                        const float gg = gd[v] * wv[c][v];
+                        o[v] = r * ((gg - mg) - xh * mgx);
+                        aw[c][v] = fmaf(gd[v], xh, aw[c][v]);
+                        if constexpr (LN) ab[c][v] += gd[v];
+                    }
+                    st_stream(dx + row * lddx + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    pdl_trigger();
+    // Combine the R row groups, in index order, into the tile's partial row(s).
+    __syncthreads();
+    float* sm = reinterpret_cast<float*>(smem_raw);  // [R][CPT][TPR][V]
+    constexpr int NOUT = LN ? 2 : 1;
+#pragma unroll
+    for (int o = 0; o < NOUT; o++) {
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            float4* dst = reinterpret_cast<float4*>(sm + ((g * CPT + c) * TPR + l) * V);
+#pragma unroll
+            for (int q = 0; q < V / 4; q++) {
+                const float(&a)[CPT][V] = (o == 0) ? aw : ab;
+                dst[q] = make_float4(a[c][4 * q], a[c][4 * q + 1], a[c][4 * q + 2],
+                                     a[c][4 * q + 3]);
+            }
+        }
+        __syncthreads();
+        float* out = part + ((int64_t)o * P + blockIdx.x) * D;
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const int cid = (int)(j / V), v = (int)(j % V);
+            const int c = cid / TPR, ll = cid % TPR;
+            float s = sm[(c * TPR + ll) * V + v];
+#pragma unroll
+            for (int q = 1; q < R; q++) s += sm[((q * CPT + c) * TPR + ll) * V + v];
+            out[j] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// ===========================================================================
+// Element-wise paths (any alignment, any D): one CTA per row (forward) or per
+// row tile (backward), several passes over each row.
+// ===========================================================================
+template <typename T, bool LN, int NT>
+__global__ void __launch_bounds__(NT)
+    norm_fwd_scalar(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                    const float* __restrict__ b, float eps, T* __restrict__ y, int64_t ldy,
+                    int64_t N, int64_t D) {
+    using E = Elt<T>;
+    constexpr bool C = std::is_same<T, float>::value;
+    __shared__ float2 red[NT / 32];
+    const float fd = (float)D;
+    pdl_wait();
+    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+        const T* xr = x + row * ldx;
+        Mean m{0.f, 0.f};
+        if constexpr (LN) {
+            Acc2 s[1] = {acc2_zero()};
+            for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
+            group_reduce<NT, NT, 1, true>(s, red);
+            m = mean_of(s[0], fd);
+        }
+        Acc2 ss[1] = {acc2_zero()};
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float d = (E::load1(xr + j) - m.mu0) - m.c;
+            s_fma<C>(ss[0], d, d);
+        }
+        group_reduce<NT, NT, 1, C>(ss, red);
+        const float r = rstd_of(s_val(ss[0]), fd, eps);
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float xh = ((E::load1(xr + j) - m.mu0) - m.c) * r;
+            E::store1(y + row * ldy + j,
+                      LN ? fmaf(xh, __ldg(w + j), __ldg(b + j)) : xh * __ldg(w + j));
+        }
+    }
+    pdl_trigger();
+}
+
+template <typename T, bool LN, int NT>
+__global__ void __launch_bounds__(NT)
+    norm_bwd_scalar(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                    const T* __restrict__ dy, int64_t lddy, float eps, T* __restrict__ dx,
+                    int64_t lddx, float* __restrict__ part, int64_t N, int64_t D, int64_t P) {
+    using E = Elt<T>;
+    constexpr bool C = std::is_same<T, float>::value;
+    constexpr int K = LN ? 3 : 2;
+    __shared__ float2 red[K * (NT / 32)];
+    const float fd = (float)D;
+    int64_t ra, rb;
+    norm_tile_rows(blockIdx.x, P, N, ra, rb);
+    pdl_wait();
+    // thread t owns the columns j ≡ t (mod NT) of the tile's partial row(s)
+    float* pw = part + (int64_t)blockIdx.x * D;
+    float* pb = part + ((int64_t)P + blockIdx.x) * D;
+    for (int64_t j = threadIdx.x; j < D; j += NT) {
+        pw[j] = 0.f;
+        if constexpr (LN) pb[j] = 0.f;
+    }
+    for (int64_t row = ra; row < rb; row++) {
+        const T* xr = x + row * ldx;
+        const T* gr = dy + row * lddy;
+        Mean m{0.f, 0.f};
+        if constexpr (LN) {
+            Acc2 s[1] = {acc2_zero()};
+            for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
+            group_reduce<NT, NT, 1, true>(s, red);
+            m = mean_of(s[0], fd);
+        }
+        Acc2 sums[K];
+#pragma unroll
+        for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float d = (E::load1(xr + j) - m.mu0) - m.c;
+            const float gg = E::load1(gr + j) * __ldg(w + j);
+            s_fma<C>(sums[0], d, d);
+            s_fma<C>(sums[1], gg, d);
+            if constexpr (LN) s_add<C>(sums[2], gg);
+        }
+        group_reduce<NT, NT, K, C>(sums, red);
+        const BwdStats st = bwd_stats<LN>(sums, fd, eps);
+        for (int64_t j = threadIdx.x; j < D; j += NT) {
+            const float g0 = E::load1(gr + j);
+            const float xh = ((E::load1(xr + j) - m.mu0) - m.c) * st.r;
+            E::store1(dx + row * lddx + j,
+                      st.r * ((g0 * __ldg(w + j) - st.mg) - xh * st.mgx));
+            pw[j] = fmaf(g0, xh, pw[j]);
+            if constexpr (LN) pb[j] += g0;
+        }
+    }
+    pdl_trigger();
+}
+
+// Stage 2: out[d] (+)= Σ_p part[o][p][d] for o = 0 (dw) and, for LayerNorm,
+// o = 1 (db); blockIdx.y picks o.  Stripes of p are summed in order, then a
+// fixed halving tree runs over the RY stripes.
+template <int RY>
+__global__ void __launch_bounds__(32 * RY)
+    norm_bwd_reduce(const float* __restrict__ part, int64_t P, int64_t D, float* __restrict__ gw,
+                    float* __restrict__ gb, int accumulate) {
+    __shared__ float sm[RY][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int64_t col = (int64_t)blockIdx.x * 32 + tx;
+    float* out = blockIdx.y == 0 ? gw : gb;
+    const float* pp = part + (int64_t)blockIdx.y * P * D;
+    pdl_wait();
+    float s = 0.f;
+    if (col < D) {
+#pragma unroll 8
+        for (int64_t p = ty; p < P; p += RY) s += pp[p * D + col];
+    }
+    sm[ty][tx] = s;
+    __syncthreads();
+#pragma unroll
+    for (int h = RY / 2; h > 0; h >>= 1) {
+        if (ty < h) sm[ty][tx] += sm[ty + h][tx];
+        __syncthreads();
+    }
+    if (ty == 0 && col < D) {
+        const float v = sm[0][tx];
+        out[col] = accumulate ? out[col] + v : v;
+    }
+    pdl_trigger();
+}
+
+// ===========================================================================
+// Host launchers
+// ===========================================================================
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+static cudaError_t allow_smem_norm(const void* kernel, size_t bytes) {
+    if (bytes < 32 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Row shape for Dv 16-byte chunks per row: each thread owns CPT chunks (16
+// elements); TPR = the power of two >= ceil(Dv / CPT) threads per row; 256
+// threads per CTA (R = 256/TPR rows at a time), or 512 for one row of
+// 4097..8192 elements.
+template <int CPT, typename F>
+static cudaError_t norm_shape(int64_t Dv, F&& go) {
+    using std::integral_constant;
+    auto pick = [&](auto tpr) -> cudaError_t {
+        constexpr int TPR = decltype(tpr)::value;
+        constexpr int NT = TPR > 256 ? TPR : 256;
+        return go(integral_constant<int, TPR>{}, integral_constant<int, CPT>{},
+                  integral_constant<int, NT>{});
+    };
+    const int64_t t = cdiv(Dv, CPT);
+    if (t <= 1) return pick(integral_constant<int, 1>{});
+    if (t <= 2) return pick(integral_constant<int, 2>{});
+    if (t <= 4) return pick(integral_constant<int, 4>{});
+    if (t <= 8) return pick(integral_constant<int, 8>{});
+    if (t <= 16) return pick(integral_constant<int, 16>{});
+    if (t <= 32) return pick(integral_constant<int, 32>{});
+    if (t <= 64) return pick(integral_constant<int, 64>{});
+    if (t <= 128) return pick(integral_constant<int, 128>{});
+    if (t <= 256) return pick(integral_constant<int, 256>{});
+    return pick(integral_constant<int, 512>{});
+}
+
+template <typename T, bool LN>
+static cudaError_t norm_fwd_t(const T* x, int64_t ldx, const float* w, const float* b, float eps,
+                              T* y, int64_t ldy, int64_t N, int64_t D, cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    const int64_t Dv = D / V;
+    if (D % V == 0 && D <= kNormRowMax && ldx % V == 0 && ldy % V == 0 && aligned16(x) &&
+        aligned16(y) && aligned16(w) && (!LN || aligned16(b))) {
+        return norm_shape<16 / V>(Dv, [&](auto tpr, auto cpt, auto nt) {
+            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+            constexpr int NT = decltype(nt)::value;
+            constexpr int S = 3;
+            auto k = norm_fwd_rows<T, LN, TPR, CPT, NT, S, NT == 256 ? 3 : 1>;
+            const size_t smem = (size_t)S * CPT * NT * 16;
+            cudaError_t e = allow_smem_norm((const void*)k, smem);
+            if (e != cudaSuccess) return e;
+            const int64_t grid = std::min<int64_t>(cdiv(N, NT / TPR), 8 * kDesignSMs);
+            return launch(k, dim3((unsigned)grid), dim3(NT), smem, s, true, x, ldx, w, b, eps, y,
+                          ldy, N, (int)Dv);
+        });
+    }
+    return launch(norm_fwd_scalar<T, LN, 256>,
+                  dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)), dim3(256), 0, s, true, x,
+                  ldx, w, b, eps, y, ldy, N, D);
+}
+
+template <typename T, bool LN>
+static cudaError_t norm_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy, int64_t lddy,
+                              float eps, T* dx, int64_t lddx, float* gw, float* gb, int accumulate,
+                              float* part, int64_t N, int64_t D, cudaStream_t s) {
+    constexpr int V = Elt<T>::V;
+    const int64_t P = norm_tiles(N, D);
+    const int64_t Dv = D / V;
+    cudaError_t e = cudaSuccess;
+    if (P > 0) {
+        if (D % V == 0 && D <= kNormRowMax && ldx % V == 0 && lddy % V == 0 && lddx % V == 0 &&
+            aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(w)) {
+            e = norm_shape<16 / V>(Dv, [&](auto tpr, auto cpt, auto nt) {
+                constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+                constexpr int NT = decltype(nt)::value;
+                constexpr int S = (NT > 256 && V == 4) ? 2 : 3;
+                auto k = norm_bwd_rows<T, LN, TPR, CPT, NT, S, NT == 256 ? 2 : 1>;
+                const size_t smem = std::max<size_t>((size_t)2 * S * CPT * NT * 16,
+                                                     (size_t)NT * CPT * V * sizeof(float));
+                cudaError_t e2 = allow_smem_norm((const void*)k, smem);
+                if (e2 != cudaSuccess) return e2;
+                return launch(k, dim3((unsigned)P), dim3(NT), smem, s, true, x, ldx, w, dy, lddy,
+                              eps, dx, lddx, part, N, (int)Dv, P);
+            });
+        } else {
+            e = launch(norm_bwd_scalar<T, LN, 256>, dim3((unsigned)P), dim3(256), 0, s, true, x,
+                       ldx, w, dy, lddy, eps, dx, lddx, part, N, D, P);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned nout = LN ? 2 : 1;
+    if (D <= 4096)
+        return launch(norm_bwd_reduce<32>, dim3((unsigned)cdiv(D, 32), nout), dim3(32, 32), 0, s,
+                      true, (const float*)part, P, D, gw, gb, accumulate);
+    return launch(norm_bwd_reduce<8>, dim3((unsigned)cdiv(D, 32), nout), dim3(32, 8), 0, s, true,
+                  (const float*)part, P, D, gw, gb, accumulate);
+}
+
+template <bool LN>
+static cudaError_t norm_fwd_any(const void* x, int64_t ldx, const float* w, const float* b,
+                                float eps, void* y, int64_t ldy, int64_t N, int64_t D, int dtype,
+                                cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return norm_fwd_t<float, LN>((const float*)x, ldx, w, b, eps, (float*)y, ldy, N, D, s);
+        case 1:
+            return norm_fwd_t<__half, LN>((const __half*)x, ldx, w, b, eps, (__half*)y, ldy, N, D,
+                                          s);
+        default:
+            return norm_fwd_t<__nv_bfloat16, LN>((const __nv_bfloat16*)x, ldx, w, b, eps,
+                                                 (__nv_bfloat16*)y, ldy, N, D, s);
+    }
+}
+
+template <bool LN>
+static cudaError_t norm_bwd_any(const void* x, int64_t ldx, const float* w, const void* dy,
+                                int64_t lddy, float eps, void* dx, int64_t lddx, float* gw,
+                                float* gb, int accumulate, float* part, int64_t N, int64_t D,
+                                int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case 0:
+            return norm_bwd_t<float, LN>((const float*)x, ldx, w, (const float*)dy, lddy, eps,
+                                         (float*)dx, lddx, gw, gb, accumulate, part, N, D, s);
+        case 1:
+            return norm_bwd_t<__half, LN>((const __half*)x, ldx, w, (const __half*)dy, lddy, eps,
+                                          (__half*)dx, lddx, gw, gb, accumulate, part, N, D, s);
+        default:
+            return norm_bwd_t<__nv_bfloat16, LN>((const __nv_bfloat16*)x, ldx, w,
+                                                 (const __nv_bfloat16*)dy, lddy, eps,
+                                                 (__nv_bfloat16*)dx, lddx, gw, gb, accumulate,
+                                                 part, N, D, s);
+    }
+}
+
+cudaError_t launch_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, float eps,
+                            void* y, int64_t ldy, int64_t N, int64_t D, int dtype, int layer,
+                            cudaStream_t s) {
+    return layer ? norm_fwd_any<true>(x, ldx, w, b, eps, y, ldy, N, D, dtype, s)
+                 : norm_fwd_any<false>(x, ldx, w, b, eps, y, ldy, N, D, dtype, s);
+}
+
+cudaError_t launch_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy,
+                            int64_t lddy, float eps, void* dx, int64_t lddx, float* gw, float* gb,
+                            int accumulate, float* part, int64_t N, int64_t D, int dtype,
+                            int layer, cudaStream_t s) {
+    return layer ? norm_bwd_any<true>(x, ldx, w, dy, lddy, eps, dx, lddx, gw, gb, accumulate, part,
+                                      N, D, dtype, s)
+                 : norm_bwd_any<false>(x, ldx, w, dy, lddy, eps, dx, lddx, gw, gb, accumulate,
+                                       part, N, D, dtype, s);
+}
+
+}  // namespace wsf

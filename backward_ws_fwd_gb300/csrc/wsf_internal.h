@@ -1,5 +1,5 @@
 // wsf_internal.h — host-side interface between the C ABI (abi.cu) and the
-// kernel launchers (ws.cu, silu.cu).  Not installed; not part of the ABI.
+// kernel launchers (ws.cu, silu.cu, softmax.cu, norm.cu).  Not installed; not part of the ABI.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -40,6 +40,18 @@ cudaError_t launch_softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy,
                                int64_t D, int dtype, cudaStream_t s);
 cudaError_t launch_softmax_bwd(const void* y, int64_t ldy, const void* dy, int64_t lddy, void* dx,
                                int64_t lddx, int64_t N, int64_t D, int dtype, cudaStream_t s);
+
+// RMSNorm (layer == 0) / LayerNorm (layer == 1) rows; norm_tiles is the
+// number of row tiles P of the backward's partial buffer ([P, D] per
+// parameter gradient).
+int64_t norm_tiles(int64_t N, int64_t D);
+cudaError_t launch_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, float eps,
+                            void* y, int64_t ldy, int64_t N, int64_t D, int dtype, int layer,
+                            cudaStream_t s);
+cudaError_t launch_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy,
+                            int64_t lddy, float eps, void* dx, int64_t lddx, float* gw, float* gb,
+                            int accumulate, float* part, int64_t N, int64_t D, int dtype,
+                            int layer, cudaStream_t s);
 
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);

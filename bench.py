@@ -40,8 +40,10 @@ METRIC = "fwd+bwd effective HBM GB/s and % of GB300 peak; elements/s per op"
 ORDER_FWD = ["c2", "c3", "c4", "c5"]
 ORDER_BWD = ["c5", "c4", "c3", "c2"]
 KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2, "softmax_fwd": 1,
-                  "softmax_bwd": 1}
-EXTRA = ["s1"]  # measured only when named with --workload
+                  "softmax_bwd": 1, "rmsnorm_fwd": 1, "rmsnorm_bwd": 2, "layernorm_fwd": 1,
+                  "layernorm_bwd": 2}
+EXTRA = ["s1", "n1", "n2"]  # measured only when named with --workload
+NORMS = ("rmsnorm", "layernorm")
 
 
 # ------------------------------------------------------------------ byte model
@@ -61,6 +63,11 @@ def op_bytes(wl, op: str, rows: int | None = None) -> int:
     n = N * wl.D
     if wl.op == "softmax":
         return 2 * n * es if op == "fwd" else 3 * n * es
+    if wl.op in NORMS:
+        # x (and dy) read, y (dx) written; w (and b) read, grad_w (and grad_b)
+        # written once; the backward's per-tile partials are not counted
+        params = 4 * wl.D * (2 if wl.op == "layernorm" else 1)
+        return 2 * n * es + params if op == "fwd" else 3 * n * es + 4 * wl.D + params
     return 2 * n * es + 4 if op == "fwd" else 3 * n * es + 8
 
 
@@ -165,6 +172,11 @@ def oracle_sample(names, frac: float):
         elif wl.op == "softmax":
             w = None
             dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
+        elif wl.op in NORMS:
+            w = [inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1),
+                 inputgen.make((wl.D,), "f32", wl.b.kind, wl.b.a, wl.b.b, 0, 3)
+                 if wl.b is not None else None]
+            dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
         else:
             w = torch.tensor([wl.w_scalar], dtype=torch.float32)
             dy = inputgen.make((rows, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2)
@@ -182,6 +194,10 @@ def oracle_step(samples):
         elif wl.op == "softmax":
             _, y = oracle.softmax_fwd(x)
             oracle.softmax_bwd(y, dy)
+        elif wl.op in NORMS:
+            layer = wl.op == "layernorm"
+            oracle.norm_fwd(x, w[0], w[1], wl.eps, layer)
+            oracle.norm_bwd(x, w[0], dy, wl.eps, layer)
         else:
             oracle.silu_fwd(x.reshape(-1), wl.w_scalar)
             oracle.silu_bwd(dy.reshape(-1), x.reshape(-1), wl.w_scalar)
@@ -247,9 +263,14 @@ def run_reference(args, names):
     return 0
 
 
+EXTRA_LABELS = {"s1": "row softmax s1 (bf16 x[65536,4096])",
+                "n1": "RMSNorm n1 (bf16 x[65536,4096])",
+                "n2": "LayerNorm n2 (bf16 x[65536,4096])"}
+
+
 def workload_label(names):
-    if names == ["s1"]:
-        return "row softmax s1 (bf16 x[65536,4096]), fwd+bwd"
+    if all(n in EXTRA for n in names):
+        return " + ".join(EXTRA_LABELS[n] for n in names) + ", fwd+bwd"
     return ("weighted sum " + "+".join(n for n in ["c3", "c4", "c5"] if n in names) +
             (" and " if "c2" in names and len(names) > 1 else "") +
             ("scaled-SiLU c2" if "c2" in names else "") + ", fwd+bwd")
@@ -275,6 +296,13 @@ class Buffers:
             self.hw = torch.zeros(1, dtype=torch.float32)
             self.hdy = inputgen.make(shape, wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
                                      pin=host_io)
+        elif wl.op in NORMS:
+            self.hw = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1, pin=host_io)
+            if wl.b is not None:
+                self.hb = inputgen.make((wl.D,), "f32", wl.b.kind, wl.b.a, wl.b.b, 0, 3,
+                                        pin=host_io)
+            self.hdy = inputgen.make(shape, wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2,
+                                     pin=host_io)
         else:
             self.hw = torch.tensor([wl.w_scalar], dtype=torch.float32)
             if host_io:
@@ -284,6 +312,9 @@ class Buffers:
         self.x = self.hx.to(dev)
         self.w = self.hw.to(dev)
         self.dy = self.hdy.to(dev)
+        self.hb = getattr(self, "hb", None)
+        self.b = self.hb.to(dev) if self.hb is not None else None
+        self.gb = None
         if wl.op == "ws":
             self.y = torch.empty(wl.N, dtype=tdt, device=dev)
             self.gw = torch.empty(wl.D, dtype=torch.float32, device=dev)
@@ -292,6 +323,12 @@ class Buffers:
             self.y = torch.empty(shape, dtype=tdt, device=dev)
             self.gw = torch.zeros(1, dtype=torch.float32, device=dev)
             nbytes = 0
+        elif wl.op in NORMS:
+            layer = wl.op == "layernorm"
+            self.y = torch.empty(shape, dtype=tdt, device=dev)
+            self.gw = torch.empty(wl.D, dtype=torch.float32, device=dev)
+            self.gb = torch.empty(wl.D, dtype=torch.float32, device=dev) if layer else None
+            nbytes = wsf.norm_bwd_workspace_bytes(wl.N, wl.D, tdt, layer)
         else:
             self.y = torch.empty(shape, dtype=tdt, device=dev)
             self.gw = torch.empty(1, dtype=torch.float32, device=dev)
@@ -302,12 +339,30 @@ class Buffers:
             self.hy = torch.empty(self.y.shape, dtype=tdt, pin_memory=True)
             self.hdx = torch.empty(shape, dtype=tdt, pin_memory=True)
             self.hgw = torch.empty(self.gw.shape, dtype=torch.float32, pin_memory=True)
+            self.hgb = (torch.empty(self.gb.shape, dtype=torch.float32, pin_memory=True)
+                        if self.gb is not None else None)
 
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in (self.hx, self.hw, self.hdy))
+        return sum(t.numel() * t.element_size() for t in (self.hx, self.hw, self.hdy, self.hb)
+                   if t is not None)
 
     def d2h_bytes(self):
-        return sum(t.numel() * t.element_size() for t in (self.y, self.dx, self.gw))
+        return sum(t.numel() * t.element_size() for t in (self.y, self.dx, self.gw, self.gb)
+                   if t is not None)
+
+    def norm(self, wsf, op, x, y, dy, dx, accumulate=False, stream=None):
+        eps = self.wl.eps
+        if self.wl.op == "layernorm":
+            if op == "fwd":
+                wsf.layernorm_fwd(x, self.w, self.b, eps, y=y, stream=stream)
+            else:
+                wsf.layernorm_bwd(x, self.w, dy, eps, dx=dx, grad_w=self.gw, grad_b=self.gb,
+                                  accumulate=accumulate, workspace=self.ws, stream=stream)
+        elif op == "fwd":
+            wsf.rmsnorm_fwd(x, self.w, eps, y=y, stream=stream)
+        else:
+            wsf.rmsnorm_bwd(x, self.w, dy, eps, dx=dx, grad_w=self.gw, accumulate=accumulate,
+                            workspace=self.ws, stream=stream)
 
     def run_rows(self, wsf, r0, r1, accumulate, stream):
         """Forward and backward of rows [r0, r1) (for the scaled SiLU, rows of
@@ -316,6 +371,9 @@ class Buffers:
         if self.wl.op == "softmax":
             wsf.softmax_fwd(x, y=y, stream=stream)
             wsf.softmax_bwd(y, dy, dx=dx, stream=stream)
+        elif self.wl.op in NORMS:
+            self.norm(wsf, "fwd", x, y, dy, dx, stream=stream)
+            self.norm(wsf, "bwd", x, y, dy, dx, accumulate=accumulate, stream=stream)
         elif self.wl.op == "ws":
             wsf.ws_fwd(x, self.w, y=y, stream=stream)
             wsf.ws_bwd(x, self.w, dy, dx=dx, grad_w=self.gw, accumulate=accumulate,
@@ -326,7 +384,9 @@ class Buffers:
                          workspace=self.ws, stream=stream)
 
     def run(self, wsf, op):
-        if self.wl.op == "softmax":
+        if self.wl.op in NORMS:
+            self.norm(wsf, op, self.x, self.y, self.dy, self.dx)
+        elif self.wl.op == "softmax":
             if op == "fwd":
                 wsf.softmax_fwd(self.x, y=self.y)
             else:
@@ -438,6 +498,8 @@ def run_cuda(args, names):
                 bounds = [b.wl.N * j // nc for j in range(nc + 1)]
                 with torch.cuda.stream(h2d):
                     b.w.copy_(b.hw, non_blocking=True)
+                    if b.hb is not None:
+                        b.b.copy_(b.hb, non_blocking=True)
                 for j in range(nc):
                     r0, r1 = bounds[j], bounds[j + 1]
                     with torch.cuda.stream(h2d):
@@ -455,6 +517,8 @@ def run_cuda(args, names):
                         b.hdx[r0:r1].copy_(b.dx[r0:r1], non_blocking=True)
                 with torch.cuda.stream(d2h):
                     b.hgw.copy_(b.gw, non_blocking=True)
+                    if b.hgb is not None:
+                        b.hgb.copy_(b.gb, non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -632,7 +696,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workload", default="all", help="all or a comma list of c2,c3,c4,c5")
+    ap.add_argument("--workload", default="all",
+                    help="all (c2..c5) or a comma list of c2,c3,c4,c5,s1,n1,n2")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="multiply every workload's row count (profiling on small cases)")
     ap.add_argument("--compare-atomic", action="store_true",

@@ -1,9 +1,10 @@
 /*
  * wsf.h — C ABI of libwsfwd: forward and backward (vector-Jacobian product)
- * kernels of two memory-bound row operators on one GPU (sm_103a).
+ * kernels of memory-bound row operators on one GPU (sm_103a).
  *
  *   weighted sum   y[i] = Σ_d x[i,d]·w[d]           x [N,D], w [D], y [N]
  *   scaled SiLU    y    = w·x·sigmoid(x)            x [n], scalar w
+ *   row softmax, RMSNorm and LayerNorm over the rows of x [N,D]
  *
  * Sources (web pages, cited by title and section):
  *   [WS]   "Writing Triton Kernels with Autograd: A Minimal End-to-End
@@ -217,6 +218,52 @@ int ws_bwd_atomic(const void* x, int64_t ldx, const float* w, const void* dy, vo
                   wsf_stream_t stream);
 int silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx, float* dw,
                     int accumulate, int64_t n, int dtype, wsf_stream_t stream);
+
+/*
+ * RMSNorm and LayerNorm over the rows of x, forward and vector-Jacobian
+ * product  ["Backward in Triton — autograd.Function and the backward grid",
+ * § Save vs recompute (the row statistic rstd is recomputed from x in the
+ * backward rather than stored) and § The backward grid is not the forward
+ * grid (RMSNorm's dw sums a length-D partial from every row: a map for dx and
+ * a separate reduce, the two-pass partials buffer being the deterministic
+ * choice); "Backprop for kernel writers", §04 (LayerNorm's backward collapses
+ * to two row scalars plus the batch-axis reductions of its parameters)].
+ * The pages give no formulas; these are the standard definitions:
+ *   RMSNorm:   r_i = 1/sqrt(mean_j x[i,j]² + eps),  x̂ = x·r_i,
+ *              y = x̂·w,                dx = r_i·(g − x̂·mean_j(g·x̂))
+ *   LayerNorm: μ_i = mean_j x[i,j],  r_i = 1/sqrt(mean_j (x[i,j]−μ_i)² + eps),
+ *              x̂ = (x−μ_i)·r_i,  y = x̂·w + b,
+ *              dx = r_i·(g − mean_j g − x̂·mean_j(g·x̂))
+ *   with g = dy·w;  grad_w[j] = Σ_i dy[i,j]·x̂[i,j],  grad_b[j] = Σ_i dy[i,j].
+ * x, dy, y, dx: [N, D] in dtype with row strides ldx, lddy, ldy, lddx (>= D);
+ * w, b, grad_w, grad_b: [D] binary32.  eps: binary32, finite and >= 0
+ * (WSF_ERR_BAD_ARG otherwise).  Nothing from the forward is needed by the
+ * backward but x: the row statistics are recomputed.  All arithmetic is
+ * binary32 (for binary32 storage the row sums are compensated); each output
+ * is rounded once to dtype.  Rows of up to 8192 elements with 16-byte
+ * aligned pointers and strides are read once and written once; other layouts
+ * take a multi-pass element-wise path.
+ * The backward writes dx and, per row tile p, the partial sums of dy·x̂ (and,
+ * LayerNorm, dy) into `workspace` (binary32 [P, D], twice for LayerNorm);
+ * then sums the tiles in a fixed order into grad_w (and grad_b), added to the
+ * existing values when accumulate == 1.  N == 0 gives zero gradients (or
+ * leaves them when accumulating); D == 0 does nothing.  The workspace size
+ * comes from the *_workspace_bytes query (0 when none is needed, SIZE_MAX for
+ * invalid sizes; host-only).  Other errors as for ws_bwd.
+ */
+int rmsnorm_fwd(const void* x, int64_t ldx, const float* w, float eps, void* y, int64_t ldy,
+                int64_t N, int64_t D, int dtype, wsf_stream_t stream);
+size_t rmsnorm_bwd_workspace_bytes(int64_t N, int64_t D, int dtype);
+int rmsnorm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64_t lddy,
+                float eps, void* dx, int64_t lddx, float* grad_w, int accumulate, void* workspace,
+                size_t workspace_bytes, int64_t N, int64_t D, int dtype, wsf_stream_t stream);
+int layernorm_fwd(const void* x, int64_t ldx, const float* w, const float* b, float eps, void* y,
+                  int64_t ldy, int64_t N, int64_t D, int dtype, wsf_stream_t stream);
+size_t layernorm_bwd_workspace_bytes(int64_t N, int64_t D, int dtype);
+int layernorm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64_t lddy,
+                  float eps, void* dx, int64_t lddx, float* grad_w, float* grad_b, int accumulate,
+                  void* workspace, size_t workspace_bytes, int64_t N, int64_t D, int dtype,
+                  wsf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,7 +1,7 @@
 """The five synthetic workloads: shapes, storage types and value distributions.
 
 Each tensor is drawn from its own generator stream under seed 0: x from
-stream 0, w from stream 1, dy from stream 2.  ``N(m, s)`` means mean m and
+stream 0, w from stream 1, dy from stream 2, b from stream 3.  ``N(m, s)`` means mean m and
 standard deviation s.  Nothing here computes any part of the method.
 """
 from __future__ import annotations
@@ -11,7 +11,7 @@ from dataclasses import dataclass, field
 from . import NORMAL, UNIFORM
 
 SEED = 0
-STREAM_X, STREAM_W, STREAM_DY = 0, 1, 2
+STREAM_X, STREAM_W, STREAM_DY, STREAM_B = 0, 1, 2, 3
 
 
 @dataclass(frozen=True)
@@ -24,13 +24,16 @@ class Dist:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                  # "ws" (weighted sum), "silu" (scaled SiLU) or "softmax"
+    op: str                  # "ws" (weighted sum), "silu" (scaled SiLU), "softmax",
+                             # "rmsnorm" or "layernorm"
     dtype: str               # storage type of x, dy, y, dx: "f32" | "f16" | "bf16"
     N: int                   # rows (ws) or leading extent (silu)
     D: int                   # features (ws) or trailing extent (silu)
     x: Dist
     dy: Dist
-    w: Dist | None = None    # ws: w[D] in binary32
+    w: Dist | None = None    # ws, norms: w[D] in binary32
+    b: Dist | None = None    # layernorm: b[D] in binary32
+    eps: float = 0.0         # norms: the binary32 eps under the square root
     w_scalar: float | None = None  # silu: the scalar w in binary32
     block_n: int = 0         # rows per partial tile (0: the library chooses)
     note: str = ""
@@ -62,4 +65,14 @@ WORKLOADS = {
     "s1": Workload("s1", "softmax", "bf16", 65536, 4096, x=Dist(NORMAL, 0.0, 2.0),
                    dy=Dist(NORMAL, 0.0, 1.0),
                    note="row softmax, bf16 x[65536,4096] ~N(0,2), dy ~N(0,1)"),
+    # measurement cases of the norm backward: B·T = 65,536 token rows of
+    # width 4096 (the RMSNorm dw example of the backward-grid essay, and
+    # LayerNorm from the VJP essay); not part of the default benchmark step
+    "n1": Workload("n1", "rmsnorm", "bf16", 65536, 4096, x=Dist(NORMAL, 0.0, 1.0),
+                   w=Dist(NORMAL, 1.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0), eps=2.0 ** -17,
+                   note="RMSNorm, bf16 x[65536,4096] ~N(0,1), w ~N(1,0.1), eps 2^-17"),
+    "n2": Workload("n2", "layernorm", "bf16", 65536, 4096, x=Dist(NORMAL, 0.5, 1.0),
+                   w=Dist(NORMAL, 1.0, 0.1), b=Dist(NORMAL, 0.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0),
+                   eps=2.0 ** -17,
+                   note="LayerNorm, bf16 x[65536,4096] ~N(0.5,1), w ~N(1,0.1), b ~N(0,0.1), eps 2^-17"),
 }

@@ -201,3 +201,69 @@ def test_softmax_rejects(wsf):
     assert L.softmax_bwd(_p(F), 64, None, 64, _p(3 * F), 64, 10, 64, 1, s) == wsf.ERR_NULL_PTR
     assert L.softmax_bwd(_p(F), 64, _p(2 * F), 64, _p(2 * F + 2), 64, 10, 64, 1, s) == \
         wsf.ERR_OVERLAP
+
+
+def test_norm_workspace_queries(wsf):
+    r, l = wsf.lib.rmsnorm_bwd_workspace_bytes, wsf.lib.layernorm_bwd_workspace_bytes
+    # 100 rows: ceil(100/64) = 2 row tiles of D fp32 partials (twice for LayerNorm)
+    assert r(100, 64, wsf.F32) == 2 * 64 * 4 and l(100, 64, wsf.F32) == 2 * 2 * 64 * 4
+    assert r(65536, 4096, wsf.BF16) == 912 * 4096 * 4
+    assert l(65536, 4096, wsf.BF16) == 2 * 912 * 4096 * 4
+    assert r(0, 64, wsf.F16) == 0 and l(5, 0, wsf.F16) == 0
+    assert r(-1, 4, wsf.F32) == wsf.SIZE_MAX and l(4, 4, 3) == wsf.SIZE_MAX
+    assert r(1 << 20, 1 << 60, wsf.F32) == wsf.SIZE_MAX  # 16 tiles · 2^60 · 4 bytes overflows
+
+
+def test_norm_rejects(wsf):
+    L = wsf.lib
+    s = None
+    eps = 1e-5
+    rf = lambda x=F, ldx=64, w=2 * F, e=eps, y=3 * F, ldy=64, N=10, D=64, dt=1: L.rmsnorm_fwd(
+        _p(x) if x else None, ldx, _p(w) if w else None, e, _p(y) if y else None, ldy, N, D, dt, s)
+    assert rf(dt=5) == wsf.ERR_BAD_DTYPE
+    assert rf(N=-1) == wsf.ERR_BAD_SHAPE
+    assert rf(e=-1.0) == wsf.ERR_BAD_ARG and rf(e=float("nan")) == wsf.ERR_BAD_ARG
+    assert rf(e=float("inf")) == wsf.ERR_BAD_ARG
+    assert rf(ldx=63) == wsf.ERR_BAD_STRIDE and rf(ldy=8) == wsf.ERR_BAD_STRIDE
+    assert rf(x=0) == wsf.ERR_NULL_PTR and rf(w=0) == wsf.ERR_NULL_PTR
+    assert rf(x=F + 1) == wsf.ERR_MISALIGNED and rf(w=2 * F + 2) == wsf.ERR_MISALIGNED
+    assert rf(y=F + 64) == wsf.ERR_OVERLAP and rf(y=2 * F - 100) == wsf.ERR_OVERLAP
+    assert rf(x=0, w=0, y=0, N=0) == wsf.OK and rf(x=0, w=0, y=0, D=0) == wsf.OK
+    # LayerNorm needs b; b must not overlap y
+    assert L.layernorm_fwd(_p(F), 64, _p(2 * F), None, eps, _p(3 * F), 64, 10, 64, 1, s) == \
+        wsf.ERR_NULL_PTR
+    assert L.layernorm_fwd(_p(F), 64, _p(2 * F), _p(3 * F + 8), eps, _p(3 * F), 64, 10, 64, 1,
+                           s) == wsf.ERR_OVERLAP
+
+    need_r = L.rmsnorm_bwd_workspace_bytes(10, 64, 1)
+    need_l = L.layernorm_bwd_workspace_bytes(10, 64, 1)
+
+    def rb(x=F, w=2 * F, dy=3 * F, lddy=64, e=eps, dx=4 * F, lddx=64, gw=5 * F, acc=0, ws=6 * F,
+           wsb=need_r, N=10, D=64, dt=1):
+        P = lambda a: _p(a) if a else None
+        return L.rmsnorm_bwd(P(x), 64, P(w), P(dy), lddy, e, P(dx), lddx, P(gw), acc, P(ws), wsb,
+                             N, D, dt, s)
+
+    assert rb(dt=-1) == wsf.ERR_BAD_DTYPE
+    assert rb(D=-2) == wsf.ERR_BAD_SHAPE
+    assert rb(acc=2) == wsf.ERR_BAD_ARG and rb(e=-0.5) == wsf.ERR_BAD_ARG
+    assert rb(lddy=10) == wsf.ERR_BAD_STRIDE and rb(lddx=63) == wsf.ERR_BAD_STRIDE
+    assert rb(dy=0) == wsf.ERR_NULL_PTR and rb(gw=0) == wsf.ERR_NULL_PTR
+    assert rb(gw=5 * F + 2) == wsf.ERR_MISALIGNED and rb(dx=4 * F + 1) == wsf.ERR_MISALIGNED
+    assert rb(ws=0) == wsf.ERR_WORKSPACE and rb(wsb=need_r - 4) == wsf.ERR_WORKSPACE
+    assert rb(dx=3 * F + 64) == wsf.ERR_OVERLAP          # dx over dy
+    assert rb(gw=4 * F + 256) == wsf.ERR_OVERLAP         # grad_w inside dx
+    assert rb(ws=2 * F + 128) == wsf.ERR_OVERLAP         # workspace over w
+    assert rb(ws=5 * F - 4) == wsf.ERR_OVERLAP           # workspace over grad_w
+    assert rb(x=0, dy=0, dx=0, w=0, ws=0, wsb=0, D=0) == wsf.OK
+    assert rb(x=0, dy=0, dx=0, w=0, ws=0, wsb=0, N=0, gw=0) == wsf.ERR_NULL_PTR  # D > 0 needs grad_w
+
+    def lb(gw=5 * F, gb=7 * F, ws=6 * F, wsb=need_l):
+        P = lambda a: _p(a) if a else None
+        return L.layernorm_bwd(_p(F), 64, _p(2 * F), _p(3 * F), 64, eps, _p(4 * F), 64, P(gw), P(gb),
+                               0, P(ws), wsb, 10, 64, 1, s)
+
+    assert lb(gb=0) == wsf.ERR_NULL_PTR
+    assert lb(wsb=need_r) == wsf.ERR_WORKSPACE   # LayerNorm needs both partial blocks
+    assert lb(gb=5 * F + 128) == wsf.ERR_OVERLAP  # grad_b over grad_w
+    assert lb(gb=6 * F + 256) == wsf.ERR_OVERLAP  # grad_b inside the workspace
