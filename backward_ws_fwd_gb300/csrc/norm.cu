@@ -26,9 +26,9 @@
 // rounding (up to ulp(μ)/2) would shift every x̂ of a row with a large common
 // offset by the same amount, an error that does not cancel in Σ dy·x̂; and c
 // cannot be taken from Σ(x − μ₀) either, since the rounding of x − μ₀ has
-// one sign across a binade.  Σx is therefore compensated (TwoSum) for every
-// storage type; for binary32 the other row sums are compensated too (Dot2),
-// so that y and dx stay within 1e-6.  In the
+// one sign across a binade.  Σx is therefore carried as an exact pair for
+// every storage type (row_sum_x); for binary32 the other row sums are
+// compensated too (Dot2), so that y and dx stay within 1e-6.  In the
 // backward each thread sums dy·x̂ (and dy) for its own columns over the rows
 // of its CTA's row tile; the CTA's row groups are combined in index order into
 // one partial row per tile, and norm_bwd_reduce sums the tiles in a fixed
@@ -91,9 +91,34 @@ __device__ __forceinline__ Acc2 s_comb(Acc2 a, Acc2 b) {
 __device__ __forceinline__ float s_val(const Acc2& a) { return a.hi + a.lo; }
 
 // Reduce K sums over each aligned group of TPR threads: xor butterfly inside
-// a warp, then (groups wider than a warp) the warps' sums in index order
-// through `red` (K·NT/32 float2).  Every thread of the CTA calls it together;
-// every lane of a group ends with the same bits, on every run.
+// a warp; for groups wider than a warp, lane 0 of each warp posts its sums to
+// `red` (K·NT/32 float2) and, after a barrier, every warp loads the group's
+// NWG partials into its lanes (lane i takes partial i mod NWG) and runs a
+// second butterfly over NWG lanes.  Every thread of the CTA calls it together;
+// the order is fixed and every lane of a group ends with the same bits (the
+// compensated addition is symmetric in its operands).
+template <int TPR, int NT, int K, bool C>
+__device__ __forceinline__ void cross_warp(Acc2 (&v)[K], float2* red) {
+    if constexpr (TPR > 32) {
+        constexpr int NW = NT / 32, NWG = TPR / 32;
+        const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int first = (threadIdx.x / TPR) * NWG;
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < K; q++) red[q * NW + wid] = make_float2(v[q].hi, v[q].lo);
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < K; q++) {
+            const float2 t = red[q * NW + first + (lane % NWG)];
+            if constexpr (C)
+                v[q] = group_sum2<NWG>(Acc2{t.x, t.y});
+            else
+                v[q] = Acc2{group_sum<NWG>(t.x), 0.f};
+        }
+        __syncthreads();
+    }
+}
+
 template <int TPR, int NT, int K, bool C>
 __device__ __forceinline__ void group_reduce(Acc2 (&v)[K], float2* red) {
     constexpr int W = TPR < 32 ? TPR : 32;
@@ -104,46 +129,35 @@ __device__ __forceinline__ void group_reduce(Acc2 (&v)[K], float2* red) {
         else
             v[q].hi = group_sum<W>(v[q].hi);
     }
-    if constexpr (TPR > 32) {
-        constexpr int NW = NT / 32, NWG = TPR / 32;
-        const int wid = threadIdx.x >> 5, first = (threadIdx.x / TPR) * NWG;
-        if ((threadIdx.x & 31) == 0)
-#pragma unroll
-            for (int q = 0; q < K; q++) red[q * NW + wid] = make_float2(v[q].hi, v[q].lo);
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < K; q++) {
-            float2 t = red[q * NW + first];
-            Acc2 s{t.x, t.y};
-#pragma unroll
-            for (int i = 1; i < NWG; i++) {
-                t = red[q * NW + first + i];
-                s = s_comb<C>(s, Acc2{t.x, t.y});
-            }
-            v[q] = s;
-        }
-        __syncthreads();
-    }
+    cross_warp<TPR, NT, K, C>(v, red);
 }
 
-// 1/sqrt(ms + eps) with ms = Σ/D; each step is correctly rounded (IEEE
-// division and square root: this library is built without fast-math).
-__device__ __forceinline__ float rstd_of(float sum_sq, float d, float eps) {
-    return 1.0f / sqrtf(sum_sq / d + eps);
+// 1/sqrt(ms + eps) with ms = Σ·(1/D).  Binary32 storage: IEEE square root
+// and division (this library is built without fast-math), within about one
+// ulp.  16-bit storage: the hardware reciprocal square root (a few ulp of
+// binary32), far inside the half-ulp of the 16-bit output.
+template <bool Exact>
+__device__ __forceinline__ float rstd_of(float sum_sq, float inv_d, float eps) {
+    const float ms = fmaf(sum_sq, inv_d, eps);
+    if constexpr (Exact)
+        return 1.0f / sqrtf(ms);
+    else
+        return rsqrtf(ms);
 }
 
-// The row mean as μ₀ + c from the compensated sum s = Σx (hi + lo): μ₀ is
-// the rounded quotient and c = (Σx − D·μ₀)/D.  hi − D·μ₀ is exact in one fma
-// (a few bits wide, the remainder of a correctly rounded division plus the
-// rounding of hi + lo); adding lo and dividing each round once, relative to c.
+// The row mean as μ₀ + c from the pair s = Σx (hi + lo): μ₀ = (hi + lo)·(1/D)
+// within two ulp, and c = (Σx − D·μ₀)/D.  hi − D·μ₀ is exact in one fma: it
+// is a multiple of ulp(μ₀)/2^k no larger than a few ulp(hi), so it has at
+// most log2(D) + 3 significant bits.  Adding lo and scaling by 1/D then round
+// relative to c, which is only a correction.
 struct Mean {
     float mu0, c;
 };
 
-__device__ __forceinline__ Mean mean_of(const Acc2& s, float d) {
+__device__ __forceinline__ Mean mean_of(const Acc2& s, float d, float inv_d) {
     Mean m;
-    m.mu0 = s_val(s) / d;
-    m.c = (fmaf(-d, m.mu0, s.hi) + s.lo) / d;
+    m.mu0 = s_val(s) * inv_d;
+    m.c = (fmaf(-d, m.mu0, s.hi) + s.lo) * inv_d;
     return m;
 }
 
@@ -153,25 +167,94 @@ struct BwdStats {
     float r, mg, mgx;
 };
 
-template <bool LN, int K>
-__device__ __forceinline__ BwdStats bwd_stats(const Acc2 (&sums)[K], float d, float eps) {
+template <bool LN, bool Exact, int K>
+__device__ __forceinline__ BwdStats bwd_stats(const Acc2 (&sums)[K], float inv_d, float eps) {
     BwdStats st;
-    st.r = rstd_of(s_val(sums[0]), d, eps);
-    st.mgx = st.r * (s_val(sums[1]) / d);
-    st.mg = LN ? s_val(sums[K - 1]) / d : 0.f;
+    st.r = rstd_of<Exact>(s_val(sums[0]), inv_d, eps);
+    st.mgx = st.r * (s_val(sums[1]) * inv_d);
+    st.mg = LN ? s_val(sums[K - 1]) * inv_d : 0.f;
     return st;
 }
 
+// LayerNorm's row mean, and x turned into d = x − μ in place (valid chunks).
+// The mean is carried as μ₀ + c from a pair s = Σx (see mean_of); the pair
+// comes from a per-thread sum joined across the group by compensated
+// additions, so no rounding of the cross-thread sum (whose terms can be
+// ~16·|μ| each) reaches the mean.  Per thread, binary32 storage is summed
+// with TwoSum per element; 16-bit storage in plain binary32 (two partial
+// sums), which is exact while the 16 values share a small exponent range
+// (the case of a large common offset, where it matters) and otherwise errs
+// by a few ulp of a 16-term partial sum, tiny next to the spread of the row.
+template <typename T, int TPR, int NT, int CPT, int V>
+__device__ __forceinline__ void center_row(float (&f)[CPT][V], unsigned valid, float fd,
+                                           float inv_d, float2* red) {
+    Acc2 s[1] = {acc2_zero()};
+    if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+#pragma unroll
+            for (int v = 0; v < V; v++) s_add<true>(s[0], f[c][v]);  // invalid chunks are zero
+    } else {
+        float s1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+#pragma unroll
+            for (int v = 0; v < V; v += 2) {
+                s[0].hi += f[c][v];
+                s1 += f[c][v + 1];
+            }
+        s[0].hi += s1;
+    }
+    group_reduce<TPR, NT, 1, true>(s, red);
+    const Mean m = mean_of(s[0], fd, inv_d);
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+        if (valid >> c & 1u)
+#pragma unroll
+            for (int v = 0; v < V; v++) f[c][v] = (f[c][v] - m.mu0) - m.c;
+}
+
+// Per-thread cp.async staging of one row at a time: chunk c of the thread is
+// the 16 bytes at chunk index l + c·TPR of the row.  The source pointer and
+// the row index advance by a fixed step per staged row; rows at or past
+// row_end, and chunks outside the row, are zero-filled without a read.
+struct RowStager {
+    const char* src;   // chunk 0 of the next row to stage
+    const char* safe;  // any valid address (not read when the copy size is 0)
+    int64_t src_step;  // bytes between staged rows
+    int64_t row, row_step, row_end;
+};
+
 template <int TPR, int CPT, int NT>
-__device__ __forceinline__ void stage_chunks(Raw16* slots, const void* base, int64_t ld_bytes,
-                                             int64_t row, int64_t row_end, int Dv, int l) {
+__device__ __forceinline__ void stage_row(Raw16* slots, RowStager& st, unsigned valid) {
+    const bool rok = st.row < st.row_end;
 #pragma unroll
     for (int k = 0; k < CPT; k++) {
-        const int c = l + k * TPR;
-        const bool ok = row < row_end && c < Dv;
-        const char* src =
-            static_cast<const char*>(base) + (ok ? row * ld_bytes + (int64_t)c * 16 : 0);
-        cp_async16(&slots[k * NT + threadIdx.x], src, ok ? 16 : 0);
+        const bool ok = rok && (valid >> k & 1u);
+        cp_async16(&slots[k * NT + threadIdx.x], ok ? st.src + k * TPR * 16 : st.safe, ok ? 16 : 0);
+    }
+    st.src += st.src_step;
+    st.row += st.row_step;
+}
+
+template <int TPR, int CPT>
+__device__ __forceinline__ unsigned chunk_mask(int Dv, int l) {
+    unsigned m = 0;
+#pragma unroll
+    for (int k = 0; k < CPT; k++) m |= (l + k * TPR < Dv ? 1u : 0u) << k;
+    return m;
+}
+
+template <typename E, int CPT, int NT, int V>
+__device__ __forceinline__ void load_row(const Raw16* cur, unsigned valid, float (&f)[CPT][V]) {
+#pragma unroll
+    for (int c = 0; c < CPT; c++) {
+        if (valid >> c & 1u) {
+            E::widen(cur[c * NT], f[c]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; v++) f[c][v] = 0.f;
+        }
     }
 }
 
@@ -191,7 +274,8 @@ __device__ __forceinline__ void load_params(const float* __restrict__ p, int Dv,
 }
 
 // ===========================================================================
-// Forward, row path: R = NT/TPR rows per CTA iteration, grid-stride.
+// Forward, row path: R = NT/TPR rows per CTA iteration, grid-stride.  The
+// row is widened into registers once; LayerNorm turns it into d in place.
 // ===========================================================================
 template <typename T, bool LN, int TPR, int CPT, int NT, int S, int MINB>
 __global__ void __launch_bounds__(NT, MINB)
@@ -206,7 +290,8 @@ __global__ void __launch_bounds__(NT, MINB)
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     __shared__ float2 red[NT / 32];
     const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
-    const float fd = (float)(Dv * V);
+    const float fd = (float)(Dv * V), inv_d = 1.0f / fd;
+    const unsigned valid = chunk_mask<TPR, CPT>(Dv, l);
     pdl_wait();
     float wv[CPT][V], bv[CPT][V];
     load_params<TPR, CPT, V>(w, Dv, l, wv);
@@ -214,71 +299,54 @@ __global__ void __launch_bounds__(NT, MINB)
     const int64_t base = (int64_t)blockIdx.x * R, stride = (int64_t)gridDim.x * R;
     const int64_t iters = base < N ? (N - base + stride - 1) / stride : 0;
     const int64_t ldb = ldx * (int64_t)sizeof(T);
+    RowStager stg{reinterpret_cast<const char*>(x) + (base + g) * ldb + (int64_t)l * 16,
+                  reinterpret_cast<const char*>(x), stride * ldb, base + g, stride, N};
+    T* yrow = y + (base + g) * ldy + (int64_t)l * V;
+    const int64_t ystep = stride * ldy;
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
-        if (k < iters)
-            stage_chunks<TPR, CPT, NT>(xs + k * CPT * NT, x, ldb, base + k * stride + g, N, Dv, l);
+        if (k < iters) stage_row<TPR, CPT, NT>(xs + k * CPT * NT, stg, valid);
         cp_async_commit();
     }
     for (int64_t k = 0; k < iters; k++) {
         cp_async_wait<S - 2>();
-        const int64_t nk = k + S - 1;
-        if (nk < iters)
-            stage_chunks<TPR, CPT, NT>(xs + (nk % S) * CPT * NT, x, ldb, base + nk * stride + g, N,
-                                       Dv, l);
+        if (k + S - 1 < iters) stage_row<TPR, CPT, NT>(xs + ((k + S - 1) % S) * CPT * NT, stg, valid);
         cp_async_commit();
         const int64_t row = base + k * stride + g;
-        const Raw16* cur = xs + (k % S) * CPT * NT + threadIdx.x;
-        Mean m{0.f, 0.f};
-        if constexpr (LN) {
-            Acc2 s[1] = {acc2_zero()};
+        float f[CPT][V];
+        load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
+        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red);
+        Acc2 ss[1] = {acc2_zero()};  // Σ d², d = x (RMSNorm) or x − μ (LayerNorm)
 #pragma unroll
-            for (int c = 0; c < CPT; c++) {
-                float f[V];
-                E::widen(cur[c * NT], f);  // masked chunks are zero-filled
+        for (int c = 0; c < CPT; c++)
+            if (valid >> c & 1u)
 #pragma unroll
-                for (int v = 0; v < V; v++) s_add<true>(s[0], f[v]);
-            }
-            group_reduce<TPR, NT, 1, true>(s, red);
-            m = mean_of(s[0], fd);
-        }
-        Acc2 ss[1] = {acc2_zero()};  // Σ d², d = (x − μ₀) − c
-#pragma unroll
-        for (int c = 0; c < CPT; c++) {
-            if (l + c * TPR < Dv) {
-                float f[V];
-                E::widen(cur[c * NT], f);
-#pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float d = (f[v] - m.mu0) - m.c;
-                    s_fma<C>(ss[0], d, d);
-                }
-            }
-        }
+                for (int v = 0; v < V; v++) s_fma<C>(ss[0], f[c][v], f[c][v]);
         group_reduce<TPR, NT, 1, C>(ss, red);
-        const float r = rstd_of(s_val(ss[0]), fd, eps);
+        const float r = rstd_of<C>(s_val(ss[0]), inv_d, eps);
         if (row < N) {
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
-                if (l + c * TPR < Dv) {
-                    float f[V], o[V];
-                    E::widen(cur[c * NT], f);
+                if (valid >> c & 1u) {
+                    float o[V];
 #pragma unroll
                     for (int v = 0; v < V; v++) {
-                        const float xh = ((f[v] - m.mu0) - m.c) * r;
+                        const float xh = f[c][v] * r;
                         o[v] = LN ? fmaf(xh, wv[c][v], bv[c][v]) : xh * wv[c][v];
                     }
-                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                    st_stream(yrow + (int64_t)c * TPR * V, E::narrow(o));
                 }
             }
         }
+        yrow += ystep;
     }
     cp_async_wait<0>();
     pdl_trigger();
 }
 
 // ===========================================================================
-// Backward stage 1, row path: blockIdx.x = row tile p, rows [ra, rb).
+// Backward stage 1, row path: blockIdx.x = row tile p, rows [ra, rb).  x and
+// dy are widened into registers once per row; x becomes d in place.
 // ===========================================================================
 template <typename T, bool LN, int TPR, int CPT, int NT, int S, int MINB>
 __global__ void __launch_bounds__(NT, MINB)
@@ -296,7 +364,8 @@ __global__ void __launch_bounds__(NT, MINB)
     Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
     __shared__ float2 red[K * (NT / 32)];
     const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
-    const float fd = (float)D;
+    const float fd = (float)D, inv_d = 1.0f / fd;
+    const unsigned valid = chunk_mask<TPR, CPT>(Dv, l);
     int64_t ra, rb;
     norm_tile_rows(blockIdx.x, P, N, ra, rb);
     pdl_wait();
@@ -310,83 +379,70 @@ __global__ void __launch_bounds__(NT, MINB)
 
     const int64_t iters = (rb - ra + R - 1) / R;
     const int64_t ldxb = ldx * (int64_t)sizeof(T), ldgb = lddy * (int64_t)sizeof(T);
+    RowStager sx{reinterpret_cast<const char*>(x) + (ra + g) * ldxb + (int64_t)l * 16,
+                 reinterpret_cast<const char*>(x), R * ldxb, ra + g, R, rb};
+    RowStager sg{reinterpret_cast<const char*>(dy) + (ra + g) * ldgb + (int64_t)l * 16,
+                 reinterpret_cast<const char*>(dy), R * ldgb, ra + g, R, rb};
+    T* dxrow = dx + (ra + g) * lddx + (int64_t)l * V;
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
         if (k < iters) {
-            stage_chunks<TPR, CPT, NT>(xs + k * CPT * NT, x, ldxb, ra + k * R + g, rb, Dv, l);
-            stage_chunks<TPR, CPT, NT>(gs + k * CPT * NT, dy, ldgb, ra + k * R + g, rb, Dv, l);
+            stage_row<TPR, CPT, NT>(xs + k * CPT * NT, sx, valid);
+            stage_row<TPR, CPT, NT>(gs + k * CPT * NT, sg, valid);
         }
         cp_async_commit();
     }
     for (int64_t k = 0; k < iters; k++) {
         cp_async_wait<S - 2>();
-        const int64_t nk = k + S - 1;
-        if (nk < iters) {
-            stage_chunks<TPR, CPT, NT>(xs + (nk % S) * CPT * NT, x, ldxb, ra + nk * R + g, rb, Dv,
-                                       l);
-            stage_chunks<TPR, CPT, NT>(gs + (nk % S) * CPT * NT, dy, ldgb, ra + nk * R + g, rb,
-                                       Dv, l);
+        if (k + S - 1 < iters) {
+            stage_row<TPR, CPT, NT>(xs + ((k + S - 1) % S) * CPT * NT, sx, valid);
+            stage_row<TPR, CPT, NT>(gs + ((k + S - 1) % S) * CPT * NT, sg, valid);
         }
         cp_async_commit();
         const int64_t row = ra + k * R + g;
-        const Raw16* cx = xs + (k % S) * CPT * NT + threadIdx.x;
-        const Raw16* cg = gs + (k % S) * CPT * NT + threadIdx.x;
-        Mean m{0.f, 0.f};
-        if constexpr (LN) {
-            Acc2 s[1] = {acc2_zero()};
-#pragma unroll
-            for (int c = 0; c < CPT; c++) {
-                float f[V];
-                E::widen(cx[c * NT], f);  // masked chunks and rows are zero-filled
-#pragma unroll
-                for (int v = 0; v < V; v++) s_add<true>(s[0], f[v]);
-            }
-            group_reduce<TPR, NT, 1, true>(s, red);
-            m = mean_of(s[0], fd);
-        }
+        float f[CPT][V], gd[CPT][V];
+        load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
+        load_row<E, CPT, NT, V>(gs + (k % S) * CPT * NT + threadIdx.x, valid, gd);
+        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red);
         // sums[0] = Σ d², sums[1] = Σ g·d, and for LayerNorm sums[2] = Σ g;
-        // d = (x − μ₀) − c, g = dy·w
+        // d = x (RMSNorm) or x − μ (LayerNorm), g = dy·w
         Acc2 sums[K];
 #pragma unroll
         for (int q = 0; q < K; q++) sums[q] = acc2_zero();
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            if (l + c * TPR < Dv) {
-                float f[V], gd[V];
-                E::widen(cx[c * NT], f);
-                E::widen(cg[c * NT], gd);
+            if (valid >> c & 1u) {
 #pragma unroll
                 for (int v = 0; v < V; v++) {
-                    const float d = (f[v] - m.mu0) - m.c;
-                    const float gg = gd[v] * wv[c][v];
-                    s_fma<C>(sums[0], d, d);
-                    s_fma<C>(sums[1], gg, d);
+                    const float gg = gd[c][v] * wv[c][v];
+                    s_fma<C>(sums[0], f[c][v], f[c][v]);
+                    s_fma<C>(sums[1], gg, f[c][v]);
                     if constexpr (LN) s_add<C>(sums[2], gg);
                 }
             }
         }
         group_reduce<TPR, NT, K, C>(sums, red);
-        const BwdStats st = bwd_stats<LN>(sums, fd, eps);
+        const BwdStats st = bwd_stats<LN, C>(sums, inv_d, eps);
         if (row < rb) {
+            const float r = st.r, rmg = st.r * st.mg, rmgx = st.r * st.mgx;
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
-                if (l + c * TPR < Dv) {
-                    float f[V], gd[V], o[V];
-                    E::widen(cx[c * NT], f);
-                    E::widen(cg[c * NT], gd);
-                    const float r = st.r, mg = st.mg, mgx = st.mgx;
+                if (valid >> c & 1u) {
+                    float o[V];
 #pragma unroll
                     for (int v = 0; v < V; v++) {
-                        const float xh = ((f[v] - m.mu0) - m.c) * r;
-                        const float gg = gd[v] * wv[c][v];
-                        o[v] = r * ((gg - mg) - xh * mgx);
-                        aw[c][v] = fmaf(gd[v], xh, aw[c][v]);
-                        if constexpr (LN) ab[c][v] += gd[v];
+                        const float xh = f[c][v] * r;
+                        const float gg = gd[c][v] * wv[c][v];
+                        // r·((g − mean g) − x̂·mean(g·x̂))
+                        o[v] = fmaf(-xh, rmgx, fmaf(gg, r, -rmg));
+                        aw[c][v] = fmaf(gd[c][v], xh, aw[c][v]);
+                        if constexpr (LN) ab[c][v] += gd[c][v];
                     }
-                    st_stream(dx + row * lddx + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                    st_stream(dxrow + (int64_t)c * TPR * V, E::narrow(o));
                 }
             }
         }
+        dxrow += R * lddx;
     }
     cp_async_wait<0>();
     pdl_trigger();
@@ -432,7 +488,7 @@ __global__ void __launch_bounds__(NT)
     using E = Elt<T>;
     constexpr bool C = std::is_same<T, float>::value;
     __shared__ float2 red[NT / 32];
-    const float fd = (float)D;
+    const float fd = (float)D, inv_d = 1.0f / fd;
     pdl_wait();
     for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
         const T* xr = x + row * ldx;
@@ -441,7 +497,7 @@ __global__ void __launch_bounds__(NT)
             Acc2 s[1] = {acc2_zero()};
             for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
             group_reduce<NT, NT, 1, true>(s, red);
-            m = mean_of(s[0], fd);
+            m = mean_of(s[0], fd, inv_d);
         }
         Acc2 ss[1] = {acc2_zero()};
         for (int64_t j = threadIdx.x; j < D; j += NT) {
@@ -449,7 +505,7 @@ __global__ void __launch_bounds__(NT)
             s_fma<C>(ss[0], d, d);
         }
         group_reduce<NT, NT, 1, C>(ss, red);
-        const float r = rstd_of(s_val(ss[0]), fd, eps);
+        const float r = rstd_of<C>(s_val(ss[0]), inv_d, eps);
         for (int64_t j = threadIdx.x; j < D; j += NT) {
             const float xh = ((E::load1(xr + j) - m.mu0) - m.c) * r;
             E::store1(y + row * ldy + j,
@@ -468,7 +524,7 @@ __global__ void __launch_bounds__(NT)
     constexpr bool C = std::is_same<T, float>::value;
     constexpr int K = LN ? 3 : 2;
     __shared__ float2 red[K * (NT / 32)];
-    const float fd = (float)D;
+    const float fd = (float)D, inv_d = 1.0f / fd;
     int64_t ra, rb;
     norm_tile_rows(blockIdx.x, P, N, ra, rb);
     pdl_wait();
@@ -487,7 +543,7 @@ __global__ void __launch_bounds__(NT)
             Acc2 s[1] = {acc2_zero()};
             for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
             group_reduce<NT, NT, 1, true>(s, red);
-            m = mean_of(s[0], fd);
+            m = mean_of(s[0], fd, inv_d);
         }
         Acc2 sums[K];
 #pragma unroll
@@ -500,7 +556,7 @@ __global__ void __launch_bounds__(NT)
             if constexpr (LN) s_add<C>(sums[2], gg);
         }
         group_reduce<NT, NT, K, C>(sums, red);
-        const BwdStats st = bwd_stats<LN>(sums, fd, eps);
+        const BwdStats st = bwd_stats<LN, C>(sums, inv_d, eps);
         for (int64_t j = threadIdx.x; j < D; j += NT) {
             const float g0 = E::load1(gr + j);
             const float xh = ((E::load1(xr + j) - m.mu0) - m.c) * st.r;

@@ -1,9 +1,9 @@
 """GPU parity of RMSNorm and LayerNorm, forward and backward, against the fp64
 oracle: every row-width class of the staged path, the element-wise path
-(unaligned or wider than 8192), row strides and guard bands, constant and
-offset rows, tall inputs that fill all 912 row tiles, accumulate, empty
-extents, bit reproducibility, and the measurement size (sampled dx rows, full
-grad_w / grad_b)."""
+(unaligned or wider than 8192), row strides and guard bands, constant rows,
+rows with a large common offset or with massive outlier columns, tall inputs
+that fill all 912 row tiles, accumulate, empty extents, bit reproducibility,
+and the measurement size (sampled dx rows, full grad_w / grad_b)."""
 import numpy as np
 import pytest
 import torch
@@ -122,6 +122,18 @@ def test_norm_constant_and_offset_rows(wsf, dt):
     x[4] = 0.25        # LayerNorm: zero variance
     x[5, ::2] = -2.0   # LayerNorm: two-valued row
     x[5, 1::2] = 2.0
+    for layer in (False, True):
+        _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b))
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_norm_outlier_columns(wsf, dt):
+    # one large value in the same columns of every row (the first element of
+    # the row and one inside it), as in activations with a few massive
+    # features; the row mean then sits far from most elements
+    x, w, dy, b = _inputs(300, 1024, dt, seed=11)
+    x[:, 0] = 500.0
+    x[:, 517] = -300.0
     for layer in (False, True):
         _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b))
 
