@@ -1,4 +1,4 @@
-"""torch.autograd glue over the C ABI: the two operators as differentiable ops.
+"""torch.autograd glue over the C ABI: the operators as differentiable ops.
 
 "Writing Triton Kernels with Autograd: A Minimal End-to-End Example", §5
 Wrapping with torch.autograd.Function, and "Backward in Triton —
@@ -7,6 +7,10 @@ the forward saves (x, w), the backward receives dy and returns one gradient
 per forward argument, in order, with None for a non-differentiable flag.
 Both gradients of each operator come from one backward launch pair (stage 1
 and the fixed-order stage 2); nothing here computes anything itself.
+
+RMSNorm and LayerNorm follow "Backward in Triton — autograd.Function and
+the backward grid", § Save vs recompute: the forward saves only x and the
+parameters, and the backward recomputes the row statistics from x.
 
 Gradient accumulation across micro-batches ("fp32 accumulation, and why
 gradients use +=") happens in PyTorch's engine, which adds each returned
@@ -18,7 +22,8 @@ from __future__ import annotations
 
 import torch
 
-from . import silu_bwd, silu_fwd, ws_bwd, ws_fwd
+from . import (layernorm_bwd, layernorm_fwd, rmsnorm_bwd, rmsnorm_fwd, silu_bwd, silu_fwd,
+               ws_bwd, ws_fwd)
 
 _STORAGE = (torch.float32, torch.float16, torch.bfloat16)
 
@@ -81,6 +86,62 @@ class ScaledSiLUFunction(torch.autograd.Function):
         return (dx if need_x else None), (dw.reshape(w.shape) if need_w else None), None
 
 
+class RMSNormFunction(torch.autograd.Function):
+    """y = x·r·w over the last dimension, r = 1/sqrt(mean x² + eps); x of
+    storage type fp32/fp16/bf16 (y has x's type), w fp32 [D]."""
+
+    @staticmethod
+    def forward(ctx, x, w, eps=1e-5):
+        if x.dtype not in _STORAGE or w.dtype != torch.float32:
+            raise TypeError("x must be float32/float16/bfloat16 and w float32")
+        x2 = _rows(x)
+        w = w.contiguous()
+        y = rmsnorm_fwd(x2, w, eps)
+        ctx.save_for_backward(x2, w)
+        ctx.eps, ctx.x_shape = eps, x.shape
+        return y.reshape(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, w = ctx.saved_tensors
+        dy = _rows(dy.reshape(x2.shape))
+        dx, grad_w = rmsnorm_bwd(x2, w, dy, ctx.eps)
+        need_x, need_w, _ = ctx.needs_input_grad
+        return (dx.reshape(ctx.x_shape) if need_x else None), (grad_w if need_w else None), None
+
+
+class LayerNormFunction(torch.autograd.Function):
+    """y = (x − mean)·r·w + b over the last dimension, r = 1/sqrt(var + eps)."""
+
+    @staticmethod
+    def forward(ctx, x, w, b, eps=1e-5):
+        if x.dtype not in _STORAGE or w.dtype != torch.float32 or b.dtype != torch.float32:
+            raise TypeError("x must be float32/float16/bfloat16, w and b float32")
+        x2 = _rows(x)
+        w, b = w.contiguous(), b.contiguous()
+        y = layernorm_fwd(x2, w, b, eps)
+        ctx.save_for_backward(x2, w)
+        ctx.eps, ctx.x_shape = eps, x.shape
+        return y.reshape(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, w = ctx.saved_tensors
+        dy = _rows(dy.reshape(x2.shape))
+        dx, grad_w, grad_b = layernorm_bwd(x2, w, dy, ctx.eps)
+        need_x, need_w, need_b, _ = ctx.needs_input_grad
+        return ((dx.reshape(ctx.x_shape) if need_x else None), (grad_w if need_w else None),
+                (grad_b if need_b else None), None)
+
+
+def rms_norm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-5) -> torch.Tensor:
+    return RMSNormFunction.apply(x, w, eps)
+
+
+def layer_norm(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, eps: float = 1e-5) -> torch.Tensor:
+    return LayerNormFunction.apply(x, w, b, eps)
+
+
 def weighted_sum(x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
     return WeightedSumFunction.apply(x, w)
 
@@ -111,3 +172,28 @@ class ScaledSiLU(torch.nn.Module):
 
     def forward(self, x):
         return scaled_silu(x, self.w)
+
+
+class RMSNorm(torch.nn.Module):
+    """RMSNorm over the last dimension with a learnable fp32 scale (init 1)."""
+
+    def __init__(self, D: int, eps: float = 1e-5, device=None):
+        super().__init__()
+        self.eps = eps
+        self.weight = torch.nn.Parameter(torch.ones(D, dtype=torch.float32, device=device))
+
+    def forward(self, x):
+        return rms_norm(x, self.weight, self.eps)
+
+
+class LayerNorm(torch.nn.Module):
+    """LayerNorm over the last dimension with learnable fp32 scale and shift."""
+
+    def __init__(self, D: int, eps: float = 1e-5, device=None):
+        super().__init__()
+        self.eps = eps
+        self.weight = torch.nn.Parameter(torch.ones(D, dtype=torch.float32, device=device))
+        self.bias = torch.nn.Parameter(torch.zeros(D, dtype=torch.float32, device=device))
+
+    def forward(self, x):
+        return layer_norm(x, self.weight, self.bias, self.eps)

@@ -154,3 +154,46 @@ def test_gradcheck_fp32(ag):
     assert torch.autograd.gradcheck(lambda a, b: ag.scaled_silu(a, b), (xs, ws), eps=1e-2,
                                     atol=2e-3, rtol=2e-3, check_grad_dtypes=False,
                                     raise_exception=True)
+
+
+@pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_norm_autograd_matches_oracle(ag, layer, dt):
+    import inputgen
+    eps = 2.0 ** -17
+    x = inputgen.make((3, 50, 768), dt, NORMAL, 0.2, 1, 4, 0)   # leading batch dims
+    w = inputgen.make((768,), "f32", NORMAL, 1, 0.1, 4, 1)
+    b = inputgen.make((768,), "f32", NORMAL, 0, 0.1, 4, 3)
+    dy = inputgen.make((3, 50, 768), dt, NORMAL, 0, 1, 4, 2)
+    xd = x.to(DEV).requires_grad_()
+    wd = w.to(DEV).requires_grad_()
+    bd = b.to(DEV).requires_grad_()
+    y = ag.layer_norm(xd, wd, bd, eps) if layer else ag.rms_norm(xd, wd, eps)
+    assert y.shape == x.shape and y.dtype == x.dtype
+    y.backward(dy.to(DEV).transpose(0, 1).contiguous().transpose(0, 1))  # non-contiguous dy
+    x2, dy2 = x.reshape(-1, 768), dy.reshape(-1, 768)
+    f = oracle.norm_fwd(x2, w, b if layer else None, eps, layer)
+    assert check_elementwise(y.detach().cpu().reshape(-1, 768), f["y"], f["y_exact"],
+                             scale=f["y_scale"])
+    r = oracle.norm_bwd(x2, w, dy2, eps, layer)
+    assert check_elementwise(xd.grad.cpu().reshape(-1, 768), r["dx"], r["dx_exact"],
+                             scale=r["dx_scale"])
+    assert check_reduction(wd.grad.cpu(), r["grad_w"], r["grad_w_abs"], 150, GRAD_TOL)
+    if layer:
+        assert check_reduction(bd.grad.cpu(), r["grad_b"], r["grad_b_abs"], 150, GRAD_TOL)
+    else:
+        assert bd.grad is None
+
+
+def test_norm_modules_accumulate_grad(ag):
+    m = ag.LayerNorm(256, device=DEV)
+    x = torch.randn(64, 256, device=DEV)
+    g = torch.randn(64, 256, device=DEV)
+    m(x).backward(g)
+    first = m.weight.grad.clone(), m.bias.grad.clone()
+    m(x).backward(g)  # a second micro-batch: PyTorch adds into .grad
+    assert torch.equal(m.weight.grad, first[0] + first[0])
+    assert torch.equal(m.bias.grad, first[1] + first[1])
+    r = ag.RMSNorm(256, device=DEV)
+    r(x.to(torch.bfloat16)).float().sum().backward()
+    assert r.weight.grad is not None and r.weight.grad.shape == (256,)
