@@ -96,7 +96,10 @@ __device__ __forceinline__ float s_val(const Acc2& a) { return a.hi + a.lo; }
 // NWG partials into its lanes (lane i takes partial i mod NWG) and runs a
 // second butterfly over NWG lanes.  Every thread of the CTA calls it together;
 // the order is fixed and every lane of a group ends with the same bits (the
-// compensated addition is symmetric in its operands).
+// compensated addition is symmetric in its operands).  There is no barrier
+// after the reads: callers alternate between two `red` buffers (RedRing), so
+// a buffer is written again only after another reduction's barrier, which no
+// thread passes before every thread has read this one.
 template <int TPR, int NT, int K, bool C>
 __device__ __forceinline__ void cross_warp(Acc2 (&v)[K], float2* red) {
     if constexpr (TPR > 32) {
@@ -115,9 +118,18 @@ __device__ __forceinline__ void cross_warp(Acc2 (&v)[K], float2* red) {
             else
                 v[q] = Acc2{group_sum<NWG>(t.x), 0.f};
         }
-        __syncthreads();
     }
 }
+
+// Two shared reduction buffers used in turn (see cross_warp).  The turn is
+// counted per thread: every thread of the CTA takes the buffers in the same
+// sequence, so all of them agree on which one is current.
+template <int N>
+struct RedRing {
+    float2 (*buf)[N];  // shared [2][N]
+    int next;
+    __device__ __forceinline__ float2* take() { return buf[(next++) & 1]; }
+};
 
 template <int TPR, int NT, int K, bool C>
 __device__ __forceinline__ void group_reduce(Acc2 (&v)[K], float2* red) {
@@ -177,19 +189,21 @@ __device__ __forceinline__ BwdStats bwd_stats(const Acc2 (&sums)[K], float inv_d
 }
 
 // LayerNorm's row mean, and x turned into d = x − μ in place (valid chunks).
-// The mean is carried as μ₀ + c from a pair s = Σx (see mean_of); the pair
-// comes from a per-thread sum joined across the group by compensated
-// additions, so no rounding of the cross-thread sum (whose terms can be
-// ~16·|μ| each) reaches the mean.  Per thread, binary32 storage is summed
-// with TwoSum per element; 16-bit storage in plain binary32 (two partial
-// sums), which is exact while the 16 values share a small exponent range
-// (the case of a large common offset, where it matters) and otherwise errs
-// by a few ulp of a 16-term partial sum, tiny next to the spread of the row.
+// The mean is carried as μ₀ + c from a pair s = Σx (see mean_of).
+// binary32 storage: TwoSum per element and compensated additions across the
+// group, so no rounding of the sum reaches the mean.  16-bit storage: plain
+// binary32 sums, which are exact where it matters — a row whose values share
+// a large common offset has them on the coarse grid of that offset (ulp(100)
+// is 0.5 in bfloat16, 1/16 in binary16), and the row sum stays below 2^24
+// grid steps — while an addition rounds only where an element is fine-grained,
+// i.e. small, and then errs by a few ulp of the partial sum, tiny next to the
+// spread of the row.
 template <typename T, int TPR, int NT, int CPT, int V>
 __device__ __forceinline__ void center_row(float (&f)[CPT][V], unsigned valid, float fd,
                                            float inv_d, float2* red) {
+    constexpr bool C = std::is_same<T, float>::value;
     Acc2 s[1] = {acc2_zero()};
-    if constexpr (std::is_same<T, float>::value) {
+    if constexpr (C) {
 #pragma unroll
         for (int c = 0; c < CPT; c++)
 #pragma unroll
@@ -205,7 +219,7 @@ __device__ __forceinline__ void center_row(float (&f)[CPT][V], unsigned valid, f
             }
         s[0].hi += s1;
     }
-    group_reduce<TPR, NT, 1, true>(s, red);
+    group_reduce<TPR, NT, 1, C>(s, red);
     const Mean m = mean_of(s[0], fd, inv_d);
 #pragma unroll
     for (int c = 0; c < CPT; c++)
@@ -288,7 +302,8 @@ __global__ void __launch_bounds__(NT, MINB)
     constexpr bool C = std::is_same<T, float>::value;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
-    __shared__ float2 red[NT / 32];
+    __shared__ float2 red_buf[2][NT / 32];
+    RedRing<NT / 32> red{red_buf, 0};
     const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
     const float fd = (float)(Dv * V), inv_d = 1.0f / fd;
     const unsigned valid = chunk_mask<TPR, CPT>(Dv, l);
@@ -315,14 +330,14 @@ __global__ void __launch_bounds__(NT, MINB)
         const int64_t row = base + k * stride + g;
         float f[CPT][V];
         load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
-        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red);
+        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red.take());
         Acc2 ss[1] = {acc2_zero()};  // Σ d², d = x (RMSNorm) or x − μ (LayerNorm)
 #pragma unroll
         for (int c = 0; c < CPT; c++)
             if (valid >> c & 1u)
 #pragma unroll
                 for (int v = 0; v < V; v++) s_fma<C>(ss[0], f[c][v], f[c][v]);
-        group_reduce<TPR, NT, 1, C>(ss, red);
+        group_reduce<TPR, NT, 1, C>(ss, red.take());
         const float r = rstd_of<C>(s_val(ss[0]), inv_d, eps);
         if (row < N) {
 #pragma unroll
@@ -362,7 +377,8 @@ __global__ void __launch_bounds__(NT, MINB)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
-    __shared__ float2 red[K * (NT / 32)];
+    __shared__ float2 red_buf[2][K * (NT / 32)];
+    RedRing<K * (NT / 32)> red{red_buf, 0};
     const int g = threadIdx.x / TPR, l = threadIdx.x % TPR;
     const float fd = (float)D, inv_d = 1.0f / fd;
     const unsigned valid = chunk_mask<TPR, CPT>(Dv, l);
@@ -403,7 +419,7 @@ __global__ void __launch_bounds__(NT, MINB)
         float f[CPT][V], gd[CPT][V];
         load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
         load_row<E, CPT, NT, V>(gs + (k % S) * CPT * NT + threadIdx.x, valid, gd);
-        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red);
+        if constexpr (LN) center_row<T, TPR, NT, CPT, V>(f, valid, fd, inv_d, red.take());
         // sums[0] = Σ d², sums[1] = Σ g·d, and for LayerNorm sums[2] = Σ g;
         // d = x (RMSNorm) or x − μ (LayerNorm), g = dy·w
         Acc2 sums[K];
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(NT, MINB)
                 }
             }
         }
-        group_reduce<TPR, NT, K, C>(sums, red);
+        group_reduce<TPR, NT, K, C>(sums, red.take());
         const BwdStats st = bwd_stats<LN, C>(sums, inv_d, eps);
         if (row < rb) {
             const float r = st.r, rmg = st.r * st.mg, rmgx = st.r * st.mgx;
@@ -487,7 +503,8 @@ __global__ void __launch_bounds__(NT)
                     int64_t N, int64_t D) {
     using E = Elt<T>;
     constexpr bool C = std::is_same<T, float>::value;
-    __shared__ float2 red[NT / 32];
+    __shared__ float2 red_buf[2][NT / 32];
+    RedRing<NT / 32> red{red_buf, 0};
     const float fd = (float)D, inv_d = 1.0f / fd;
     pdl_wait();
     for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
@@ -496,7 +513,7 @@ __global__ void __launch_bounds__(NT)
         if constexpr (LN) {
             Acc2 s[1] = {acc2_zero()};
             for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
-            group_reduce<NT, NT, 1, true>(s, red);
+            group_reduce<NT, NT, 1, true>(s, red.take());
             m = mean_of(s[0], fd, inv_d);
         }
         Acc2 ss[1] = {acc2_zero()};
@@ -504,7 +521,7 @@ __global__ void __launch_bounds__(NT)
             const float d = (E::load1(xr + j) - m.mu0) - m.c;
             s_fma<C>(ss[0], d, d);
         }
-        group_reduce<NT, NT, 1, C>(ss, red);
+        group_reduce<NT, NT, 1, C>(ss, red.take());
         const float r = rstd_of<C>(s_val(ss[0]), inv_d, eps);
         for (int64_t j = threadIdx.x; j < D; j += NT) {
             const float xh = ((E::load1(xr + j) - m.mu0) - m.c) * r;
@@ -523,7 +540,8 @@ __global__ void __launch_bounds__(NT)
     using E = Elt<T>;
     constexpr bool C = std::is_same<T, float>::value;
     constexpr int K = LN ? 3 : 2;
-    __shared__ float2 red[K * (NT / 32)];
+    __shared__ float2 red_buf[2][K * (NT / 32)];
+    RedRing<K * (NT / 32)> red{red_buf, 0};
     const float fd = (float)D, inv_d = 1.0f / fd;
     int64_t ra, rb;
     norm_tile_rows(blockIdx.x, P, N, ra, rb);
@@ -542,7 +560,7 @@ __global__ void __launch_bounds__(NT)
         if constexpr (LN) {
             Acc2 s[1] = {acc2_zero()};
             for (int64_t j = threadIdx.x; j < D; j += NT) s_add<true>(s[0], E::load1(xr + j));
-            group_reduce<NT, NT, 1, true>(s, red);
+            group_reduce<NT, NT, 1, true>(s, red.take());
             m = mean_of(s[0], fd, inv_d);
         }
         Acc2 sums[K];
@@ -555,7 +573,7 @@ __global__ void __launch_bounds__(NT)
             s_fma<C>(sums[1], gg, d);
             if constexpr (LN) s_add<C>(sums[2], gg);
         }
-        group_reduce<NT, NT, K, C>(sums, red);
+        group_reduce<NT, NT, K, C>(sums, red.take());
         const BwdStats st = bwd_stats<LN, C>(sums, inv_d, eps);
         for (int64_t j = threadIdx.x; j < D; j += NT) {
             const float g0 = E::load1(gr + j);
