@@ -220,15 +220,29 @@ def calibrated_fraction(names, budget_s: float, max_frac: float = 1 / 16):
 
 
 def cpu_baseline(names):
+    """The oracle on this host: all cores (OpenMP; the main figure) and one
+    core, each on a bounded sample of the workloads (about 10 s of work)."""
     import oracle
     oracle.build()
-    frac = calibrated_fraction(names, budget_s=10.0)
-    samples = oracle_sample(names, frac)
-    t = time.perf_counter()
-    nbytes = oracle_step(samples)
-    dt = time.perf_counter() - t
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": sample_desc(samples) + f"; {dt:.1f} s of single-threaded fp64 CPU work"}
+    cores = oracle.threads()
+    out = {}
+    for label, n in (("all", cores), ("one", 1)):
+        old = oracle.set_threads(n)
+        try:
+            frac = calibrated_fraction(names, budget_s=8.0)
+            samples = oracle_sample(names, frac)
+            t = time.perf_counter()
+            nbytes = oracle_step(samples)
+            dt = time.perf_counter() - t
+        finally:
+            oracle.set_threads(old)
+        out[label] = (nbytes / dt / 1e9, dt, samples)
+    v, dt, samples = out["all"]
+    v1, dt1, samples1 = out["one"]
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample_desc(samples) + f"; {dt:.1f} s of fp64 CPU work on {cores} threads",
+            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": sample_desc(samples1) + f"; {dt1:.1f} s"}}
 
 
 def run_reference(args, names):
@@ -237,6 +251,7 @@ def run_reference(args, names):
         return 0
     import oracle
     oracle.build()
+    cores = oracle.threads()
     budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
     frac = calibrated_fraction(names, budget_s=budget)
     samples = oracle_sample(names, frac)
@@ -255,7 +270,7 @@ def run_reference(args, names):
             "impl": "reference",
             "config": {"workload": workload_label(names) + (f" (rows x {args.scale})"
                                                              if args.scale != 1.0 else ""), "reference": "fp64 CPU oracle"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": sample_desc(samples)},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -478,6 +493,11 @@ def run_cuda(args, names):
     per_op_ms = [sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)) / args.steps
                  for j in range(len(ops))]
 
+    # isolated per-op protocol: an L2 flush (a write of twice the L2 size)
+    # before every timed op, 5 warm-ups, the median of 20; fwd+bwd is the two
+    # ops back to back after one flush
+    isolated = isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS) if args.isolated else None
+
     # end to end through the public API with host buffers: every input is
     # copied from pinned host memory and every output back, inside the timed
     # region.  Each workload is cut into row chunks on three streams (H2D,
@@ -588,12 +608,50 @@ def run_cuda(args, names):
             "roofline": roofline, "per_op": per_op, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "per_op_pass_ms_per_step": round(sum(per_op_ms), 4), "clocks": clk}
+    if isolated is not None:
+        line["per_op_isolated"] = isolated
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(names)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS, warmup=5, reps=20):
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    out = {}
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.fill_(0)
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for n in names:
+        wl, b = WORKLOADS[n], bufs[n]
+        t = {op: timed(lambda op=op: b.run(wsf, op)) for op in ("fwd", "bwd")}
+        t["fwd+bwd"] = timed(lambda: (b.run(wsf, "fwd"), b.run(wsf, "bwd")))
+        for op, ms in t.items():
+            nb = (op_bytes(wl, "fwd") + op_bytes(wl, "bwd")) if op == "fwd+bwd" else op_bytes(wl, op)
+            out[f"{n}.{op}"] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
+                                "frac_of_8TBs": round(nb / (ms * 1e-3) / 1e9 / 8000.0, 4),
+                                "elements_per_s": round(op_elems(wl) / (ms * 1e-3), 1)}
+    out["_how"] = (f"L2 flush (write of {2 * l2 >> 20} MiB) before every timed op; "
+                   f"{warmup} warm-ups, median of {reps}; fwd+bwd = both ops back to back after one flush")
+    return out
 
 
 def scaled_workloads(scale: float):
@@ -703,6 +761,8 @@ def main(argv=None):
     ap.add_argument("--compare-atomic", action="store_true",
                     help="measure the atomic-add backward variants against the two-pass ones")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--isolated", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time every op alone after an L2 flush (median of 20)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     names = ORDER_FWD if args.workload == "all" else [s.strip() for s in args.workload.split(",")]

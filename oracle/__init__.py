@@ -25,9 +25,9 @@ DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 
 def build(force: bool = False) -> str:
     """Compile liboracle.so next to its source (gcc, -O2, no fast-math, no
-    contraction of a·b + c into fused multiply-adds)."""
+    contraction of a·b + c into fused multiply-adds, OpenMP)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", _SRC,
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", _SRC,
                "-o", _LIB + ".tmp", "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(_LIB + ".tmp", _LIB)
@@ -53,6 +53,8 @@ def lib():
         L.orc_f64_to_bf16.restype = ctypes.c_uint16
         L.orc_pairwise_sum.argtypes = [_vp, _i64]
         L.orc_pairwise_sum.restype = _dbl
+        L.orc_set_threads.argtypes = [_int]
+        L.orc_set_threads.restype = _int
         L.orc_ws_fwd.argtypes = [_vp, _i64, _vp, _i64, _i64, _int, _vp, _vp, _vp]
         L.orc_ws_fwd.restype = _int
         L.orc_ws_bwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _i64, _vp]
@@ -74,6 +76,17 @@ def lib():
         _lib = L
     return _lib
 
+
+
+def set_threads(n: int) -> int:
+    """Use n host threads (n >= 1; results do not depend on n); returns the
+    previous count."""
+    return int(lib().orc_set_threads(int(n)))
+
+
+def threads() -> int:
+    n = lib().orc_set_threads(0)  # n < 1 leaves the count unchanged
+    return int(n)
 
 def _ptr(t):
     if t is None:

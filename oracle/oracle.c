@@ -28,11 +28,19 @@
  *
  * Storage types: 0 = binary32, 1 = binary16, 2 = bfloat16 (raw 16-bit
  * patterns for the last two).
+ *
+ * Threads.  Built with OpenMP, independent rows (or elements) are computed in
+ * parallel, and the upper levels of the long pairwise sums run as separate
+ * tasks with the same split points; every result is the same bits at any
+ * thread count (orc_set_threads chooses it; tested).
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_F32 0
 #define ORC_F16 1
@@ -158,6 +166,76 @@ double orc_pairwise_sum(const double* t, int64_t n) {
 }
 
 /* ------------------------------------------------------------------ */
+/* Threads.                                                            */
+/* ------------------------------------------------------------------ */
+
+/* Sets the number of threads (n >= 1) and returns the previous number; a
+ * build without OpenMP has one thread and ignores n. */
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+    const int old = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return old;
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+static int n_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int thread_id(void) {
+#ifdef _OPENMP
+    return omp_get_thread_num();
+#else
+    return 0;
+#endif
+}
+
+static void set_flag(int* f) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+    *f = 1;
+}
+
+/* A sub-range shorter than this many terms is summed by one thread. */
+#define TASK_MIN_TERMS ((int64_t)1 << 16)
+
+/* orc_pairwise_sum with the two halves of each range longer than
+ * TASK_MIN_TERMS summed as separate tasks: the same tree. */
+static double pairwise_task(const double* t, int64_t n) {
+    if (n <= TASK_MIN_TERMS) return orc_pairwise_sum(t, n);
+    const int64_t h = n / 2;
+    double left = 0.0, right = 0.0;
+#ifdef _OPENMP
+#pragma omp task shared(left) firstprivate(t, h)
+#endif
+    left = pairwise_task(t, h);
+    right = pairwise_task(t + h, n - h);
+#ifdef _OPENMP
+#pragma omp taskwait
+#endif
+    return left + right;
+}
+
+static double pairwise_par(const double* t, int64_t n) {
+    double s = 0.0;
+#ifdef _OPENMP
+#pragma omp parallel
+#pragma omp single
+#endif
+    s = pairwise_task(t, n);
+    return s;
+}
+
+/* ------------------------------------------------------------------ */
 /* Weighted sum, forward  [WS §1, §2]:  y[i] = Σ_d x[i,d] · w[d].      */
 /* ------------------------------------------------------------------ */
 
@@ -168,10 +246,15 @@ int orc_ws_fwd(const void* x, int64_t ldx, const float* w, int64_t N, int64_t D,
                double* y_exact, double* y_abs, void* y_out) {
     if (!x || !w || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
     make_tables();
-    double* t = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
-    double* ta = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
-    if (!t || !ta) { free(t); free(ta); return -2; }
+    const int64_t Dm = D > 0 ? D : 1;
+    double* tb = (double*)malloc(sizeof(double) * (size_t)Dm * 2 * (size_t)n_threads());
+    if (!tb) return -2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < N; i++) {
+        double* t = tb + (size_t)thread_id() * 2 * Dm;  /* this thread's scratch */
+        double* ta = t + Dm;
         for (int64_t d = 0; d < D; d++) {
             t[d] = decode(x, i * ldx + d, dt) * (double)w[d];
             ta[d] = fabs(t[d]);
@@ -181,8 +264,7 @@ int orc_ws_fwd(const void* x, int64_t ldx, const float* w, int64_t N, int64_t D,
         if (y_abs) y_abs[i] = orc_pairwise_sum(ta, D);
         if (y_out) store(y_out, i, dt, y);
     }
-    free(t);
-    free(ta);
+    free(tb);
     return 0;
 }
 
@@ -228,14 +310,49 @@ static void colsum(const void* x, int64_t ldx, const void* dy, int dt, int64_t a
     }
 }
 
+/* colsum with the upper levels of the recursion (ranges of more than
+ * TASK_MIN_TERMS terms) run as tasks: the same split points and the same
+ * additions, so the same result at any thread count. */
+static void colsum_task(const void* x, int64_t ldx, const void* dy, int dt, int64_t a, int64_t b,
+                        int64_t D, double* out, double* out_abs, int* err) {
+    const int64_t n = b - a;
+    const int64_t Dm = D > 0 ? D : 1;
+    if (n <= 8 || n * Dm <= TASK_MIN_TERMS) {
+        /* recursion depth <= 64; each level needs 2·D doubles */
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)Dm * 2 * 66);
+        if (!scratch) { set_flag(err); return; }
+        colsum(x, ldx, dy, dt, a, b, D, out, out_abs, scratch);
+        free(scratch);
+        return;
+    }
+    const int64_t h = n / 2;
+    double* r = (double*)malloc(sizeof(double) * (size_t)Dm * 2);  /* right half */
+    if (!r) { set_flag(err); return; }
+    double* ra = r + Dm;
+#ifdef _OPENMP
+#pragma omp task firstprivate(x, ldx, dy, dt, a, h, D, out, out_abs, err)
+#endif
+    colsum_task(x, ldx, dy, dt, a, a + h, D, out, out_abs, err);
+    colsum_task(x, ldx, dy, dt, a + h, b, D, out ? r : NULL, out_abs ? ra : NULL, err);
+#ifdef _OPENMP
+#pragma omp taskwait
+#endif
+    for (int64_t d = 0; d < D; d++) {
+        if (out) out[d] += r[d];
+        if (out_abs) out_abs[d] += ra[d];
+    }
+    free(r);
+}
+
 static int colsum_range(const void* x, int64_t ldx, const void* dy, int dt, int64_t a, int64_t b,
                         int64_t D, double* out, double* out_abs) {
-    /* recursion depth <= 64; each level needs 2·D doubles */
-    double* scratch = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1) * 2 * 66);
-    if (!scratch) return -2;
-    colsum(x, ldx, dy, dt, a, b, D, out, out_abs, scratch);
-    free(scratch);
-    return 0;
+    int err = 0;
+#ifdef _OPENMP
+#pragma omp parallel
+#pragma omp single
+#endif
+    colsum_task(x, ldx, dy, dt, a, b, D, out, out_abs, &err);
+    return err ? -2 : 0;
 }
 
 /* Inputs: x [N,D] (row stride ldx), w [D] binary32, dy [N], storage dt.
@@ -248,11 +365,15 @@ int orc_ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, int64
                double* partial) {
     if (!x || !w || !dy || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
     make_tables();
-    if (dx_out)
+    if (dx_out) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
         for (int64_t i = 0; i < N; i++) {
             const double g = decode(dy, i, dt);
             for (int64_t d = 0; d < D; d++) store(dx_out, i * D + d, dt, g * (double)w[d]);
         }
+    }
     if ((grad_w || grad_w_abs) && colsum_range(x, ldx, dy, dt, 0, N, D, grad_w, grad_w_abs))
         return -2;
     if (partial && block_n > 0) {
@@ -278,6 +399,9 @@ static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 int orc_silu_fwd(const void* x, double w, int64_t n, int dt, double* y_exact, void* y_out) {
     if (!x || n < 0 || dt < 0 || dt > 2) return -1;
     make_tables();
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t k = 0; k < n; k++) {
         const double xv = decode(x, k, dt);
         const double y = w * xv * sigmoid(xv);
@@ -302,6 +426,9 @@ int orc_silu_bwd(const void* dy, const void* x, double w, int64_t n, int dt, dou
         ta = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
         if (!t || !ta) { free(t); free(ta); return -2; }
     }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t k = 0; k < n; k++) {
         const double g = decode(dy, k, dt);
         const double xv = decode(x, k, dt);
@@ -317,8 +444,8 @@ int orc_silu_bwd(const void* dy, const void* x, double w, int64_t n, int dt, dou
             ta[k] = fabs(t[k]);
         }
     }
-    if (dw) *dw = orc_pairwise_sum(t, n);
-    if (dw_abs) *dw_abs = orc_pairwise_sum(ta, n);
+    if (dw) *dw = pairwise_par(t, n);
+    if (dw_abs) *dw_abs = pairwise_par(ta, n);
     free(t);
     free(ta);
     return 0;
@@ -337,9 +464,14 @@ int orc_softmax_fwd(const void* x, int64_t ldx, int64_t N, int64_t D, int dt, do
                     void* y_out) {
     if (!x || N < 0 || D < 0 || ldx < D || dt < 0 || dt > 2) return -1;
     make_tables();
-    double* e = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
-    if (!e) return -2;
+    const int64_t Dm = D > 0 ? D : 1;
+    double* eb = (double*)malloc(sizeof(double) * (size_t)Dm * (size_t)n_threads());
+    if (!eb) return -2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < N; i++) {
+        double* e = eb + (size_t)thread_id() * Dm;  /* this thread's scratch */
         double m = -INFINITY;
         for (int64_t j = 0; j < D; j++) {
             const double v = decode(x, i * ldx + j, dt);
@@ -353,7 +485,7 @@ int orc_softmax_fwd(const void* x, int64_t ldx, int64_t N, int64_t D, int dt, do
             if (y_out) store(y_out, i * D + j, dt, y);
         }
     }
-    free(e);
+    free(eb);
     return 0;
 }
 
@@ -364,10 +496,15 @@ int orc_softmax_bwd(const void* y, const void* dy, int64_t N, int64_t D, int dt,
                     double* dx_scale, void* dx_out, double* s_exact) {
     if (!y || !dy || N < 0 || D < 0 || dt < 0 || dt > 2) return -1;
     make_tables();
-    double* t = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
-    double* ta = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
-    if (!t || !ta) { free(t); free(ta); return -2; }
+    const int64_t Dm = D > 0 ? D : 1;
+    double* tb = (double*)malloc(sizeof(double) * (size_t)Dm * 2 * (size_t)n_threads());
+    if (!tb) return -2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < N; i++) {
+        double* t = tb + (size_t)thread_id() * 2 * Dm;  /* this thread's scratch */
+        double* ta = t + Dm;
         for (int64_t j = 0; j < D; j++) {
             t[j] = decode(dy, i * D + j, dt) * decode(y, i * D + j, dt);
             ta[j] = fabs(t[j]);
@@ -383,8 +520,7 @@ int orc_softmax_bwd(const void* y, const void* dy, int64_t N, int64_t D, int dt,
             if (dx_out) store(dx_out, i * D + j, dt, dx);
         }
     }
-    free(t);
-    free(ta);
+    free(tb);
     return 0;
 }
 
@@ -428,9 +564,13 @@ int orc_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, dou
                  double* r_out, double* mu_out) {
     if (!x || !w || (ln && !b) || N < 0 || D <= 0 || ldx < D || dt < 0 || dt > 2) return -1;
     make_tables();
-    double* t = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!t) return -2;
+    double* tb = (double*)malloc(sizeof(double) * (size_t)D * (size_t)n_threads());
+    if (!tb) return -2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < N; i++) {
+        double* t = tb + (size_t)thread_id() * D;  /* this thread's scratch */
         double mu, r;
         norm_stats(x, i * ldx, D, dt, ln, eps, t, &mu, &r);
         if (r_out) r_out[i] = r;
@@ -445,7 +585,7 @@ int orc_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, dou
             if (y_out) store(y_out, i * D + j, dt, y);
         }
     }
-    free(t);
+    free(tb);
     return 0;
 }
 
@@ -485,6 +625,39 @@ static void normcol(const void* x, int64_t ldx, const void* dy, int dt, const do
     }
 }
 
+/* normcol with the upper levels of the recursion run as tasks (as
+ * colsum_task): the same split points and additions. */
+static void normcol_task(const void* x, int64_t ldx, const void* dy, int dt, const double* mu,
+                         const double* r, int64_t a, int64_t b, int64_t D, double* gw, double* gwa,
+                         double* gb, double* gba, int* err) {
+    const int64_t n = b - a;
+    if (n <= 8 || n * D <= TASK_MIN_TERMS) {
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)D * 4 * 68);
+        if (!scratch) { set_flag(err); return; }
+        normcol(x, ldx, dy, dt, mu, r, a, b, D, gw, gwa, gb, gba, scratch);
+        free(scratch);
+        return;
+    }
+    const int64_t h = n / 2;
+    double* rr = (double*)malloc(sizeof(double) * (size_t)D * 4);  /* right half */
+    if (!rr) { set_flag(err); return; }
+#ifdef _OPENMP
+#pragma omp task firstprivate(x, ldx, dy, dt, mu, r, a, h, D, gw, gwa, gb, gba, err)
+#endif
+    normcol_task(x, ldx, dy, dt, mu, r, a, a + h, D, gw, gwa, gb, gba, err);
+    normcol_task(x, ldx, dy, dt, mu, r, a + h, b, D, rr, rr + D, rr + 2 * D, rr + 3 * D, err);
+#ifdef _OPENMP
+#pragma omp taskwait
+#endif
+    for (int64_t j = 0; j < D; j++) {
+        gw[j] += rr[j];
+        gwa[j] += rr[D + j];
+        gb[j] += rr[2 * D + j];
+        gba[j] += rr[3 * D + j];
+    }
+    free(rr);
+}
+
 /* x [N, D] (row stride ldx), w [D], dy [N, D] contiguous, storage dt.
  * Outputs (any may be NULL): dx_exact, dx_scale (|r|·(|g| + mean|g| + |xh|·mean|g·xh|)),
  * dx_out (dt, contiguous), grad_w / grad_w_abs [D], grad_b / grad_b_abs [D] (ln only). */
@@ -493,16 +666,19 @@ int orc_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, dou
                  double* grad_w, double* grad_w_abs, double* grad_b, double* grad_b_abs) {
     if (!x || !w || !dy || N < 0 || D <= 0 || ldx < D || dt < 0 || dt > 2) return -1;
     make_tables();
-    double* t = (double*)malloc(sizeof(double) * (size_t)D);
-    double* t2 = (double*)malloc(sizeof(double) * (size_t)D);
+    double* tb = (double*)malloc(sizeof(double) * (size_t)D * 2 * (size_t)n_threads());
     double* mus = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double* rs = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
-    double* cols = (double*)malloc(sizeof(double) * (size_t)D * 4 * 68);
-    if (!t || !t2 || !mus || !rs || !cols) {
-        free(t); free(t2); free(mus); free(rs); free(cols);
+    if (!tb || !mus || !rs) {
+        free(tb); free(mus); free(rs);
         return -2;
     }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < N; i++) {
+        double* t = tb + (size_t)thread_id() * 2 * D;  /* this thread's scratch */
+        double* t2 = t + D;
         double mu, r;
         norm_stats(x, i * ldx, D, dt, ln, eps, t, &mu, &r);
         mus[i] = mu;
@@ -528,11 +704,18 @@ int orc_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, dou
     }
     if (grad_w || grad_w_abs || grad_b || grad_b_abs) {
         double* gw = (double*)malloc(sizeof(double) * (size_t)D * 4);
-        if (!gw) {
-            free(t); free(t2); free(mus); free(rs); free(cols);
+        int err = 0;
+        if (gw) {
+#ifdef _OPENMP
+#pragma omp parallel
+#pragma omp single
+#endif
+            normcol_task(x, ldx, dy, dt, mus, rs, 0, N, D, gw, gw + D, gw + 2 * D, gw + 3 * D, &err);
+        }
+        if (!gw || err) {
+            free(gw); free(tb); free(mus); free(rs);
             return -2;
         }
-        normcol(x, ldx, dy, dt, mus, rs, 0, N, D, gw, gw + D, gw + 2 * D, gw + 3 * D, cols);
         for (int64_t j = 0; j < D; j++) {
             if (grad_w) grad_w[j] = gw[j];
             if (grad_w_abs) grad_w_abs[j] = gw[D + j];
@@ -541,6 +724,6 @@ int orc_norm_bwd(const void* x, int64_t ldx, const float* w, const void* dy, dou
         }
         free(gw);
     }
-    free(t); free(t2); free(mus); free(rs); free(cols);
+    free(tb); free(mus); free(rs);
     return 0;
 }
