@@ -230,40 +230,41 @@ __global__ void __launch_bounds__(NT)
                     st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
                 }
             }
-            continue;
-        }
-        float f[CPT][V];
-        bool cok[CPT];
+        } else {
+            // binary32 storage: exactly split exponentials, compensated sum
+            float f[CPT][V];
+            bool cok[CPT];
 #pragma unroll
-        for (int c = 0; c < CPT; c++) {
-            cok[c] = rok && l + c * TPR < Dv;
-            E::widen(cur[c * NT + threadIdx.x], f[c]);
-        }
-        float m = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < CPT; c++)
-            if (cok[c])
-#pragma unroll
-                for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
-        m = group_max<TPR>(m, redm);
-        Acc2 s = acc2_zero();
-#pragma unroll
-        for (int c = 0; c < CPT; c++) {
-#pragma unroll
-            for (int v = 0; v < V; v++) {
-                f[c][v] = cok[c] ? exp_diff<kSoftmaxFast<T>>(f[c][v], m) : 0.f;
-                add_to<kComp>(s, f[c][v]);
+            for (int c = 0; c < CPT; c++) {
+                cok[c] = rok && l + c * TPR < Dv;
+                E::widen(cur[c * NT + threadIdx.x], f[c]);
             }
-        }
-        s = group_sum_acc2<TPR>(s, reds);
-        const float inv = 1.0f / (s.hi + s.lo);
+            float m = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < CPT; c++) {
-            if (cok[c]) {
-                float o[V];
+            for (int c = 0; c < CPT; c++)
+                if (cok[c])
 #pragma unroll
-                for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
-                st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                    for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
+            m = group_max<TPR>(m, redm);
+            Acc2 s = acc2_zero();
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    f[c][v] = cok[c] ? exp_diff<kSoftmaxFast<T>>(f[c][v], m) : 0.f;
+                    add_to<kComp>(s, f[c][v]);
+                }
+            }
+            s = group_sum_acc2<TPR>(s, reds);
+            const float inv = 1.0f / (s.hi + s.lo);
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                if (cok[c]) {
+                    float o[V];
+#pragma unroll
+                    for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
+                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                }
             }
         }
     }
