@@ -1,0 +1,104 @@
+"""The library's calls can be captured into a CUDA graph: every entry point
+enqueues its kernels on the caller's stream and allocates nothing, and the
+programmatic-dependent launches become graph edges.  One capture of every
+operator's forward and backward, replayed, gives the same bits as the same
+calls made eagerly, and replays again after the inputs change in place."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def wsf():
+    import __graft_entry__
+    __graft_entry__.build()
+    import backward_ws_fwd_gb300 as m
+    return m
+
+
+def _tensors():
+    g = torch.Generator(device=DEV).manual_seed(0)
+    t = {}
+    t["x"] = torch.randn(4096, 1000, device=DEV, generator=g).bfloat16()
+    t["w"] = torch.randn(1000, device=DEV, generator=g) * 0.03
+    t["dyv"] = torch.randn(4096, device=DEV, generator=g).bfloat16()
+    t["xs"] = (torch.randn(1 << 20, device=DEV, generator=g) * 2).half()
+    t["dys"] = torch.randn(1 << 20, device=DEV, generator=g).half()
+    t["ws"] = torch.tensor([0.75], device=DEV)
+    t["dyn"] = torch.randn(4096, 1000, device=DEV, generator=g).bfloat16()
+    t["wn"] = 1 + 0.1 * torch.randn(1000, device=DEV, generator=g)
+    t["bn"] = 0.1 * torch.randn(1000, device=DEV, generator=g)
+    return t
+
+
+def _outputs(wsf, t):
+    o = {}
+    o["y"] = torch.empty(4096, dtype=torch.bfloat16, device=DEV)
+    o["dx"] = torch.empty_like(t["x"])
+    o["gw"] = torch.empty(1000, device=DEV)
+    o["ws_ws"] = torch.empty(wsf.ws_bwd_workspace_bytes(4096, 1000, torch.bfloat16), dtype=torch.uint8,
+                             device=DEV)
+    o["ys"] = torch.empty_like(t["xs"])
+    o["dxs"] = torch.empty_like(t["xs"])
+    o["dws"] = torch.empty(1, device=DEV)
+    o["silu_ws"] = torch.empty(wsf.silu_bwd_workspace_bytes(1 << 20, torch.float16), dtype=torch.uint8,
+                               device=DEV)
+    o["ym"] = torch.empty_like(t["x"])
+    o["dxm"] = torch.empty_like(t["x"])
+    o["yn"] = torch.empty_like(t["x"])
+    o["dxn"] = torch.empty_like(t["x"])
+    o["gwn"] = torch.empty(1000, device=DEV)
+    o["gbn"] = torch.empty(1000, device=DEV)
+    o["norm_ws"] = torch.empty(wsf.norm_bwd_workspace_bytes(4096, 1000, torch.bfloat16, True),
+                               dtype=torch.uint8, device=DEV)
+    return o
+
+
+def _step(wsf, t, o, s):
+    eps = 2.0 ** -17
+    wsf.ws_fwd(t["x"], t["w"], y=o["y"], stream=s)
+    wsf.ws_bwd(t["x"], t["w"], t["dyv"], dx=o["dx"], grad_w=o["gw"], workspace=o["ws_ws"], stream=s)
+    wsf.silu_fwd(t["xs"], t["ws"], y=o["ys"], stream=s)
+    wsf.silu_bwd(t["dys"], t["xs"], t["ws"], dx=o["dxs"], dw=o["dws"], workspace=o["silu_ws"], stream=s)
+    wsf.softmax_fwd(t["x"], y=o["ym"], stream=s)
+    wsf.softmax_bwd(o["ym"], t["dyn"], dx=o["dxm"], stream=s)
+    wsf.layernorm_fwd(t["x"], t["wn"], t["bn"], eps, y=o["yn"], stream=s)
+    wsf.layernorm_bwd(t["x"], t["wn"], t["dyn"], eps, dx=o["dxn"], grad_w=o["gwn"], grad_b=o["gbn"],
+                      workspace=o["norm_ws"], stream=s)
+
+
+def test_capture_and_replay_match_eager(wsf):
+    t = _tensors()
+    eager = _outputs(wsf, t)
+    s = torch.cuda.Stream(device=DEV)
+    with torch.cuda.stream(s):
+        _step(wsf, t, eager, s)
+    s.synchronize()
+    o = _outputs(wsf, t)
+    for v in o.values():
+        v.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _step(wsf, t, o, s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for k in eager:
+        if k.endswith("_ws"):
+            continue
+        assert torch.equal(o[k], eager[k]), k
+    # new inputs in place: the replay follows them
+    t["x"].mul_(0.5)
+    t["dys"].neg_()
+    with torch.cuda.stream(s):
+        _step(wsf, t, eager, s)
+    s.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in eager:
+        if k.endswith("_ws"):
+            continue
+        assert torch.equal(o[k], eager[k]), k
