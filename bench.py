@@ -498,9 +498,10 @@ def run_cuda(args, names):
     per_op_ms = [sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)) / args.steps
                  for j in range(len(ops))]
 
-    # isolated per-op protocol: an L2 flush (a write of twice the L2 size)
-    # before every timed op, 5 warm-ups, the median of 20; fwd+bwd is the two
-    # ops back to back after one flush
+    # isolated per-op protocol: an L2 flush (a write of twice the L2 size, then
+    # a read of another such buffer, so that the flush's own dirty lines are
+    # written back before the op starts) before every timed op, 5 warm-ups,
+    # the median of 20; fwd+bwd is the two ops back to back after one flush
     isolated = isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS) if args.isolated else None
 
     # end to end through the public API with host buffers: every input is
@@ -635,15 +636,18 @@ def isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS, warmup=5, reps=20)
     import torch
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    clean = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
     out = {}
 
     def timed(fn):
         for _ in range(warmup):
             flush.fill_(0)
+            clean.sum()
             fn()
         ts = []
         for _ in range(reps):
             flush.fill_(1)
+            clean.sum()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -662,7 +666,8 @@ def isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS, warmup=5, reps=20)
             out[f"{n}.{op}"] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
                                 "frac_of_8TBs": round(nb / (ms * 1e-3) / 1e9 / 8000.0, 4),
                                 "elements_per_s": round(op_elems(wl) / (ms * 1e-3), 1)}
-    out["_how"] = (f"L2 flush (write of {2 * l2 >> 20} MiB) before every timed op; "
+    out["_how"] = (f"L2 flush before every timed op: a write of {2 * l2 >> 20} MiB, then a read of "
+                   f"another {2 * l2 >> 20} MiB (no dirty lines left for the op to write back); "
                    f"{warmup} warm-ups, median of {reps}; fwd+bwd = both ops back to back after one flush")
     return out
 
