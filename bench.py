@@ -609,8 +609,7 @@ def run_cuda(args, names):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded SplitMix64/Box-Muller, BASELINE workload recipes)"
-                    .replace("BASELINE ", ""),
+            "data": "synthetic (seeded SplitMix64/Box-Muller, workload recipes)",
             "config": {"workload": workload_label(names) + (f" (rows x {args.scale})"
                                                              if args.scale != 1.0 else ""),
                        "step": [f"{n}.{op}" for n, op in ops],
