@@ -16,6 +16,7 @@
 // multi-pass path with one CTA per row.  Sums of binary32 rows are
 // compensated and their exponents taken of exactly split differences.
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "wsf_device.cuh"
@@ -38,7 +39,8 @@ __device__ __forceinline__ float exp_diff(float a, float b) {
         float d, e;
         two_sum(a, -b, d, e);
         const float r = expf(d);
-        return fmaf(r, e, r);
+        // a = −inf (a masked logit) makes e NaN; exp(−inf) = 0 stands as is
+        return r > 0.f ? fmaf(r, e, r) : r;
     }
 }
 
@@ -404,6 +406,277 @@ __global__ void __launch_bounds__(NT)
 }
 
 // ---------------------------------------------------------------------------
+// Cluster path (16-byte aligned rows wider than the row path holds): one
+// thread-block cluster of CS CTAs takes one row per iteration (grid-stride
+// over rows by cluster).  The CTA of rank r owns the row's chunks
+// [r·NT·CPT, (r+1)·NT·CPT), CPT = 4 chunks a thread, staged S rows ahead into
+// the thread's private shared-memory slots with cp.async, so each CTA reads
+// its slice of x (y, dy) once and writes y (dx) once.
+//
+// One exchange a row.  Each warp reduces its own part of the slice (xor
+// butterfly) and lane 0 publishes the warp's entry in shared memory; after a
+// cluster barrier every warp of every CTA reads all CS·NT/32 entries through
+// distributed shared memory, lane ℓ taking entries ℓ, ℓ+32, …, combines them
+// in that order and then across lanes (xor butterfly).  Every warp therefore
+// derives the same bits of the row statistic, with no barrier inside the
+// CTA.  The forward publishes (m_w, s_w): the warp's maximum and its sum of
+// exp(x − m_w); the row sum is Σ_w s_w·exp(m_w − M), M = max_w m_w, and
+// y = exp(x − m_w)·(exp(m_w − M)/sum) (the combination of partial softmax
+// sums by rescaling, as in online softmax).  The backward publishes the
+// warp's part of Σ dy·y.
+//
+// Every CTA of a cluster runs the same number of rows (it depends only on the
+// cluster's index), hence the same number of cluster barriers.  Entries
+// alternate between two buffers by row parity: the buffer of row k is written
+// again for row k + 2, after the barrier of row k + 1, which every reader
+// reaches only after its reads of row k; a last barrier keeps each CTA's
+// shared memory alive until the other CTAs have read it.
+constexpr int kClusterCPT = 4;
+constexpr int kClusterMaxCS = 16;
+
+__device__ __forceinline__ float4 cluster_ld_f32x4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
+    return v;
+}
+
+// exp(a − b) for the combination of partial sums: the binary32 form of the
+// elements (exactly split difference) or the base-2 form of 16-bit rows.
+template <bool Comp>
+__device__ __forceinline__ float rescale(float a, float b) {
+    if constexpr (Comp) return exp_diff<false>(a, b);
+    else return exp2_approx(fmaf(a, kLog2e, -b * kLog2e));
+}
+
+template <typename T, int NT, int S>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+    softmax_fwd_cluster(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
+                        int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
+    constexpr int EPL = (kClusterMaxCS * W + 31) / 32;  // entries a lane reads, at most
+    constexpr bool kComp = std::is_same<T, float>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* slots = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    __shared__ __align__(16) float4 pub[2][W];
+    const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;  // chunk l + c·NT
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int total = (int)cluster_nctarank() * W;
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    const int64_t iters = cid < N ? (N - 1 - cid) / ncl + 1 : 0;
+    pdl_wait();
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) stage_row<T, NT, CPT, NT>(slots + k * CPT * NT, x, ldx, cid + k * ncl, N, Dv, l);
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters)
+            stage_row<T, NT, CPT, NT>(slots + (nk % S) * CPT * NT, x, ldx, cid + nk * ncl, N, Dv, l);
+        cp_async_commit();
+        const int64_t row = cid + k * ncl;
+        const Raw16* cur = slots + (k % S) * CPT * NT;
+        // the warp's maximum and its sum of exp(x − m_w)
+        float f[CPT][V];
+        float m = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * NT < Dv) {
+                if constexpr (!kComp) {
+                    m = fmaxf(m, chunk_max16<T>(cur[c * NT + threadIdx.x]));
+                } else {
+                    E::widen(cur[c * NT + threadIdx.x], f[c]);
+#pragma unroll
+                    for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
+                }
+            }
+        }
+        m = warp_max(m);
+        // a warp whose elements are all −inf (masked) shifts by 0: its
+        // exponentials and its sum are then 0, and its entry is skipped
+        if (m == -INFINITY) m = 0.f;
+        Acc2 s = acc2_zero();
+        if constexpr (!kComp) {
+            const float ms = m * kLog2e;
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                E::widen(cur[c * NT + threadIdx.x], f[c]);
+                const bool ok = l + c * NT < Dv;
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    f[c][v] = ok ? exp2_approx(fmaf(f[c][v], kLog2e, -ms)) : 0.f;
+                    s.hi += f[c][v];
+                }
+            }
+            s.hi = group_sum<32>(s.hi);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                const bool ok = l + c * NT < Dv;
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    f[c][v] = ok ? exp_diff<false>(f[c][v], m) : 0.f;
+                    add_to<true>(s, f[c][v]);
+                }
+            }
+            s = group_sum2<32>(s);
+        }
+        float4* buf = pub[k & 1];
+        if (lane == 0) buf[wid] = make_float4(m, s.hi, s.lo, 0.f);
+        cluster_sync();
+        // every (rank, warp) entry: j = rank·W + warp
+        float4 ent[EPL];
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; i++) {
+            const int j = lane + 32 * i;
+            if (j < total) {
+                ent[i] = cluster_ld_f32x4(cluster_map(&buf[j % W], (unsigned)(j / W)));
+                M = fmaxf(M, ent[i].x);
+            }
+        }
+        M = warp_max(M);
+        Acc2 t = acc2_zero();
+#pragma unroll
+        for (int i = 0; i < EPL; i++) {
+            const int j = lane + 32 * i;
+            if (j < total && ent[i].y > 0.f) {  // skip warps without a finite element
+                const float g = rescale<kComp>(ent[i].x, M);
+                if constexpr (kComp)
+                    acc2_fma(t, __fadd_rn(ent[i].y, ent[i].z), g);
+                else
+                    t.hi = fmaf(ent[i].y, g, t.hi);
+            }
+        }
+        float inv;
+        if constexpr (kComp) {
+            t = group_sum2<32>(t);
+            inv = 1.0f / (t.hi + t.lo);
+        } else {
+            inv = 1.0f / group_sum<32>(t.hi);
+        }
+        const float sc = rescale<kComp>(m, M) * inv;
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * NT < Dv) {
+                float o[V];
+#pragma unroll
+                for (int v = 0; v < V; v++) o[v] = f[c][v] * sc;
+                st_stream(y + row * ldy + (int64_t)(l + c * NT) * V, E::narrow(o));
+            }
+        }
+    }
+    cp_async_wait<0>();
+    cluster_sync();
+    pdl_trigger();
+}
+
+template <typename T, int NT, int S>
+__global__ void __launch_bounds__(NT)
+    softmax_bwd_cluster(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy,
+                        int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
+    constexpr int EPL = (kClusterMaxCS * W + 31) / 32;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* ys = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    Raw16* gs = ys + S * CPT * NT;                    // [S][CPT][NT]
+    __shared__ __align__(8) float2 pub[2][W];
+    const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int total = (int)cluster_nctarank() * W;
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    const int64_t iters = cid < N ? (N - 1 - cid) / ncl + 1 : 0;
+    pdl_wait();
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) {
+            stage_row<T, NT, CPT, NT>(ys + k * CPT * NT, y, ldy, cid + k * ncl, N, Dv, l);
+            stage_row<T, NT, CPT, NT>(gs + k * CPT * NT, dy, lddy, cid + k * ncl, N, Dv, l);
+        }
+        cp_async_commit();
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        cp_async_wait<S - 2>();
+        const int64_t nk = k + S - 1;
+        if (nk < iters) {
+            stage_row<T, NT, CPT, NT>(ys + (nk % S) * CPT * NT, y, ldy, cid + nk * ncl, N, Dv, l);
+            stage_row<T, NT, CPT, NT>(gs + (nk % S) * CPT * NT, dy, lddy, cid + nk * ncl, N, Dv, l);
+        }
+        cp_async_commit();
+        const int64_t row = cid + k * ncl;
+        const Raw16* cy = ys + (k % S) * CPT * NT;
+        const Raw16* cg = gs + (k % S) * CPT * NT;
+        Acc2 s = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * NT < Dv) {
+                float fy[V], fg[V];
+                E::widen(cy[c * NT + threadIdx.x], fy);
+                E::widen(cg[c * NT + threadIdx.x], fg);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    if constexpr (kComp)
+                        acc2_fma(s, fg[v], fy[v]);
+                    else
+                        s.hi = fmaf(fg[v], fy[v], s.hi);
+                }
+            }
+        }
+        if constexpr (kComp)
+            s = group_sum2<32>(s);
+        else
+            s.hi = group_sum<32>(s.hi);
+        float2* buf = pub[k & 1];
+        if (lane == 0) buf[wid] = make_float2(s.hi, s.lo);
+        cluster_sync();
+        Acc2 t = acc2_zero();
+#pragma unroll
+        for (int i = 0; i < EPL; i++) {
+            const int j = lane + 32 * i;
+            if (j < total) {
+                const float2 o = cluster_ld_f32x2(cluster_map(&buf[j % W], (unsigned)(j / W)));
+                if constexpr (kComp)
+                    t = acc2_add(t, Acc2{o.x, o.y});
+                else
+                    t.hi += o.x;
+            }
+        }
+        float sv;
+        if constexpr (kComp) {
+            t = group_sum2<32>(t);
+            sv = t.hi + t.lo;
+        } else {
+            sv = group_sum<32>(t.hi);
+        }
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (l + c * NT < Dv) {
+                float fy[V], fg[V], o[V];
+                E::widen(cy[c * NT + threadIdx.x], fy);
+                E::widen(cg[c * NT + threadIdx.x], fg);
+#pragma unroll
+                for (int v = 0; v < V; v++) o[v] = fy[v] * (fg[v] - sv);
+                st_stream(dx + row * lddx + (int64_t)(l + c * NT) * V, E::narrow(o));
+            }
+        }
+    }
+    cp_async_wait<0>();
+    cluster_sync();
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
 static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline int next_pow2(int64_t v) {
@@ -458,6 +731,77 @@ static cudaError_t dispatch_rows(int64_t Dv, int64_t N, F&& go) {
     return with_rows<256, 8, 2>(N, go);
 }
 
+// Cluster shapes: a CTA of NT threads holds NT·4 chunks of a row; rows of up
+// to 8 CTAs of 256 threads (8192 chunks, 128 KB) take clusters of 256-thread
+// CTAs, wider rows 512-thread CTAs, up to 16 a cluster (32768 chunks, 512 KB).
+constexpr int kMaxDevices = 64;
+constexpr int64_t kClusterRowChunks = (int64_t)kClusterMaxCS * 512 * kClusterCPT;
+
+static void cluster_shape(int64_t Dv, int& nt, unsigned& cs) {
+    nt = Dv <= 8 * 256 * kClusterCPT ? 256 : 512;
+    cs = (unsigned)cdiv(Dv, (int64_t)nt * kClusterCPT);
+}
+
+// Launch `kernel` as clusters of cs CTAs, as many clusters as the device
+// holds at once (at most one a row); returns cudaErrorNotSupported when no
+// cluster of that shape fits, so that the caller falls back.
+template <auto kernel, typename... Args>
+static cudaError_t go_cluster(int nt, unsigned cs, size_t smem, int64_t N, cudaStream_t s,
+                              Args&&... args) {
+    cudaError_t e = cudaFuncSetAttribute((const void*)kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && cs > 8)
+        e = cudaFuncSetAttribute((const void*)kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    // resident clusters of this kernel and size, per device, queried once
+    static std::atomic<int> fits[kMaxDevices][kClusterMaxCS + 1];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int fit = dev < kMaxDevices ? fits[dev][cs].load(std::memory_order_relaxed) : 0;
+    if (fit == 0) {
+        fit = max_active_clusters(kernel, cs, dim3(nt), smem);
+        if (fit <= 0) fit = -1;
+        if (dev < kMaxDevices) fits[dev][cs].store(fit, std::memory_order_relaxed);
+    }
+    if (fit < 0) return cudaErrorNotSupported;
+    const unsigned clusters = (unsigned)std::min<int64_t>(N, fit);
+    return launch_cluster(kernel, clusters, cs, dim3(nt), smem, s, std::forward<Args>(args)...);
+}
+
+template <typename T>
+static cudaError_t softmax_fwd_cluster_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
+                                         int64_t Dv, cudaStream_t s) {
+    int nt;
+    unsigned cs;
+    cluster_shape(Dv, nt, cs);
+    if (nt == 256) {
+        constexpr int S = 3;
+        return go_cluster<softmax_fwd_cluster<T, 256, S>>(256, cs,
+                          (size_t)S * kClusterCPT * 256 * 16, N, s, x, ldx, y, ldy, N, (int)Dv);
+    }
+    constexpr int S = 2;
+    return go_cluster<softmax_fwd_cluster<T, 512, S>>(512, cs, (size_t)S * kClusterCPT * 512 * 16,
+                      N, s, x, ldx, y, ldy, N, (int)Dv);
+}
+
+template <typename T>
+static cudaError_t softmax_bwd_cluster_t(const T* y, int64_t ldy, const T* dy, int64_t lddy, T* dx,
+                                         int64_t lddx, int64_t N, int64_t Dv, cudaStream_t s) {
+    int nt;
+    unsigned cs;
+    cluster_shape(Dv, nt, cs);
+    constexpr int S = 2;
+    if (nt == 256)
+        return go_cluster<softmax_bwd_cluster<T, 256, S>>(256, cs,
+                          (size_t)2 * S * kClusterCPT * 256 * 16, N, s, y, ldy, dy, lddy, dx, lddx,
+                          N, (int)Dv);
+    return go_cluster<softmax_bwd_cluster<T, 512, S>>(512, cs,
+                      (size_t)2 * S * kClusterCPT * 512 * 16, N, s, y, ldy, dy, lddy, dx, lddx, N,
+                      (int)Dv);
+}
+
 template <typename T>
 static cudaError_t softmax_fwd_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N, int64_t D,
                                  cudaStream_t s) {
@@ -474,6 +818,11 @@ static cudaError_t softmax_fwd_t(const T* x, int64_t ldx, T* y, int64_t ldy, int
             if (e != cudaSuccess) return e;
             return launch(k, grid, block, smem, s, true, x, ldx, y, ldy, N, (int)Dv);
         });
+    }
+    if (D % V == 0 && ldx % V == 0 && ldy % V == 0 && aligned16(x) && aligned16(y) &&
+        Dv <= kClusterRowChunks && N > 0) {
+        const cudaError_t e = softmax_fwd_cluster_t(x, ldx, y, ldy, N, Dv, s);
+        if (e != cudaErrorNotSupported) return e;
     }
     constexpr int NT = 256;
     return launch(softmax_fwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
@@ -496,6 +845,11 @@ static cudaError_t softmax_bwd_t(const T* y, int64_t ldy, const T* dy, int64_t l
             if (e != cudaSuccess) return e;
             return launch(k, grid, block, smem, s, true, y, ldy, dy, lddy, dx, lddx, N, (int)Dv);
         });
+    }
+    if (D % V == 0 && ldy % V == 0 && lddy % V == 0 && lddx % V == 0 && aligned16(y) &&
+        aligned16(dy) && aligned16(dx) && Dv <= kClusterRowChunks && N > 0) {
+        const cudaError_t e = softmax_bwd_cluster_t(y, ldy, dy, lddy, dx, lddx, N, Dv, s);
+        if (e != cudaErrorNotSupported) return e;
     }
     constexpr int NT = 256;
     return launch(softmax_bwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),

@@ -233,4 +233,57 @@ __device__ __forceinline__ float select(const float (&a)[K], int i) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Thread-block clusters (sm_90 and later).  A cluster's CTAs are scheduled
+// together and can read one another's shared memory ("distributed shared
+// memory"): mapa turns a local shared-memory address into the address of the
+// same variable in the CTA of a given rank, and ld.shared::cluster reads it.
+// cluster_sync() is the hardware cluster barrier (every thread of every CTA
+// of the cluster arrives; .release/.acquire make shared-memory writes made
+// before the arrival visible to reads made after the wait).  It is not a
+// spin loop: like __syncthreads() it completes once every thread has
+// arrived, so each CTA of a cluster must execute the same number of them.
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_nctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_id_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_count_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// Address of the shared variable at local address `p` in the CTA of rank `r`.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, unsigned r) {
+    uint32_t out;
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(r));
+    return out;
+}
+__device__ __forceinline__ float cluster_ld_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 cluster_ld_f32x2(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a)
+                 : "memory");
+    return v;
+}
+
 }  // namespace wsf

@@ -1,7 +1,8 @@
 """GPU parity of the softmax forward and backward against the fp64 oracle:
-register rows of every width class, the two-pass wide/unaligned path, row
-strides, guard bands, bit reproducibility, and sampled rows at the
-measurement size."""
+register rows of every width class, cluster rows (clusters of 3 to 16 CTAs,
+both CTA widths, ragged last slices, more rows than resident clusters), the
+element-wise wide/unaligned path, masked (−inf) logits, row strides, guard
+bands, bit reproducibility, and sampled rows at the measurement size."""
 import numpy as np
 import pytest
 import torch
@@ -97,6 +98,70 @@ def test_softmax_large_logits_and_reproducible(wsf):
     outs = [(wsf.softmax_fwd(xd), wsf.softmax_bwd(yd, gd)) for _ in range(3)]
     for a, b in outs[1:]:
         assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1])
+
+
+# Cluster rows: 16-byte chunks (8 16-bit or 4 fp32 elements) split over CTAs
+# of 1024 (256 threads) or 2048 (512 threads) chunks.
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D", [
+    (700, 16392),   # 16-bit: 2049 chunks, 3 CTAs, the last holding one chunk; more rows than clusters
+    (50, 65536),    # 16-bit: 8 CTAs of 256; fp32: 8 CTAs of 512
+    (20, 131072),   # 16-bit: 8 CTAs of 512; fp32: 16 CTAs of 512
+    (9, 262144),    # 16-bit: 16 CTAs of 512; fp32: beyond the cluster rows (element-wise path)
+    (31, 100008),   # ragged last slice
+    (13, 50264),
+    (3, 50257),     # width not a whole number of chunks (element-wise path)
+])
+def test_softmax_cluster_rows(wsf, dt, N, D):
+    x, dy = _inputs(N, D, dt, seed=N)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_softmax_cluster_extremes_and_reproducible(wsf, dt):
+    # the row maximum in the last CTA's slice, large spreads, a row of equal
+    # values, and bit-identical repeats
+    N, D = 6, 70000
+    x, dy = _inputs(N, D, dt, seed=7)
+    x[0, -1] = 60.0
+    x[1, 5] = 60.0
+    x[2, ::3] = -60.0
+    x[3] = 1.5
+    x[4, 40000:] = -1e4 if dt != "f16" else -6e4
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+    xd, yd, gd = x.to(DEV), yin.to(DEV), dy.to(DEV)
+    outs = [(wsf.softmax_fwd(xd), wsf.softmax_bwd(yd, gd)) for _ in range(3)]
+    for a, b in outs[1:]:
+        assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1])
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D", [(6, 1000), (6, 40000), (4, 50257), (3, 262144)])
+def test_softmax_masked_logits(wsf, dt, N, D):
+    # −inf logits (an attention mask): row i keeps columns [0, t_i) and masks
+    # the rest, from most of the row down to a single column; the masked
+    # spans cover whole warps and whole CTAs of the cluster rows
+    x, dy = _inputs(N, D, dt, seed=21)
+    keep = [D, D // 2, D // 7, 33, 1, D - 1][:N]
+    for i, t in enumerate(keep):
+        x[i, t:] = float("-inf")
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+    for i, t in enumerate(keep):
+        assert bool((y[i, t:] == 0).all()) and bool((dx[i, t:] == 0).all())
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_softmax_cluster_strides(wsf, dt):
+    x, dy = _inputs(40, 40000, dt, seed=2)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin, pad=8)
+    _check(x, dy, y, dx, yin)
 
 
 @pytest.mark.slow

@@ -42,6 +42,26 @@ def test_shift_invariance_and_uniform():
     assert yb[0, 0] == 1.0 and yb[0, 2] == 0.0
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_masked_logits_equal_softmax_of_kept_columns(dt):
+    # −inf entries (a mask) get probability exactly 0, and the kept columns
+    # get the softmax of the kept sub-row; the backward is 0 where y is 0
+    x = _x(4, 300, dt, seed=5)
+    keep = [300, 150, 1, 77]
+    xm = x.clone()
+    for i, t in enumerate(keep):
+        xm[i, t:] = float("-inf")
+    ye, _ = oracle.softmax_fwd(xm)
+    for i, t in enumerate(keep):
+        ref = scipy.special.softmax(x[i, :t].double().numpy())
+        assert np.allclose(ye[i, :t], ref, rtol=1e-13, atol=0)
+        assert np.all(ye[i, t:] == 0.0)
+    dy = _x(4, 300, dt, seed=6)
+    r = oracle.softmax_bwd(torch.from_numpy(ye).to(x.dtype), dy)
+    for i, t in enumerate(keep):
+        assert np.all(r["dx_exact"][i, t:] == 0.0)
+
+
 @pytest.mark.parametrize("D", [1, 2, 5])
 def test_backward_equals_dense_jacobian(D):
     """Materialise J = diag(y) − y·yᵀ (only for the test) and compare Jᵀ·dy."""
