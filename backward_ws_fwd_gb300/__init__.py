@@ -32,6 +32,8 @@ lib.wsf_status_string.argtypes = [_int]
 lib.wsf_status_string.restype = ctypes.c_char_p
 lib.wsf_version.argtypes = []
 lib.wsf_version.restype = _int
+lib.wsf_cluster_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint), _int]
+lib.wsf_cluster_wait_timeouts.restype = _int
 lib.ws_fwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _int, _vp]
 lib.ws_fwd.restype = _int
 lib.ws_bwd_workspace_bytes.argtypes = [_i64, _i64, _int, _i64]
@@ -337,7 +339,16 @@ def layernorm_bwd(x, w, dy, eps=1e-5, dx=None, grad_w=None, grad_b=None, accumul
     return dx, grad_w, grad_b
 
 
-__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
+def cluster_wait_timeouts(reset: bool = False) -> int:
+    """Waits of the cluster paths' partial-sum exchanges that ran out on the
+    current device (zero in correct operation); synchronises the device."""
+    n = ctypes.c_uint(0)
+    _check(lib.wsf_cluster_wait_timeouts(ctypes.byref(n), int(bool(reset))),
+           "wsf_cluster_wait_timeouts")
+    return int(n.value)
+
+
+__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "cluster_wait_timeouts", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
            "ws_bwd_atomic", "silu_bwd_atomic", "softmax_fwd", "softmax_bwd", "silu_fwd",
            "silu_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "layernorm_fwd", "layernorm_bwd",
            "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "norm_bwd_workspace_bytes", "F32",

@@ -80,6 +80,12 @@ const char* wsf_status_string(int status) {
 
 int wsf_version(void) { return 100; }
 
+int wsf_cluster_wait_timeouts(unsigned* count, int reset) {
+    if (!count) return WSF_ERR_NULL_PTR;
+    if (reset != 0 && reset != 1) return WSF_ERR_BAD_ARG;
+    return cuda_status(wsf::norm_wait_timeouts(count, reset != 0));
+}
+
 int ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N, int64_t D, int dtype,
            wsf_stream_t stream) {
     if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;

@@ -543,6 +543,445 @@ __global__ void __launch_bounds__(NT, MINB)
 }
 
 // ===========================================================================
+// Cluster path (16-byte aligned rows of 8193..65536 elements).  A row is
+// split over a thread-block cluster of CS CTAs of NT = 256 threads: the CTA
+// of rank r owns the chunks [r·NT·CPT, (r+1)·NT·CPT) (16 elements a thread,
+// 4096 a CTA) and stages them S rows ahead into the threads' private slots.
+// The forward holds its slice of w (and b) in registers; the backward reads
+// it through the read-only cache, re-widens x and dy from their slots in each
+// pass, and holds only the dw/db accumulators of exactly those columns.  The row sums are reduced inside each warp (xor butterfly)
+// and exchanged as one entry a warp with WarpPush: every CTA receives the
+// entries of all CS·NT/32 warps of the cluster in its own shared memory, and
+// each warp combines them (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
+// butterfly over the lanes), so every thread derives the same bits of the
+// row statistics, with the arithmetic of the row path.
+//
+// One exchange a row.  LayerNorm needs Σx before the sums over d = x − μ;
+// its Σx travels one row ahead: the exchange of row k carries the sums of
+// row k and Σx of row k + 1 (staged already), so that the mean of row k + 1
+// is known when its turn comes, and only the first row's Σx is exchanged on
+// its own.  Σx is compensated across threads for every storage type: the
+// plain binary32 row sum that suffices for 16-bit rows of the row path is
+// exact only while Σx stays below 2^24 steps of the data's grid, i.e. up to
+// 2^24/2^11 = 8192 binary16 elements of one binade (2^24/2^8 = 65536 for
+// bfloat16), and wider binary16 rows with a large common offset would shift
+// every x̂ of a row by the rounding of their mean (see staged_sum_x).
+//
+// The forward takes rows cid, cid + ncl, … (cluster cid of ncl).  The
+// backward keeps the row tiles of the row path (a function of N alone, so
+// dw/db have the same bits on any device): cluster cid takes tiles cid,
+// cid + ncl, … one after the other, staging across tile boundaries, and at
+// the end of a tile each CTA writes its columns of the tile's partial row.
+// Every CTA of a cluster runs the same rows, hence the same exchanges.
+// ===========================================================================
+constexpr int kNormClusterNT = 256;
+// backward stages (indexed by LayerNorm) and whether w sits in per-thread
+// shared-memory slots, for 16-bit and binary32 rows
+constexpr int kNormBwdStages16[2] = {3, 3};
+constexpr int kNormBwdStages32[2] = {2, 3};
+constexpr bool kNormBwdWSlots[2] = {true, true};
+constexpr int kNormFwdStages[2] = {3, 4};
+constexpr int64_t kNormClusterRowMax = (int64_t)kClusterMaxCS * kNormClusterNT * 16;  // 65536
+
+// Waits of the cluster exchanges that ran out (see WarpPush); zero unless
+// the exchange protocol failed.
+__device__ unsigned g_norm_wait_timeouts;
+
+template <int NT>
+using NormPush = WarpPush<NT / 32, kClusterMaxCS*(NT / 32), 2>;
+
+__device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
+    return comp ? group_sum2<32>(v) : Acc2{group_sum<32>(v.hi), 0.f};
+}
+
+// Sum K (up to 4) row sums over the cluster; sum q is compensated if bit q
+// of CM is set.  Every thread of every CTA of the cluster calls it together.
+template <int NT, int K, unsigned CM>
+__device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp) {
+    static_assert(K >= 1 && K <= 4, "up to four sums");
+    constexpr int W = NT / 32, EPL = (kClusterMaxCS * W + 31) / 32, NX = (K + 1) / 2;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CM >> q) & 1u);
+    float4 e[NX];
+#pragma unroll
+    for (int n = 0; n < NX; n++) {
+        const Acc2 a = v[2 * n], b = 2 * n + 1 < K ? v[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
+        e[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
+    }
+    const float4(*buf)[2] = xp.template exchange<NX>(e);
+    const int total = (int)cluster_nctarank() * W;
+    Acc2 t[K];
+#pragma unroll
+    for (int q = 0; q < K; q++) t[q] = acc2_zero();
+#pragma unroll
+    for (int i = 0; i < EPL; i++) {
+        const int j = lane + 32 * i;
+        if (j < total) {
+#pragma unroll
+            for (int n = 0; n < NX; n++) {
+                const float4 en = buf[j][n];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int q = 2 * n + h;
+                    if (q < K) {
+                        const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
+                        t[q] = ((CM >> q) & 1u) ? acc2_add(t[q], o) : Acc2{t[q].hi + o.hi, 0.f};
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < K; q++) v[q] = warp_sum(t[q], (CM >> q) & 1u);
+}
+
+// Σx over this thread's valid chunks of a staged row, exact up to the
+// rounding that the cross-thread levels then compensate: binary32 elements
+// with TwoSum each; 16-bit elements (8 or 11 significant bits) in plain
+// binary32, which is exact unless the thread's 16 elements span more than 12
+// (bfloat16) or 9 (binary16) binades, and then errs by at most 2^-24 of the
+// thread's partial sum — a shift of the mean by 2^-24·max|x|/D at most.
+template <typename E, int CPT, int NT, int V, bool Comp>
+__device__ __forceinline__ Acc2 staged_sum_x(const Raw16* slot, unsigned valid) {
+    Acc2 s = acc2_zero();
+    float s1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPT; c++) {
+        if (valid >> c & 1u) {
+            float f[V];
+            E::widen(slot[c * NT], f);
+#pragma unroll
+            for (int v = 0; v < V; v++) {
+                if constexpr (Comp)
+                    s_add<true>(s, f[v]);
+                else if (v & 1)
+                    s1 += f[v];
+                else
+                    s.hi += f[v];
+            }
+        }
+    }
+    if constexpr (!Comp) s.hi += s1;
+    return s;
+}
+
+template <int CPT, int V>
+__device__ __forceinline__ void center(float (&f)[CPT][V], unsigned valid, const Mean& m) {
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+        if (valid >> c & 1u)
+#pragma unroll
+            for (int v = 0; v < V; v++) f[c][v] = (f[c][v] - m.mu0) - m.c;
+}
+
+template <typename T, bool LN, int NT, int S>
+__global__ void __launch_bounds__(NT, 3)
+    norm_fwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                     const float* __restrict__ b, float eps, T* __restrict__ y, int64_t ldy,
+                     int64_t N, int Dv) {
+    using E = Elt<T>;
+    constexpr int V = E::V, CPT = 16 / V;
+    constexpr bool C = std::is_same<T, float>::value;
+    static_assert(S >= (LN ? 3 : 2), "LayerNorm holds two staged rows");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
+    __shared__ __align__(8) uint64_t xbar[2];
+    NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
+    xc.init();
+    cluster_sync();
+    const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;  // chunk l + c·NT
+    const float fd = (float)(Dv * V), inv_d = 1.0f / fd;
+    const unsigned valid = chunk_mask<NT, CPT>(Dv, l);
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    const int64_t iters = cid < N ? (N - 1 - cid) / ncl + 1 : 0;
+    pdl_wait();
+    float wv[CPT][V], bv[CPT][V];
+    load_params<NT, CPT, V>(w, Dv, l, wv);
+    if constexpr (LN) load_params<NT, CPT, V>(b, Dv, l, bv);
+    const int64_t ldb = ldx * (int64_t)sizeof(T);
+    RowStager stg{reinterpret_cast<const char*>(x) + cid * ldb + (int64_t)l * 16,
+                  reinterpret_cast<const char*>(x), ncl * ldb, cid, ncl, N};
+    T* yrow = y + cid * ldy + (int64_t)l * V;
+    const int64_t ystep = ncl * ldy;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        if (k < iters) stage_row<NT, CPT, NT>(xs + k * CPT * NT, stg, valid);
+        cp_async_commit();
+    }
+    Mean mn{0.f, 0.f};
+    if (LN && iters > 0) {  // the first row's Σx
+        cp_async_wait<S - 2>();
+        Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
+        cluster_reduce<NT, 1, 1u>(s0, xc);
+        mn = mean_of(s0[0], fd, inv_d);
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        if constexpr (LN)
+            cp_async_wait<(LN ? S - 3 : 0)>();  // rows k and k + 1
+        else
+            cp_async_wait<S - 2>();
+        if (k + S - 1 < iters) stage_row<NT, CPT, NT>(xs + ((k + S - 1) % S) * CPT * NT, stg, valid);
+        cp_async_commit();
+        float f[CPT][V];
+        load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
+        if constexpr (LN) center<CPT, V>(f, valid, mn);
+        // Σ d², d = x (RMSNorm) or x − μ (LayerNorm); LayerNorm: Σx of row k + 1
+        Acc2 sm[LN ? 2 : 1];
+        sm[0] = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+            if (valid >> c & 1u)
+#pragma unroll
+                for (int v = 0; v < V; v++) s_fma<C>(sm[0], f[c][v], f[c][v]);
+        if constexpr (LN) {
+            sm[LN ? 1 : 0] = k + 1 < iters
+                ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
+                : acc2_zero();
+            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u>(sm, xc);
+        } else {
+            cluster_reduce<NT, 1, C ? 1u : 0u>(sm, xc);
+        }
+        const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
+        if constexpr (LN) mn = mean_of(sm[LN ? 1 : 0], fd, inv_d);
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (valid >> c & 1u) {
+                float o[V];
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float xh = f[c][v] * r;
+                    o[v] = LN ? fmaf(xh, wv[c][v], bv[c][v]) : xh * wv[c][v];
+                }
+                st_stream(yrow + (int64_t)c * NT * V, E::narrow(o));
+            }
+        }
+        yrow += ystep;
+    }
+    cp_async_wait<0>();
+    cluster_sync();
+    pdl_trigger();
+}
+
+// A cursor over the rows of tiles t, t + step, … (of P tiles over N rows).
+struct TileCursor {
+    int tile;
+    int64_t row, end;
+};
+
+__device__ __forceinline__ void tile_seek(TileCursor& c, int P, int64_t N) {
+    if (c.tile < P)
+        norm_tile_rows(c.tile, P, N, c.row, c.end);
+    else
+        c.row = c.end = 0;
+}
+
+__device__ __forceinline__ void tile_advance(TileCursor& c, int step, int P, int64_t N) {
+    if (++c.row == c.end) {
+        c.tile += step;
+        tile_seek(c, P, N);
+    }
+}
+
+template <typename T, bool LN, int NT, int S, bool WS>
+__global__ void __launch_bounds__(NT, 3)
+    norm_bwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
+                     const T* __restrict__ dy, int64_t lddy, float eps, T* __restrict__ dx,
+                     int64_t lddx, float* __restrict__ part, int64_t N, int Dv, int64_t P) {
+    using E = Elt<T>;
+    constexpr int V = E::V, CPT = 16 / V;
+    constexpr bool C = std::is_same<T, float>::value;
+    static_assert(S >= (LN ? 3 : 2), "LayerNorm holds two staged rows");
+    // sums: Σ d², Σ g·d[, Σ g, Σx of the next row]
+    constexpr int K = LN ? 4 : 2;
+    constexpr unsigned CM = (C ? (LN ? 7u : 3u) : 0u) | (LN ? 8u : 0u);
+    const int64_t D = (int64_t)Dv * V;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
+    Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
+    __shared__ __align__(8) uint64_t xbar[2];
+    NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
+    xc.init();
+    cluster_sync();
+    const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;
+    const float fd = (float)D, inv_d = 1.0f / fd;
+    const unsigned valid = chunk_mask<NT, CPT>(Dv, l);
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    pdl_wait();
+    // w of chunk c: this thread's own shared-memory slots (WS), or read-only
+    // loads of the CTA's slice
+    float4* ws4 = reinterpret_cast<float4*>(gs + S * CPT * NT);  // [CPT·V/4][NT]
+    if constexpr (WS) {
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            const int ch = l + c * NT;
+#pragma unroll
+            for (int q = 0; q < V / 4; q++) {
+                const Raw16 r = (ch < Dv) ? ld_keep(w + (int64_t)ch * V + 4 * q) : raw_zero();
+                ws4[(c * (V / 4) + q) * NT + threadIdx.x] =
+                    make_float4(__uint_as_float(r.u[0]), __uint_as_float(r.u[1]),
+                                __uint_as_float(r.u[2]), __uint_as_float(r.u[3]));
+            }
+        }
+    }
+    auto w_of = [&](int c, float (&o)[V]) {
+#pragma unroll
+        for (int q = 0; q < V / 4; q++) {
+            float4 t;
+            if constexpr (WS) {
+                t = ws4[(c * (V / 4) + q) * NT + threadIdx.x];
+            } else {
+                const Raw16 r = ld_keep(w + (int64_t)(l + c * NT) * V + 4 * q);
+                t = make_float4(__uint_as_float(r.u[0]), __uint_as_float(r.u[1]),
+                                __uint_as_float(r.u[2]), __uint_as_float(r.u[3]));
+            }
+            o[4 * q] = t.x;
+            o[4 * q + 1] = t.y;
+            o[4 * q + 2] = t.z;
+            o[4 * q + 3] = t.w;
+        }
+    };
+    // rows of this cluster: its tiles in order
+    int64_t iters = 0;
+    for (int64_t t = cid; t < P; t += ncl) {
+        int64_t a, b2;
+        norm_tile_rows(t, P, N, a, b2);
+        iters += b2 - a;
+    }
+    const int Pi = (int)P, step = (int)ncl;
+    TileCursor cw{(int)cid, 0, 0}, sw{(int)cid, 0, 0};
+    tile_seek(cw, Pi, N);
+    tile_seek(sw, Pi, N);
+    const int64_t ldxb = ldx * (int64_t)sizeof(T), ldgb = lddy * (int64_t)sizeof(T);
+    const char* xb = reinterpret_cast<const char*>(x) + (int64_t)l * 16;
+    const char* gb = reinterpret_cast<const char*>(dy) + (int64_t)l * 16;
+    auto stage = [&](int slot) {
+        if (sw.tile < Pi) {
+            const char* px = xb + sw.row * ldxb;
+            const char* pg = gb + sw.row * ldgb;
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                const bool ok = valid >> c & 1u;
+                cp_async16(&xs[(slot * CPT + c) * NT + threadIdx.x],
+                           ok ? px + c * NT * 16 : reinterpret_cast<const char*>(x), ok ? 16 : 0);
+                cp_async16(&gs[(slot * CPT + c) * NT + threadIdx.x],
+                           ok ? pg + c * NT * 16 : reinterpret_cast<const char*>(dy), ok ? 16 : 0);
+            }
+            tile_advance(sw, step, Pi, N);
+        }
+    };
+    float aw[CPT][V], ab[CPT][V];
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+#pragma unroll
+        for (int v = 0; v < V; v++) aw[c][v] = ab[c][v] = 0.f;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) {
+        stage(k);
+        cp_async_commit();
+    }
+    Mean mn{0.f, 0.f};
+    if (LN && iters > 0) {  // the first row's Σx
+        cp_async_wait<S - 2>();
+        Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
+        cluster_reduce<NT, 1, 1u>(s0, xc);
+        mn = mean_of(s0[0], fd, inv_d);
+    }
+    for (int64_t k = 0; k < iters; k++) {
+        if constexpr (LN)
+            cp_async_wait<(LN ? S - 3 : 0)>();  // rows k and k + 1
+        else
+            cp_async_wait<S - 2>();
+        stage((int)((k + S - 1) % S));
+        cp_async_commit();
+        const int64_t row = cw.row;
+        const Raw16* cx = xs + (k % S) * CPT * NT + threadIdx.x;
+        const Raw16* cg = gs + (k % S) * CPT * NT + threadIdx.x;
+        // d of chunk c (x, or x − μ), widened from the staged slot in each
+        // pass rather than held across the exchange
+        auto d_of = [&](int c, float (&o)[V]) {
+            E::widen(cx[c * NT], o);
+            if constexpr (LN)
+#pragma unroll
+                for (int v = 0; v < V; v++) o[v] = (o[v] - mn.mu0) - mn.c;
+        };
+        Acc2 sums[K];
+#pragma unroll
+        for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (valid >> c & 1u) {
+                float dc[V], gc[V], wc[V];
+                d_of(c, dc);
+                E::widen(cg[c * NT], gc);
+                w_of(c, wc);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float gg = gc[v] * wc[v];
+                    s_fma<C>(sums[0], dc[v], dc[v]);
+                    s_fma<C>(sums[1], gg, dc[v]);
+                    if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
+                }
+            }
+        }
+        if constexpr (LN)
+            if (k + 1 < iters)
+                sums[LN ? 3 : 0] =
+                    staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
+        cluster_reduce<NT, K, CM>(sums, xc);
+        const float r = rstd_of<C>(s_val(sums[0]), inv_d, eps);
+        const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
+        const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;
+        T* dxrow = dx + row * lddx + (int64_t)l * V;
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (valid >> c & 1u) {
+                float o[V], dc[V], gc[V], wc[V];
+                d_of(c, dc);
+                E::widen(cg[c * NT], gc);
+                w_of(c, wc);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float xh = dc[v] * r;
+                    const float gg = gc[v] * wc[v];
+                    // r·((g − mean g) − x̂·mean(g·x̂))
+                    o[v] = fmaf(-xh, rmgx, fmaf(gg, r, -rmg));
+                    aw[c][v] = fmaf(gc[v], xh, aw[c][v]);
+                    if constexpr (LN) ab[c][v] += gc[v];
+                }
+                st_stream(dxrow + (int64_t)c * NT * V, E::narrow(o));
+            }
+        }
+        if constexpr (LN) mn = mean_of(sums[LN ? 3 : 0], fd, inv_d);  // the next row's
+        if (row + 1 == cw.end) {  // the tile's last row: its partial row(s)
+            float* pw = part + cw.tile * D;
+            float* pb = part + (P + cw.tile) * D;
+#pragma unroll
+            for (int c = 0; c < CPT; c++) {
+                if (valid >> c & 1u) {
+                    const int64_t col = (int64_t)(l + c * NT) * V;
+#pragma unroll
+                    for (int v = 0; v < V; v++) {
+                        pw[col + v] = aw[c][v];
+                        aw[c][v] = 0.f;
+                        if constexpr (LN) {
+                            pb[col + v] = ab[c][v];
+                            ab[c][v] = 0.f;
+                        }
+                    }
+                }
+            }
+        }
+        tile_advance(cw, step, Pi, N);
+    }
+    cp_async_wait<0>();
+    cluster_sync();
+    pdl_trigger();
+}
+
+// ===========================================================================
 // Element-wise paths (any alignment, any D): one CTA per row (forward) or per
 // row tile (backward), several passes over each row.
 // ===========================================================================
@@ -726,6 +1165,19 @@ static cudaError_t norm_fwd_t(const T* x, int64_t ldx, const float* w, const flo
                           ldy, N, (int)Dv);
         });
     }
+    if (D % V == 0 && D <= kNormClusterRowMax && ldx % V == 0 && ldy % V == 0 && aligned16(x) &&
+        aligned16(y) && aligned16(w) && (!LN || aligned16(b))) {
+        constexpr int NT = kNormClusterNT, S = kNormFwdStages[LN], CPT = 16 / V;
+        constexpr auto k = norm_fwd_cluster<T, LN, NT, S>;
+        const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
+        const size_t smem = (size_t)S * CPT * NT * 16;
+        int fit = 0;
+        cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
+        if (e == cudaSuccess)
+            return launch_cluster(k, (unsigned)std::min<int64_t>(N, fit), cs, dim3(NT), smem, s, x,
+                                  ldx, w, b, eps, y, ldy, N, (int)Dv);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return launch(norm_fwd_scalar<T, LN, 256>,
                   dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)), dim3(256), 0, s, true, x,
                   ldx, w, b, eps, y, ldy, N, D);
@@ -764,8 +1216,26 @@ static cudaError_t norm_bwd_t(const T* x, int64_t ldx, const float* w, const T* 
                               eps, dx, lddx, part, N, (int)Dv, P);
             });
         } else {
-            e = launch(norm_bwd_scalar<T, LN, 256>, dim3((unsigned)P), dim3(256), 0, s, true, x,
-                       ldx, w, dy, lddy, eps, dx, lddx, part, N, D, P);
+            e = cudaErrorNotSupported;
+            if (D % V == 0 && D <= kNormClusterRowMax && ldx % V == 0 && lddy % V == 0 &&
+                lddx % V == 0 && aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(w)) {
+                constexpr int NT = kNormClusterNT, CPT = 16 / V;
+                constexpr int S = V == 4 ? kNormBwdStages32[LN] : kNormBwdStages16[LN];
+                constexpr bool WS = kNormBwdWSlots[LN];
+                constexpr auto k = norm_bwd_cluster<T, LN, NT, S, WS>;
+                const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
+                // staged x and dy, then (WS) this thread's w slots
+                const size_t smem =
+                    (size_t)2 * S * CPT * NT * 16 + (WS ? (size_t)CPT * V * NT * 4 : 0);
+                int fit = 0;
+                e = cluster_fit<k>(cs, NT, smem, fit);
+                if (e == cudaSuccess)
+                    e = launch_cluster(k, (unsigned)std::min<int64_t>(P, fit), cs, dim3(NT), smem,
+                                       s, x, ldx, w, dy, lddy, eps, dx, lddx, part, N, (int)Dv, P);
+            }
+            if (e == cudaErrorNotSupported)
+                e = launch(norm_bwd_scalar<T, LN, 256>, dim3((unsigned)P), dim3(256), 0, s, true,
+                           x, ldx, w, dy, lddy, eps, dx, lddx, part, N, D, P);
         }
         if (e != cudaSuccess) return e;
     }
@@ -811,6 +1281,15 @@ static cudaError_t norm_bwd_any(const void* x, int64_t ldx, const float* w, cons
                                                  (__nv_bfloat16*)dx, lddx, gw, gb, accumulate,
                                                  part, N, D, s);
     }
+}
+
+cudaError_t norm_wait_timeouts(unsigned* count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_norm_wait_timeouts, sizeof(unsigned));
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_norm_wait_timeouts, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 cudaError_t launch_norm_fwd(const void* x, int64_t ldx, const float* w, const float* b, float eps,

@@ -16,7 +16,6 @@
 // multi-pass path with one CTA per row.  Sums of binary32 rows are
 // compensated and their exponents taken of exactly split differences.
 #include <algorithm>
-#include <atomic>
 #include <type_traits>
 
 #include "wsf_device.cuh"
@@ -432,14 +431,6 @@ __global__ void __launch_bounds__(NT)
 // reaches only after its reads of row k; a last barrier keeps each CTA's
 // shared memory alive until the other CTAs have read it.
 constexpr int kClusterCPT = 4;
-constexpr int kClusterMaxCS = 16;
-
-__device__ __forceinline__ float4 cluster_ld_f32x4(uint32_t a) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -734,7 +725,6 @@ static cudaError_t dispatch_rows(int64_t Dv, int64_t N, F&& go) {
 // Cluster shapes: a CTA of NT threads holds NT·4 chunks of a row; rows of up
 // to 8 CTAs of 256 threads (8192 chunks, 128 KB) take clusters of 256-thread
 // CTAs, wider rows 512-thread CTAs, up to 16 a cluster (32768 chunks, 512 KB).
-constexpr int kMaxDevices = 64;
 constexpr int64_t kClusterRowChunks = (int64_t)kClusterMaxCS * 512 * kClusterCPT;
 
 static void cluster_shape(int64_t Dv, int& nt, unsigned& cs) {
@@ -748,24 +738,9 @@ static void cluster_shape(int64_t Dv, int& nt, unsigned& cs) {
 template <auto kernel, typename... Args>
 static cudaError_t go_cluster(int nt, unsigned cs, size_t smem, int64_t N, cudaStream_t s,
                               Args&&... args) {
-    cudaError_t e = cudaFuncSetAttribute((const void*)kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && cs > 8)
-        e = cudaFuncSetAttribute((const void*)kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    int fit = 0;
+    const cudaError_t e = cluster_fit<kernel>(cs, nt, smem, fit);
     if (e != cudaSuccess) return e;
-    // resident clusters of this kernel and size, per device, queried once
-    static std::atomic<int> fits[kMaxDevices][kClusterMaxCS + 1];
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int fit = dev < kMaxDevices ? fits[dev][cs].load(std::memory_order_relaxed) : 0;
-    if (fit == 0) {
-        fit = max_active_clusters(kernel, cs, dim3(nt), smem);
-        if (fit <= 0) fit = -1;
-        if (dev < kMaxDevices) fits[dev][cs].store(fit, std::memory_order_relaxed);
-    }
-    if (fit < 0) return cudaErrorNotSupported;
     const unsigned clusters = (unsigned)std::min<int64_t>(N, fit);
     return launch_cluster(kernel, clusters, cs, dim3(nt), smem, s, std::forward<Args>(args)...);
 }

@@ -285,5 +285,115 @@ __device__ __forceinline__ float2 cluster_ld_f32x2(uint32_t a) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ float4 cluster_ld_f32x4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier-completed pushes into another CTA's shared memory (sm_90 and
+// later).  st.async writes a value into the shared memory of a CTA of the
+// cluster and counts its bytes against that CTA's mbarrier; the receiver
+// posts how many bytes it expects (arrive.expect_tx) and waits on the
+// barrier's phase, after which the pushed data is visible to it.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// about `limit_ns` nanoseconds; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+// Push 16 bytes to the cluster shared address `dst`, completing `bar` (the
+// cluster shared address of the receiving CTA's mbarrier).
+__device__ __forceinline__ void st_async_f32x4(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
+
+// One entry a warp (NV float4, the same in every lane) exchanged among the
+// CTAs of a cluster: lane q of each warp pushes the warp's entry into slot
+// rank·W + warp of CTA q, and every CTA waits until the entries of all
+// cs·W warps of the cluster have arrived in its own buffer.  Turns alternate
+// between two buffers, each with its own mbarrier (phase parity = turn/2).
+// A buffer is written again two turns later; a CTA pushes turn t + 2 only
+// after it has received every entry of turn t + 1, and each warp pushes its
+// turn t + 1 entry only after it has read turn t, so no entry overwrites one
+// still being read, and the mbarrier of a turn sees only that turn's bytes.
+// The count of bytes expected is posted by thread 0 (pushes that land
+// before it leave the phase pending).  A wait longer than a second marks
+// the exchange dead (later waits are skipped) and counts a timeout, so that
+// a fault in the protocol ends the kernel with wrong results and a raised
+// counter instead of a hang.  Each CTA of a cluster must run the same turns,
+// and the caller must make every CTA's barriers initialised (init(), then a
+// cluster barrier) before the first turn.
+template <int W, int SLOTS, int NV>
+struct WarpPush {
+    float4 (*buf)[SLOTS][NV];  // shared [2][SLOTS][NV]
+    uint64_t* bar;             // shared [2]
+    unsigned* timeouts;        // device counter of waits that ran out
+    unsigned turn;
+    bool live;
+
+    __device__ __forceinline__ void init() {
+        if (threadIdx.x == 0) {
+            mbar_init(&bar[0], 1);
+            mbar_init(&bar[1], 1);
+            mbar_init_fence();
+        }
+    }
+
+    // Push `e` (the first NX float4 of an entry) and return this turn's
+    // local buffer once every warp's entry has arrived.
+    template <int NX>
+    __device__ __forceinline__ const float4 (*exchange(const float4 (&e)[NX]))[NV] {
+        static_assert(NX >= 1 && NX <= NV, "entry size");
+        const unsigned p = turn & 1u, ph = (turn >> 1) & 1u;
+        turn++;
+        const unsigned cs = cluster_nctarank(), me = cluster_ctarank();
+        const unsigned lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
+        if (threadIdx.x == 0) mbar_expect_tx(&bar[p], cs * W * NX * 16u);
+        if (lane < cs) {
+            const uint32_t dst = cluster_map(&buf[p][me * W + wid][0], lane);
+            const uint32_t rb = cluster_map(&bar[p], lane);
+#pragma unroll
+            for (int q = 0; q < NX; q++) st_async_f32x4(dst + 16u * q, e[q], rb);
+        }
+        if (live && !mbar_wait(&bar[p], ph, 1000000000ull)) {
+            live = false;
+            if (lane == 0) atomicAdd(timeouts, 1u);
+        }
+        return buf[p];
+    }
+};
 
 }  // namespace wsf

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace wsf {
@@ -52,6 +53,10 @@ cudaError_t launch_norm_bwd(const void* x, int64_t ldx, const float* w, const vo
                             int64_t lddy, float eps, void* dx, int64_t lddx, float* gw, float* gb,
                             int accumulate, float* part, int64_t N, int64_t D, int dtype,
                             int layer, cudaStream_t s);
+
+// Read (and optionally zero) the count of cluster-exchange waits that ran
+// out in the norm kernels on the current device; synchronises the device.
+cudaError_t norm_wait_timeouts(unsigned* count, bool reset);
 
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);
@@ -125,6 +130,39 @@ int max_active_clusters(void (*kernel)(KArgs...), unsigned cs, dim3 block, size_
         return 0;
     }
     return n;
+}
+
+// Clusters of `cs` CTAs of `kernel` resident at once on the current device,
+// queried once per device, kernel and cluster size (the kernel's shape and
+// shared memory are fixed for a given cs).  Sets the kernel's dynamic
+// shared-memory limit and, for cs > 8, allows the non-portable cluster size.
+// `fit` = 0 with cudaErrorNotSupported when no such cluster fits.
+constexpr int kClusterMaxCS = 16;
+constexpr int kMaxDevices = 64;
+
+template <auto kernel>
+cudaError_t cluster_fit(unsigned cs, int nt, size_t smem, int& fit) {
+    static std::atomic<int> fits[kMaxDevices][kClusterMaxCS + 1];
+    fit = 0;
+    if (cs < 1 || cs > (unsigned)kClusterMaxCS) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute((const void*)kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && cs > 8)
+        e = cudaFuncSetAttribute((const void*)kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int f = dev < kMaxDevices ? fits[dev][cs].load(std::memory_order_relaxed) : 0;
+    if (f == 0) {
+        f = max_active_clusters(kernel, cs, dim3(nt), smem);
+        if (f <= 0) f = -1;
+        if (dev < kMaxDevices) fits[dev][cs].store(f, std::memory_order_relaxed);
+    }
+    if (f < 0) return cudaErrorNotSupported;
+    fit = f;
+    return cudaSuccess;
 }
 
 }  // namespace wsf

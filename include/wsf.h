@@ -85,6 +85,20 @@ const char* wsf_status_string(int status);
 int wsf_version(void);
 
 /*
+ * wsf_cluster_wait_timeouts — health counter of the cluster paths.
+ * Rows too wide for one CTA (RMSNorm/LayerNorm rows of 8193..65536
+ * elements) are split over a thread-block cluster whose CTAs exchange their
+ * partial row sums through distributed shared memory.  Each wait for the
+ * other CTAs' sums gives up after about a second; the launch then finishes
+ * with invalid results and adds one to this counter per thread that gave up,
+ * instead of hanging the GPU.  The counter is zero in correct operation.
+ * count: host pointer receiving the value for the current device.  reset = 1
+ * zeroes it after reading.  Synchronises the current device.
+ * Returns WSF_OK, WSF_ERR_NULL_PTR or WSF_ERR_CUDA.
+ */
+int wsf_cluster_wait_timeouts(unsigned* count, int reset);
+
+/*
  * ws_fwd — weighted-sum forward  [WS §1, §2]
  *   y[i] = Σ_{d<D} x[i,d] · w[d]   for 0 <= i < N
  * x: [N, D] dtype, row stride ldx; w: [D] binary32; y: [N] dtype.

@@ -35,6 +35,13 @@ def test_exports_every_declared_symbol(wsf):
         assert hasattr(wsf.lib, n), n
 
 
+def test_cluster_wait_timeouts_rejects(wsf):
+    n = ctypes.c_uint(7)
+    assert wsf.lib.wsf_cluster_wait_timeouts(None, 0) == -1
+    assert wsf.lib.wsf_cluster_wait_timeouts(ctypes.byref(n), 2) == -8
+    assert n.value == 7
+
+
 def test_status_strings(wsf):
     for code in range(-9, 1):
         s = wsf.status_string(code)

@@ -1,6 +1,8 @@
 """GPU parity of RMSNorm and LayerNorm, forward and backward, against the fp64
-oracle: every row-width class of the staged path, the element-wise path
-(unaligned or wider than 8192), row strides and guard bands, constant rows,
+oracle: every row-width class of the staged path, the cluster path (rows of
+8193..65536 elements over clusters of 3 to 16 CTAs, ragged last slices,
+clusters that walk several row tiles), the element-wise path (unaligned or
+wider than 65536), row strides and guard bands, constant rows,
 rows with a large common offset or with massive outlier columns, tall inputs
 that fill all 912 row tiles, accumulate, empty extents, bit reproducibility,
 and the measurement size (sampled dx rows, full grad_w / grad_b)."""
@@ -174,6 +176,69 @@ def test_norm_accumulate_reproducible_empty(wsf, layer):
     y0 = wsf.layernorm_fwd(x0, w, b, eps) if layer else wsf.rmsnorm_fwd(x0, w, eps)
     torch.cuda.synchronize()
     assert y0.shape == (0, 768)
+
+
+# Cluster rows: CTAs of 4096 elements, one cluster a row.
+@pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D", [(300, 8200), (200, 12288), (130, 16384), (40, 32768),
+                                 (37, 36864), (20, 50000), (9, 65536), (3, 65544)])
+def test_norm_cluster_rows(wsf, layer, dt, N, D):
+    x, w, dy, b = _inputs(N, D, dt, seed=D % 97)
+    _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b))
+
+
+@pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
+def test_norm_cluster_tile_walk(wsf, layer):
+    # 63 row tiles over clusters of 9 CTAs: fewer clusters fit at once, so
+    # clusters take several tiles each and stage across tile boundaries
+    x, w, dy, b = _inputs(4000, 36864, "bf16", seed=4)
+    _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b))
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_norm_cluster_offset_outliers_strides(wsf, dt):
+    x, w, dy, b = _inputs(40, 20000, dt, seed=6, mean=100.0)
+    x[3] = 0.0
+    x[4] = 0.25
+    x[5, ::2] = -2.0
+    x[5, 1::2] = 2.0
+    x[10:, 0] = 500.0      # outliers in the first and in the last CTA's slice
+    x[10:, 17000] = -300.0
+    for layer in (False, True):
+        _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b, pad=8))
+
+
+@pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
+def test_norm_cluster_accumulate_reproducible(wsf, layer):
+    D = 20000
+    x, w, dy, b = (t.to(DEV) for t in _inputs(500, D, "bf16", seed=9))
+
+    def bwd(gw=None, gb=None, acc=False):
+        if layer:
+            return wsf.layernorm_bwd(x, w, dy, EPS, grad_w=gw, grad_b=gb, accumulate=acc)
+        dx, g = wsf.rmsnorm_bwd(x, w, dy, EPS, grad_w=gw, accumulate=acc)
+        return dx, g, None
+
+    runs = [bwd() for _ in range(3)]
+    for r in runs[1:]:
+        for a, c in zip(r, runs[0]):
+            assert a is None or torch.equal(a, c)
+    fw = [wsf.layernorm_fwd(x, w, b, EPS) if layer else wsf.rmsnorm_fwd(x, w, EPS) for _ in range(2)]
+    assert torch.equal(fw[0], fw[1])
+    old_w, old_b = torch.randn(D, device=DEV), torch.randn(D, device=DEV)
+    _, gw, gb = bwd(gw=old_w.clone(), gb=old_b.clone() if layer else None, acc=True)
+    assert torch.equal(gw, old_w + runs[0][1])
+    if layer:
+        assert torch.equal(gb, old_b + runs[0][2])
+
+
+def test_norm_cluster_no_wait_timeouts(wsf):
+    # every cluster launch so far exchanged its partial sums without a wait
+    # running out (the counter is per process and device)
+    x, w, dy, b = _inputs(64, 30000, "bf16", seed=8)
+    _run(wsf, True, x, w, dy, b)
+    assert wsf.cluster_wait_timeouts() == 0
 
 
 @pytest.mark.slow
