@@ -83,7 +83,12 @@ int wsf_version(void) { return 100; }
 int wsf_cluster_wait_timeouts(unsigned* count, int reset) {
     if (!count) return WSF_ERR_NULL_PTR;
     if (reset != 0 && reset != 1) return WSF_ERR_BAD_ARG;
-    return cuda_status(wsf::norm_wait_timeouts(count, reset != 0));
+    unsigned a = 0, b = 0;
+    cudaError_t e = wsf::norm_wait_timeouts(&a, reset != 0);
+    if (e == cudaSuccess) e = wsf::softmax_wait_timeouts(&b, reset != 0);
+    if (e != cudaSuccess) return WSF_ERR_CUDA;
+    *count = a + b;
+    return WSF_OK;
 }
 
 int ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N, int64_t D, int dtype,

@@ -599,7 +599,7 @@ __device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
 template <int NT, int K, unsigned CM>
 __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp) {
     static_assert(K >= 1 && K <= 4, "up to four sums");
-    constexpr int W = NT / 32, EPL = (kClusterMaxCS * W + 31) / 32, NX = (K + 1) / 2;
+    constexpr int W = NT / 32, NX = (K + 1) / 2;
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CM >> q) & 1u);
@@ -614,20 +614,16 @@ __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp) {
     Acc2 t[K];
 #pragma unroll
     for (int q = 0; q < K; q++) t[q] = acc2_zero();
+    for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
 #pragma unroll
-    for (int i = 0; i < EPL; i++) {
-        const int j = lane + 32 * i;
-        if (j < total) {
+        for (int n = 0; n < NX; n++) {
+            const float4 en = buf[j][n];
 #pragma unroll
-            for (int n = 0; n < NX; n++) {
-                const float4 en = buf[j][n];
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int q = 2 * n + h;
-                    if (q < K) {
-                        const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
-                        t[q] = ((CM >> q) & 1u) ? acc2_add(t[q], o) : Acc2{t[q].hi + o.hi, 0.f};
-                    }
+            for (int h = 0; h < 2; h++) {
+                const int q = 2 * n + h;
+                if (q < K) {
+                    const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
+                    t[q] = ((CM >> q) & 1u) ? acc2_add(t[q], o) : Acc2{t[q].hi + o.hi, 0.f};
                 }
             }
         }

@@ -413,24 +413,26 @@ __global__ void __launch_bounds__(NT)
 // its slice of x (y, dy) once and writes y (dx) once.
 //
 // One exchange a row.  Each warp reduces its own part of the slice (xor
-// butterfly) and lane 0 publishes the warp's entry in shared memory; after a
-// cluster barrier every warp of every CTA reads all CS·NT/32 entries through
-// distributed shared memory, lane ℓ taking entries ℓ, ℓ+32, …, combines them
-// in that order and then across lanes (xor butterfly).  Every warp therefore
-// derives the same bits of the row statistic, with no barrier inside the
-// CTA.  The forward publishes (m_w, s_w): the warp's maximum and its sum of
-// exp(x − m_w); the row sum is Σ_w s_w·exp(m_w − M), M = max_w m_w, and
-// y = exp(x − m_w)·(exp(m_w − M)/sum) (the combination of partial softmax
-// sums by rescaling, as in online softmax).  The backward publishes the
-// warp's part of Σ dy·y.
-//
-// Every CTA of a cluster runs the same number of rows (it depends only on the
-// cluster's index), hence the same number of cluster barriers.  Entries
-// alternate between two buffers by row parity: the buffer of row k is written
-// again for row k + 2, after the barrier of row k + 1, which every reader
-// reaches only after its reads of row k; a last barrier keeps each CTA's
-// shared memory alive until the other CTAs have read it.
+// butterfly) and pushes the warp's entry into every CTA of the cluster
+// (WarpPush: st.async completing on the receiver's mbarrier, no cluster
+// barrier in the loop); every warp of every CTA then combines all CS·NT/32
+// entries from its own shared memory, lane ℓ taking entries ℓ, ℓ+32, …, in
+// that order and then across lanes (xor butterfly), so every warp derives
+// the same bits of the row statistic.  The forward publishes (m_w, s_w): the
+// warp's maximum and its sum of exp(x − m_w); the row sum is
+// Σ_w s_w·exp(m_w − M), M = max_w m_w, and y = exp(x − m_w)·(exp(m_w − M)/sum)
+// (the combination of partial softmax sums by rescaling, as in online
+// softmax).  The backward publishes the warp's part of Σ dy·y.  Every CTA of
+// a cluster runs the same number of rows (it depends only on the cluster's
+// index), hence the same exchanges.
 constexpr int kClusterCPT = 4;
+
+// Waits of the cluster exchanges that ran out (see WarpPush); zero unless
+// the exchange protocol failed.
+__device__ unsigned g_softmax_wait_timeouts;
+
+template <int NT>
+using SoftmaxPush = WarpPush<NT / 32, kClusterMaxCS*(NT / 32), 1>;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -452,13 +454,16 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
                         int64_t N, int Dv) {
     using E = Elt<T>;
     constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
-    constexpr int EPL = (kClusterMaxCS * W + 31) / 32;  // entries a lane reads, at most
     constexpr bool kComp = std::is_same<T, float>::value;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* slots = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
-    __shared__ __align__(16) float4 pub[2][W];
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
+    __shared__ __align__(8) uint64_t xbar[2];
+    SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
+    xp.init();
+    cluster_sync();
     const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;  // chunk l + c·NT
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int total = (int)cluster_nctarank() * W;
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     const int64_t iters = cid < N ? (N - 1 - cid) / ncl + 1 : 0;
@@ -521,31 +526,21 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
             }
             s = group_sum2<32>(s);
         }
-        float4* buf = pub[k & 1];
-        if (lane == 0) buf[wid] = make_float4(m, s.hi, s.lo, 0.f);
-        cluster_sync();
-        // every (rank, warp) entry: j = rank·W + warp
-        float4 ent[EPL];
+        const float4 mine[1] = {make_float4(m, s.hi, s.lo, 0.f)};
+        const float4(*buf)[1] = xp.template exchange<1>(mine);
+        // every (rank, warp) entry j = rank·W + warp, from this CTA's buffer
         float M = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const int j = lane + 32 * i;
-            if (j < total) {
-                ent[i] = cluster_ld_f32x4(cluster_map(&buf[j % W], (unsigned)(j / W)));
-                M = fmaxf(M, ent[i].x);
-            }
-        }
+        for (int j = lane; j < total; j += 32) M = fmaxf(M, buf[j][0].x);
         M = warp_max(M);
         Acc2 t = acc2_zero();
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const int j = lane + 32 * i;
-            if (j < total && ent[i].y > 0.f) {  // skip warps without a finite element
-                const float g = rescale<kComp>(ent[i].x, M);
+        for (int j = lane; j < total; j += 32) {
+            const float4 en = buf[j][0];
+            if (en.y > 0.f) {  // skip warps without a finite element
+                const float g = rescale<kComp>(en.x, M);
                 if constexpr (kComp)
-                    acc2_fma(t, __fadd_rn(ent[i].y, ent[i].z), g);
+                    acc2_fma(t, __fadd_rn(en.y, en.z), g);
                 else
-                    t.hi = fmaf(ent[i].y, g, t.hi);
+                    t.hi = fmaf(en.y, g, t.hi);
             }
         }
         float inv;
@@ -577,14 +572,17 @@ __global__ void __launch_bounds__(NT)
                         int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int Dv) {
     using E = Elt<T>;
     constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
-    constexpr int EPL = (kClusterMaxCS * W + 31) / 32;
     constexpr bool kComp = std::is_same<T, float>::value;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* ys = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     Raw16* gs = ys + S * CPT * NT;                    // [S][CPT][NT]
-    __shared__ __align__(8) float2 pub[2][W];
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
+    __shared__ __align__(8) uint64_t xbar[2];
+    SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
+    xp.init();
+    cluster_sync();
     const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int total = (int)cluster_nctarank() * W;
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     const int64_t iters = cid < N ? (N - 1 - cid) / ncl + 1 : 0;
@@ -628,20 +626,15 @@ __global__ void __launch_bounds__(NT)
             s = group_sum2<32>(s);
         else
             s.hi = group_sum<32>(s.hi);
-        float2* buf = pub[k & 1];
-        if (lane == 0) buf[wid] = make_float2(s.hi, s.lo);
-        cluster_sync();
+        const float4 mine[1] = {make_float4(s.hi, s.lo, 0.f, 0.f)};
+        const float4(*buf)[1] = xp.template exchange<1>(mine);
         Acc2 t = acc2_zero();
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const int j = lane + 32 * i;
-            if (j < total) {
-                const float2 o = cluster_ld_f32x2(cluster_map(&buf[j % W], (unsigned)(j / W)));
-                if constexpr (kComp)
-                    t = acc2_add(t, Acc2{o.x, o.y});
-                else
-                    t.hi += o.x;
-            }
+        for (int j = lane; j < total; j += 32) {
+            const float4 o = buf[j][0];
+            if constexpr (kComp)
+                t = acc2_add(t, Acc2{o.x, o.y});
+            else
+                t.hi += o.x;
         }
         float sv;
         if constexpr (kComp) {
@@ -829,6 +822,15 @@ static cudaError_t softmax_bwd_t(const T* y, int64_t ldy, const T* dy, int64_t l
     constexpr int NT = 256;
     return launch(softmax_bwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
                   dim3(NT), 0, s, true, y, ldy, dy, lddy, dx, lddx, N, D);
+}
+
+cudaError_t softmax_wait_timeouts(unsigned* count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_softmax_wait_timeouts, sizeof(unsigned));
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_softmax_wait_timeouts, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 cudaError_t launch_softmax_fwd(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t N,

@@ -55,8 +55,10 @@ cudaError_t launch_norm_bwd(const void* x, int64_t ldx, const float* w, const vo
                             int layer, cudaStream_t s);
 
 // Read (and optionally zero) the count of cluster-exchange waits that ran
-// out in the norm kernels on the current device; synchronises the device.
+// out in the norm (softmax) kernels on the current device; synchronises the
+// device.
 cudaError_t norm_wait_timeouts(unsigned* count, bool reset);
+cudaError_t softmax_wait_timeouts(unsigned* count, bool reset);
 
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);

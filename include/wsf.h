@@ -86,9 +86,10 @@ int wsf_version(void);
 
 /*
  * wsf_cluster_wait_timeouts — health counter of the cluster paths.
- * Rows too wide for one CTA (RMSNorm/LayerNorm rows of 8193..65536
- * elements) are split over a thread-block cluster whose CTAs exchange their
- * partial row sums through distributed shared memory.  Each wait for the
+ * Rows too wide for one CTA (softmax rows of more than 2048 16-byte chunks,
+ * RMSNorm/LayerNorm rows of 8193..65536 elements) are split over a
+ * thread-block cluster whose CTAs exchange their partial row sums through
+ * distributed shared memory.  Each wait for the
  * other CTAs' sums gives up after about a second; the launch then finishes
  * with invalid results and adds one to this counter per thread that gave up,
  * instead of hanging the GPU.  The counter is zero in correct operation.

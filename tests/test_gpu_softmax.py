@@ -156,6 +156,15 @@ def test_softmax_masked_logits(wsf, dt, N, D):
         assert bool((y[i, t:] == 0).all()) and bool((dx[i, t:] == 0).all())
 
 
+def test_softmax_cluster_no_wait_timeouts(wsf):
+    # every cluster launch so far exchanged its partial sums without a wait
+    # running out (the counter is per process and device)
+    x, dy = _inputs(16, 50000, "bf16", seed=3)
+    _, yin = oracle.softmax_fwd(x)
+    _run(wsf, x, dy, yin)
+    assert wsf.cluster_wait_timeouts() == 0
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_softmax_cluster_strides(wsf, dt):
     x, dy = _inputs(40, 40000, dt, seed=2)
