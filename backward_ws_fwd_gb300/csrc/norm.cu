@@ -551,9 +551,10 @@ __global__ void __launch_bounds__(NT, MINB)
 // it through the read-only cache, re-widens x and dy from their slots in each
 // pass, and holds only the dw/db accumulators of exactly those columns.  The row sums are reduced inside each warp (xor butterfly)
 // and exchanged as one entry a warp with WarpPush: every CTA receives the
-// entries of all CS·NT/32 warps of the cluster in its own shared memory, and
-// each warp combines them (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
-// butterfly over the lanes), so every thread derives the same bits of the
+// entries of all CS·NT/32 warps of the cluster in its own shared memory;
+// warp 0 combines them (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
+// butterfly over the lanes) and hands the sums to the other warps through
+// shared memory and a CTA barrier, so every CTA derives the same bits of the
 // row statistics, with the arithmetic of the row path.
 //
 // One exchange a row.  LayerNorm needs Σx before the sums over d = x − μ;
@@ -596,8 +597,13 @@ __device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
 
 // Sum K (up to 4) row sums over the cluster; sum q is compensated if bit q
 // of CM is set.  Every thread of every CTA of the cluster calls it together.
+// Warp 0 waits for the turn, combines the entries (lane ℓ takes entries ℓ,
+// ℓ+32, …, then an xor butterfly) and posts the sums in `res`; a CTA barrier
+// hands them to the other warps (and orders this turn's reads before any
+// warp's next push).
 template <int NT, int K, unsigned CM>
-__device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp) {
+__device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp,
+                                               float4 (*res)[2]) {
     static_assert(K >= 1 && K <= 4, "up to four sums");
     constexpr int W = NT / 32, NX = (K + 1) / 2;
     const int lane = threadIdx.x & 31;
@@ -609,27 +615,45 @@ __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp) {
         const Acc2 a = v[2 * n], b = 2 * n + 1 < K ? v[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
         e[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
     }
-    const float4(*buf)[2] = xp.template exchange<NX>(e);
-    const int total = (int)cluster_nctarank() * W;
-    Acc2 t[K];
+    const unsigned t = xp.template push<NX>(e);
+    float4* out = res[t & 1u];
+    if (threadIdx.x < 32) {
+        const float4(*buf)[2] = xp.wait(t);
+        const int total = (int)cluster_nctarank() * W;
+        Acc2 s[K];
 #pragma unroll
-    for (int q = 0; q < K; q++) t[q] = acc2_zero();
-    for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
+        for (int q = 0; q < K; q++) s[q] = acc2_zero();
+        for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
 #pragma unroll
-        for (int n = 0; n < NX; n++) {
-            const float4 en = buf[j][n];
+            for (int n = 0; n < NX; n++) {
+                const float4 en = buf[j][n];
 #pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const int q = 2 * n + h;
-                if (q < K) {
-                    const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
-                    t[q] = ((CM >> q) & 1u) ? acc2_add(t[q], o) : Acc2{t[q].hi + o.hi, 0.f};
+                for (int h = 0; h < 2; h++) {
+                    const int q = 2 * n + h;
+                    if (q < K) {
+                        const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
+                        s[q] = ((CM >> q) & 1u) ? acc2_add(s[q], o) : Acc2{s[q].hi + o.hi, 0.f};
+                    }
                 }
             }
         }
-    }
 #pragma unroll
-    for (int q = 0; q < K; q++) v[q] = warp_sum(t[q], (CM >> q) & 1u);
+        for (int q = 0; q < K; q++) s[q] = warp_sum(s[q], (CM >> q) & 1u);
+        if (lane == 0)
+#pragma unroll
+            for (int n = 0; n < NX; n++) {
+                const Acc2 a = s[2 * n],
+                           b = 2 * n + 1 < K ? s[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
+                out[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
+            }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NX; n++) {
+        const float4 r = out[n];
+        v[2 * n] = Acc2{r.x, r.y};
+        if (2 * n + 1 < K) v[2 * n + 1 < K ? 2 * n + 1 : 0] = Acc2{r.z, r.w};
+    }
 }
 
 // Σx over this thread's valid chunks of a staged row, exact up to the
@@ -684,6 +708,7 @@ __global__ void __launch_bounds__(NT, 3)
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
     __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
     NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
     xc.init();
     cluster_sync();
@@ -710,7 +735,7 @@ __global__ void __launch_bounds__(NT, 3)
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
         Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u>(s0, xc);
+        cluster_reduce<NT, 1, 1u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
     for (int64_t k = 0; k < iters; k++) {
@@ -735,9 +760,9 @@ __global__ void __launch_bounds__(NT, 3)
             sm[LN ? 1 : 0] = k + 1 < iters
                 ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
                 : acc2_zero();
-            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u>(sm, xc);
+            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u>(sm, xc, xres);
         } else {
-            cluster_reduce<NT, 1, C ? 1u : 0u>(sm, xc);
+            cluster_reduce<NT, 1, C ? 1u : 0u>(sm, xc, xres);
         }
         const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
         if constexpr (LN) mn = mean_of(sm[LN ? 1 : 0], fd, inv_d);
@@ -798,6 +823,7 @@ __global__ void __launch_bounds__(NT, 3)
     Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
     __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
     NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
     xc.init();
     cluster_sync();
@@ -882,7 +908,7 @@ __global__ void __launch_bounds__(NT, 3)
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
         Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u>(s0, xc);
+        cluster_reduce<NT, 1, 1u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
     for (int64_t k = 0; k < iters; k++) {
@@ -926,7 +952,7 @@ __global__ void __launch_bounds__(NT, 3)
             if (k + 1 < iters)
                 sums[LN ? 3 : 0] =
                     staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
-        cluster_reduce<NT, K, CM>(sums, xc);
+        cluster_reduce<NT, K, CM>(sums, xc, xres);
         const float r = rstd_of<C>(s_val(sums[0]), inv_d, eps);
         const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
         const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;

@@ -415,10 +415,11 @@ __global__ void __launch_bounds__(NT)
 // One exchange a row.  Each warp reduces its own part of the slice (xor
 // butterfly) and pushes the warp's entry into every CTA of the cluster
 // (WarpPush: st.async completing on the receiver's mbarrier, no cluster
-// barrier in the loop); every warp of every CTA then combines all CS·NT/32
+// barrier in the loop); warp 0 of every CTA then combines all CS·NT/32
 // entries from its own shared memory, lane ℓ taking entries ℓ, ℓ+32, …, in
-// that order and then across lanes (xor butterfly), so every warp derives
-// the same bits of the row statistic.  The forward publishes (m_w, s_w): the
+// that order and then across lanes (xor butterfly), and hands the result to
+// the other warps through shared memory and a CTA barrier, so every CTA
+// derives the same bits of the row statistic.  The forward publishes (m_w, s_w): the
 // warp's maximum and its sum of exp(x − m_w); the row sum is
 // Σ_w s_w·exp(m_w − M), M = max_w m_w, and y = exp(x − m_w)·(exp(m_w − M)/sum)
 // (the combination of partial softmax sums by rescaling, as in online
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     Raw16* slots = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
     __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float2 res[2];  // (row maximum, 1/sum), by turn parity
     SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
     xp.init();
     cluster_sync();
@@ -527,30 +529,37 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
             s = group_sum2<32>(s);
         }
         const float4 mine[1] = {make_float4(m, s.hi, s.lo, 0.f)};
-        const float4(*buf)[1] = xp.template exchange<1>(mine);
-        // every (rank, warp) entry j = rank·W + warp, from this CTA's buffer
-        float M = -INFINITY;
-        for (int j = lane; j < total; j += 32) M = fmaxf(M, buf[j][0].x);
-        M = warp_max(M);
-        Acc2 t = acc2_zero();
-        for (int j = lane; j < total; j += 32) {
-            const float4 en = buf[j][0];
-            if (en.y > 0.f) {  // skip warps without a finite element
-                const float g = rescale<kComp>(en.x, M);
-                if constexpr (kComp)
-                    acc2_fma(t, __fadd_rn(en.y, en.z), g);
-                else
-                    t.hi = fmaf(en.y, g, t.hi);
+        const unsigned turn = xp.template push<1>(mine);
+        float2* out = &res[turn & 1u];
+        if (threadIdx.x < 32) {  // warp 0 combines the turn's entries
+            const float4(*buf)[1] = xp.wait(turn);
+            // every (rank, warp) entry j = rank·W + warp, from this CTA's buffer
+            float M = -INFINITY;
+            for (int j = lane; j < total; j += 32) M = fmaxf(M, buf[j][0].x);
+            M = warp_max(M);
+            Acc2 t = acc2_zero();
+            for (int j = lane; j < total; j += 32) {
+                const float4 en = buf[j][0];
+                if (en.y > 0.f) {  // skip warps without a finite element
+                    const float g = rescale<kComp>(en.x, M);
+                    if constexpr (kComp)
+                        acc2_fma(t, __fadd_rn(en.y, en.z), g);
+                    else
+                        t.hi = fmaf(en.y, g, t.hi);
+                }
             }
+            float inv;
+            if constexpr (kComp) {
+                t = group_sum2<32>(t);
+                inv = 1.0f / (t.hi + t.lo);
+            } else {
+                inv = 1.0f / group_sum<32>(t.hi);
+            }
+            if (lane == 0) *out = make_float2(M, inv);
         }
-        float inv;
-        if constexpr (kComp) {
-            t = group_sum2<32>(t);
-            inv = 1.0f / (t.hi + t.lo);
-        } else {
-            inv = 1.0f / group_sum<32>(t.hi);
-        }
-        const float sc = rescale<kComp>(m, M) * inv;
+        __syncthreads();
+        const float2 Mi = *out;
+        const float sc = rescale<kComp>(m, Mi.x) * Mi.y;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (l + c * NT < Dv) {
@@ -578,6 +587,7 @@ __global__ void __launch_bounds__(NT)
     Raw16* gs = ys + S * CPT * NT;                    // [S][CPT][NT]
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
     __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float res[2];  // Σ dy·y, by turn parity
     SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
     xp.init();
     cluster_sync();
@@ -627,22 +637,29 @@ __global__ void __launch_bounds__(NT)
         else
             s.hi = group_sum<32>(s.hi);
         const float4 mine[1] = {make_float4(s.hi, s.lo, 0.f, 0.f)};
-        const float4(*buf)[1] = xp.template exchange<1>(mine);
-        Acc2 t = acc2_zero();
-        for (int j = lane; j < total; j += 32) {
-            const float4 o = buf[j][0];
-            if constexpr (kComp)
-                t = acc2_add(t, Acc2{o.x, o.y});
-            else
-                t.hi += o.x;
+        const unsigned turn = xp.template push<1>(mine);
+        float* out = &res[turn & 1u];
+        if (threadIdx.x < 32) {  // warp 0 combines the turn's entries
+            const float4(*buf)[1] = xp.wait(turn);
+            Acc2 t = acc2_zero();
+            for (int j = lane; j < total; j += 32) {
+                const float4 o = buf[j][0];
+                if constexpr (kComp)
+                    t = acc2_add(t, Acc2{o.x, o.y});
+                else
+                    t.hi += o.x;
+            }
+            float r;
+            if constexpr (kComp) {
+                t = group_sum2<32>(t);
+                r = t.hi + t.lo;
+            } else {
+                r = group_sum<32>(t.hi);
+            }
+            if (lane == 0) *out = r;
         }
-        float sv;
-        if constexpr (kComp) {
-            t = group_sum2<32>(t);
-            sv = t.hi + t.lo;
-        } else {
-            sv = group_sum<32>(t.hi);
-        }
+        __syncthreads();
+        const float sv = *out;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (l + c * NT < Dv) {

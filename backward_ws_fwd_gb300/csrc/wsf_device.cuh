@@ -342,20 +342,21 @@ __device__ __forceinline__ void st_async_f32x4(uint32_t dst, float4 v, uint32_t 
 
 // One entry a warp (NV float4, the same in every lane) exchanged among the
 // CTAs of a cluster: lane q of each warp pushes the warp's entry into slot
-// rank·W + warp of CTA q, and every CTA waits until the entries of all
+// rank·W + warp of CTA q; a CTA's turn is complete when the entries of all
 // cs·W warps of the cluster have arrived in its own buffer.  Turns alternate
 // between two buffers, each with its own mbarrier (phase parity = turn/2).
-// A buffer is written again two turns later; a CTA pushes turn t + 2 only
-// after it has received every entry of turn t + 1, and each warp pushes its
-// turn t + 1 entry only after it has read turn t, so no entry overwrites one
-// still being read, and the mbarrier of a turn sees only that turn's bytes.
-// The count of bytes expected is posted by thread 0 (pushes that land
-// before it leave the phase pending).  A wait longer than a second marks
-// the exchange dead (later waits are skipped) and counts a timeout, so that
-// a fault in the protocol ends the kernel with wrong results and a raised
+// Thread 0 posts the bytes expected (pushes that land before it leave the
+// phase pending); the threads that wait (wait()) may then read the turn's
+// buffer.  A buffer is written again two turns later, which no CTA can reach
+// before every CTA has finished reading it, provided that each warp pushes
+// turn t + 1 only after this CTA's readers of turn t are done (the callers
+// put a CTA barrier between them) and that every turn is waited for by
+// thread 0.  A wait longer than a second marks the exchange dead for the
+// waiting thread (later waits are skipped) and counts a timeout, so that a
+// fault in the protocol ends the kernel with wrong results and a raised
 // counter instead of a hang.  Each CTA of a cluster must run the same turns,
-// and the caller must make every CTA's barriers initialised (init(), then a
-// cluster barrier) before the first turn.
+// and every CTA's barriers must be initialised (init(), then a cluster
+// barrier) before the first push.
 template <int W, int SLOTS, int NV>
 struct WarpPush {
     float4 (*buf)[SLOTS][NV];  // shared [2][SLOTS][NV]
@@ -372,13 +373,11 @@ struct WarpPush {
         }
     }
 
-    // Push `e` (the first NX float4 of an entry) and return this turn's
-    // local buffer once every warp's entry has arrived.
+    // Push `e` (the first NX float4 of an entry); returns the turn's number.
     template <int NX>
-    __device__ __forceinline__ const float4 (*exchange(const float4 (&e)[NX]))[NV] {
+    __device__ __forceinline__ unsigned push(const float4 (&e)[NX]) {
         static_assert(NX >= 1 && NX <= NV, "entry size");
-        const unsigned p = turn & 1u, ph = (turn >> 1) & 1u;
-        turn++;
+        const unsigned t = turn++, p = t & 1u;
         const unsigned cs = cluster_nctarank(), me = cluster_ctarank();
         const unsigned lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
         if (threadIdx.x == 0) mbar_expect_tx(&bar[p], cs * W * NX * 16u);
@@ -388,11 +387,16 @@ struct WarpPush {
 #pragma unroll
             for (int q = 0; q < NX; q++) st_async_f32x4(dst + 16u * q, e[q], rb);
         }
-        if (live && !mbar_wait(&bar[p], ph, 1000000000ull)) {
+        return t;
+    }
+
+    // Wait until turn t is complete; returns its buffer.
+    __device__ __forceinline__ const float4 (*wait(unsigned t))[NV] {
+        if (live && !mbar_wait(&bar[t & 1u], (t >> 1) & 1u, 1000000000ull)) {
             live = false;
-            if (lane == 0) atomicAdd(timeouts, 1u);
+            if ((threadIdx.x & 31u) == 0) atomicAdd(timeouts, 1u);
         }
-        return buf[p];
+        return buf[t & 1u];
     }
 };
 

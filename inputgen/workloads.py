@@ -75,4 +75,16 @@ WORKLOADS = {
                    w=Dist(NORMAL, 1.0, 0.1), b=Dist(NORMAL, 0.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0),
                    eps=2.0 ** -17,
                    note="LayerNorm, bf16 x[65536,4096] ~N(0.5,1), w ~N(1,0.1), b ~N(0,0.1), eps 2^-17"),
+    # wide rows, split over thread-block clusters: a vocabulary-sized softmax
+    # (131,072 columns) and norms over a hidden size of 16,384
+    "s2": Workload("s2", "softmax", "bf16", 4096, 131072, x=Dist(NORMAL, 0.0, 2.0),
+                   dy=Dist(NORMAL, 0.0, 1.0),
+                   note="row softmax, bf16 x[4096,131072] ~N(0,2), dy ~N(0,1)"),
+    "n3": Workload("n3", "rmsnorm", "bf16", 16384, 16384, x=Dist(NORMAL, 0.0, 1.0),
+                   w=Dist(NORMAL, 1.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0), eps=2.0 ** -17,
+                   note="RMSNorm, bf16 x[16384,16384] ~N(0,1), w ~N(1,0.1), eps 2^-17"),
+    "n4": Workload("n4", "layernorm", "bf16", 16384, 16384, x=Dist(NORMAL, 0.5, 1.0),
+                   w=Dist(NORMAL, 1.0, 0.1), b=Dist(NORMAL, 0.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0),
+                   eps=2.0 ** -17,
+                   note="LayerNorm, bf16 x[16384,16384] ~N(0.5,1), w ~N(1,0.1), b ~N(0,0.1), eps 2^-17"),
 }

@@ -242,7 +242,7 @@ def test_norm_cluster_no_wait_timeouts(wsf):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["n1", "n2"])
+@pytest.mark.parametrize("name", ["n1", "n2", "n3", "n4"])
 def test_norm_measurement_size(wsf, name):
     import inputgen
     from inputgen.workloads import WORKLOADS

@@ -174,10 +174,11 @@ def test_softmax_cluster_strides(wsf, dt):
 
 
 @pytest.mark.slow
-def test_softmax_measurement_size_sampled(wsf):
+@pytest.mark.parametrize("name", ["s1", "s2"])
+def test_softmax_measurement_size_sampled(wsf, name):
     import inputgen
     from inputgen.workloads import WORKLOADS
-    wl = WORKLOADS["s1"]
+    wl = WORKLOADS[name]
     x = inputgen.make((wl.N, wl.D), wl.dtype, wl.x.kind, wl.x.a, wl.x.b, 0, 0, pin=True)
     dy = inputgen.make((wl.N, wl.D), wl.dtype, wl.dy.kind, wl.dy.a, wl.dy.b, 0, 2, pin=True)
     xd, gd = x.to(DEV), dy.to(DEV)
