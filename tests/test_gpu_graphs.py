@@ -102,3 +102,52 @@ def test_capture_and_replay_match_eager(wsf):
         if k.endswith("_ws"):
             continue
         assert torch.equal(o[k], eager[k]), k
+
+
+def test_capture_cluster_paths(wsf):
+    # wide rows take thread-block clusters; run alone, this test makes the
+    # first use of the fp16 softmax cluster kernels inside the capture (their
+    # one-time occupancy query and kernel attributes happen there), while the
+    # bf16 norm kernels were used eagerly before
+    g = torch.Generator(device=DEV).manual_seed(1)
+    eps = 2.0 ** -17
+    x16 = torch.randn(64, 36000, device=DEV, generator=g).half()
+    dy16 = torch.randn(64, 36000, device=DEV, generator=g).half()
+    xb = torch.randn(300, 20000, device=DEV, generator=g).bfloat16()
+    dyb = torch.randn(300, 20000, device=DEV, generator=g).bfloat16()
+    wn = 1 + 0.1 * torch.randn(20000, device=DEV, generator=g)
+    bn = 0.1 * torch.randn(20000, device=DEV, generator=g)
+    wsf.rmsnorm_fwd(xb, wn, eps)
+    wsf.layernorm_bwd(xb, wn, dyb, eps)
+    torch.cuda.synchronize()
+
+    def outs():
+        return {"ym": torch.empty_like(x16), "dxm": torch.empty_like(x16),
+                "yn": torch.empty_like(xb), "dxn": torch.empty_like(xb),
+                "gw": torch.empty(20000, device=DEV), "gb": torch.empty(20000, device=DEV),
+                "ws": torch.empty(wsf.norm_bwd_workspace_bytes(300, 20000, torch.bfloat16, True),
+                                  dtype=torch.uint8, device=DEV)}
+
+    def step(o, s):
+        wsf.softmax_fwd(x16, y=o["ym"], stream=s)
+        wsf.softmax_bwd(o["ym"], dy16, dx=o["dxm"], stream=s)
+        wsf.layernorm_fwd(xb, wn, bn, eps, y=o["yn"], stream=s)
+        wsf.layernorm_bwd(xb, wn, dyb, eps, dx=o["dxn"], grad_w=o["gw"], grad_b=o["gb"],
+                          workspace=o["ws"], stream=s)
+
+    s = torch.cuda.Stream(device=DEV)
+    o = outs()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        step(o, s)
+    gr.replay()
+    torch.cuda.synchronize()
+    eager = outs()
+    with torch.cuda.stream(s):
+        step(eager, s)
+    s.synchronize()
+    for k in eager:
+        if k != "ws":
+            assert torch.equal(o[k], eager[k]), k
+    assert wsf.cluster_wait_timeouts() == 0
