@@ -158,23 +158,91 @@ struct RowStage {
     static constexpr size_t bytes(int arrays) { return (size_t)arrays * S * CPT * NT * 16; }
 };
 
-template <typename T, int TPR, int CPT, int NT>
+// A row of D elements as 16-byte chunks.  Aligned rows (U = false) start at
+// their first element.  Otherwise (U) the chunks start at the row's first
+// element rounded down to 16 bytes, off = that element's place in chunk 0:
+// chunk c holds the row's elements c·V − off … c·V − off + V − 1, and those
+// outside [0, D) are masked (reads of the masked elements stay inside the
+// 16-byte blocks that hold the row's own elements).  Every array of a call
+// has the same offset in each row (checked by the launcher).
+template <typename T, bool U>
+__device__ __forceinline__ int win_off(const T* row_start) {
+    if constexpr (U)
+        return (int)(((uintptr_t)row_start & 15u) / sizeof(T));
+    else
+        return 0;
+}
+
+// Row window of a thread's chunk cc (= chunk index in the row): any element
+// of the row, only elements of the row, element v of the row.
+template <typename T, bool U>
+struct Win {
+    static constexpr int V = Elt<T>::V;
+    int off, D;
+    __device__ __forceinline__ bool has(int cc) const {
+        return U ? cc * V < off + D : cc * V < D;
+    }
+    __device__ __forceinline__ bool full(int cc) const {
+        return !U || (cc * V >= off && (cc + 1) * V <= off + D);
+    }
+    __device__ __forceinline__ bool elt(int cc, int v) const {
+        const int j = cc * V + v - off;
+        return !U || (j >= 0 && j < D);
+    }
+    // first element of chunk cc, relative to the row's first element
+    __device__ __forceinline__ int64_t at(int cc) const { return (int64_t)cc * V - off; }
+};
+
+template <typename T, int TPR, int CPT, int NT, bool U>
 __device__ __forceinline__ void stage_row(Raw16* slots, const T* __restrict__ p, int64_t ld,
-                                          int64_t row, int64_t N, int Dv, int l) {
+                                          int64_t row, int64_t N, int D, int l) {
     constexpr int V = Elt<T>::V;
+    const bool rok = row < N;
+    const T* rp = p + (rok ? row : 0) * ld;
+    const int off = win_off<T, U>(rp);
+    const T* base = rp - off;
+    const int nc = (off + D + V - 1) / V;  // D / V for aligned rows
 #pragma unroll
     for (int k = 0; k < CPT; k++) {
         const int c = l + k * TPR;
-        const bool ok = row < N && c < Dv;
+        const bool ok = rok && c < nc;
         cp_async16(&slots[k * NT + threadIdx.x],
-                   ok ? (const void*)(p + row * ld + (int64_t)c * V) : (const void*)p, ok ? 16 : 0);
+                   ok ? (const void*)(base + (int64_t)c * V) : (const void*)p, ok ? 16 : 0);
     }
 }
 
-template <typename T, int TPR, int CPT, int NT, int S>
+// The 16-bit lanes of a chunk outside [lo, hi) set to −inf (for the packed
+// maximum).
+template <typename T>
+__device__ __forceinline__ Raw16 mask_ninf(Raw16 r, int lo, int hi) {
+    constexpr uint32_t ninf = std::is_same<T, __half>::value ? 0xFC00u : 0xFF80u;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        if (2 * i < lo || 2 * i >= hi) r.u[i] = (r.u[i] & 0xFFFF0000u) | ninf;
+        if (2 * i + 1 < lo || 2 * i + 1 >= hi) r.u[i] = (r.u[i] & 0x0000FFFFu) | (ninf << 16);
+    }
+    return r;
+}
+
+// Store chunk cc of a row: one 16-byte store for a full chunk, else the
+// row's elements one by one.
+template <typename T, bool U>
+__device__ __forceinline__ void store_chunk(T* row_start, const Win<T, U>& w, int cc,
+                                            const float (&o)[Elt<T>::V]) {
+    using E = Elt<T>;
+    if (w.full(cc)) {
+        st_stream(row_start + w.at(cc), E::narrow(o));
+    } else {
+#pragma unroll
+        for (int v = 0; v < E::V; v++)
+            if (w.elt(cc, v)) E::store1(row_start + w.at(cc) + v, o[v]);
+    }
+}
+
+template <typename T, int TPR, int CPT, int NT, int S, bool U>
 __global__ void __launch_bounds__(NT)
     softmax_fwd_rows(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
-                     int64_t N, int Dv) {
+                     int64_t N, int D) {
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int R = NT / TPR;
@@ -189,24 +257,37 @@ __global__ void __launch_bounds__(NT)
     const int64_t iters = ((int64_t)blockIdx.x * R < N) ? (N - (int64_t)blockIdx.x * R + stride - 1) / stride : 0;
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
-        if (k < iters) stage_row<T, TPR, CPT, NT>(slots + k * CPT * NT, x, ldx, first + k * stride, N, Dv, l);
+        if (k < iters) stage_row<T, TPR, CPT, NT, U>(slots + k * CPT * NT, x, ldx, first + k * stride, N, D, l);
         cp_async_commit();
     }
     for (int64_t k = 0; k < iters; k++) {
         cp_async_wait<S - 2>();
         const int64_t nk = k + S - 1;
         if (nk < iters)
-            stage_row<T, TPR, CPT, NT>(slots + (nk % S) * CPT * NT, x, ldx, first + nk * stride, N, Dv, l);
+            stage_row<T, TPR, CPT, NT, U>(slots + (nk % S) * CPT * NT, x, ldx, first + nk * stride, N, D, l);
         cp_async_commit();
         const int64_t row = first + k * stride;
         const bool rok = row < N;
-        const Raw16* cur = slots + (k % S) * CPT * NT;
+        Raw16* cur = slots + (k % S) * CPT * NT;
+        const Win<T, U> win{rok ? win_off<T, U>(x + row * ldx) : 0, D};
+        T* yrow = y + (rok ? row : 0) * ldy;
         if constexpr (!kComp) {
-            // 16-bit storage: packed max, one FMA + ex2 per element, plain sums
+            // 16-bit storage: packed max, one FMA + ex2 per element, plain
+            // sums; an edge chunk of a windowed row gets −inf outside the row
+            // (in the thread's own slot), whose exponential is 0
             float m = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < CPT; c++)
-                if (rok && l + c * TPR < Dv) m = fmaxf(m, chunk_max16<T>(cur[c * NT + threadIdx.x]));
+            for (int c = 0; c < CPT; c++) {
+                const int cc = l + c * TPR;
+                if (rok && win.has(cc)) {
+                    Raw16 r = cur[c * NT + threadIdx.x];
+                    if (!win.full(cc)) {
+                        r = mask_ninf<T>(r, win.off - cc * V, win.off + D - cc * V);
+                        cur[c * NT + threadIdx.x] = r;
+                    }
+                    m = fmaxf(m, chunk_max16<T>(r));
+                }
+            }
             m = group_max<TPR>(m, redm);
             const float ms = m * kLog2e;
             float f[CPT][V];
@@ -214,7 +295,7 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
                 E::widen(cur[c * NT + threadIdx.x], f[c]);
-                const bool ok = rok && l + c * TPR < Dv;
+                const bool ok = rok && win.has(l + c * TPR);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
                     f[c][v] = ok ? exp2_approx(fmaf(f[c][v], kLog2e, -ms)) : 0.f;
@@ -224,11 +305,12 @@ __global__ void __launch_bounds__(NT)
             const float inv = 1.0f / group_sum_plain<TPR>(st, redm);
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
-                if (rok && l + c * TPR < Dv) {
+                const int cc = l + c * TPR;
+                if (rok && win.has(cc)) {
                     float o[V];
 #pragma unroll
                     for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
-                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                    store_chunk<T, U>(yrow, win, cc, o);
                 }
             }
         } else {
@@ -237,21 +319,27 @@ __global__ void __launch_bounds__(NT)
             bool cok[CPT];
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
-                cok[c] = rok && l + c * TPR < Dv;
+                cok[c] = rok && win.has(l + c * TPR);
                 E::widen(cur[c * NT + threadIdx.x], f[c]);
             }
             float m = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < CPT; c++)
+            for (int c = 0; c < CPT; c++) {
+                if (cok[c] && !win.full(l + c * TPR))  // edge chunk: −inf outside the row
+#pragma unroll
+                    for (int v = 0; v < V; v++)
+                        if (!win.elt(l + c * TPR, v)) f[c][v] = -INFINITY;
                 if (cok[c])
 #pragma unroll
                     for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
+            }
             m = group_max<TPR>(m, redm);
             Acc2 s = acc2_zero();
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
 #pragma unroll
                 for (int v = 0; v < V; v++) {
+                    // exp(−inf − m) = 0 outside the row
                     f[c][v] = cok[c] ? exp_diff<kSoftmaxFast<T>>(f[c][v], m) : 0.f;
                     add_to<kComp>(s, f[c][v]);
                 }
@@ -264,7 +352,7 @@ __global__ void __launch_bounds__(NT)
                     float o[V];
 #pragma unroll
                     for (int v = 0; v < V; v++) o[v] = f[c][v] * inv;
-                    st_stream(y + row * ldy + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                    store_chunk<T, U>(yrow, win, l + c * TPR, o);
                 }
             }
         }
@@ -273,10 +361,10 @@ __global__ void __launch_bounds__(NT)
     pdl_trigger();
 }
 
-template <typename T, int TPR, int CPT, int NT, int S>
+template <typename T, int TPR, int CPT, int NT, int S, bool U>
 __global__ void __launch_bounds__(NT)
     softmax_bwd_rows(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy, int64_t lddy,
-                     T* __restrict__ dx, int64_t lddx, int64_t N, int Dv) {
+                     T* __restrict__ dx, int64_t lddx, int64_t N, int D) {
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int R = NT / TPR;
@@ -293,8 +381,8 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
         if (k < iters) {
-            stage_row<T, TPR, CPT, NT>(ys + k * CPT * NT, y, ldy, first + k * stride, N, Dv, l);
-            stage_row<T, TPR, CPT, NT>(gs + k * CPT * NT, dy, lddy, first + k * stride, N, Dv, l);
+            stage_row<T, TPR, CPT, NT, U>(ys + k * CPT * NT, y, ldy, first + k * stride, N, D, l);
+            stage_row<T, TPR, CPT, NT, U>(gs + k * CPT * NT, dy, lddy, first + k * stride, N, D, l);
         }
         cp_async_commit();
     }
@@ -302,31 +390,37 @@ __global__ void __launch_bounds__(NT)
         cp_async_wait<S - 2>();
         const int64_t nk = k + S - 1;
         if (nk < iters) {
-            stage_row<T, TPR, CPT, NT>(ys + (nk % S) * CPT * NT, y, ldy, first + nk * stride, N, Dv, l);
-            stage_row<T, TPR, CPT, NT>(gs + (nk % S) * CPT * NT, dy, lddy, first + nk * stride, N, Dv, l);
+            stage_row<T, TPR, CPT, NT, U>(ys + (nk % S) * CPT * NT, y, ldy, first + nk * stride, N, D, l);
+            stage_row<T, TPR, CPT, NT, U>(gs + (nk % S) * CPT * NT, dy, lddy, first + nk * stride, N, D, l);
         }
         cp_async_commit();
         const int64_t row = first + k * stride;
         const bool rok = row < N;
         const Raw16* cy = ys + (k % S) * CPT * NT;
         const Raw16* cg = gs + (k % S) * CPT * NT;
+        const Win<T, U> win{rok ? win_off<T, U>(y + row * ldy) : 0, D};
         float fy[CPT][V], fg[CPT][V];
         bool cok[CPT];
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            cok[c] = rok && l + c * TPR < Dv;
+            cok[c] = rok && win.has(l + c * TPR);
             E::widen(cy[c * NT + threadIdx.x], fy[c]);
             E::widen(cg[c * NT + threadIdx.x], fg[c]);
+            if (U && !win.full(l + c * TPR))
+#pragma unroll
+                for (int v = 0; v < V; v++)
+                    if (!win.elt(l + c * TPR, v)) fy[c][v] = fg[c][v] = 0.f;
         }
         Acc2 s = acc2_zero();
 #pragma unroll
         for (int c = 0; c < CPT; c++)
 #pragma unroll
             for (int v = 0; v < V; v++) {
+                const float a = cok[c] ? fg[c][v] : 0.f, b = cok[c] ? fy[c][v] : 0.f;
                 if constexpr (kComp)
-                    acc2_fma(s, fg[c][v], fy[c][v]);
+                    acc2_fma(s, a, b);
                 else
-                    s.hi = fmaf(fg[c][v], fy[c][v], s.hi);
+                    s.hi = fmaf(a, b, s.hi);
             }
         float sv;
         if constexpr (kComp) {
@@ -335,13 +429,14 @@ __global__ void __launch_bounds__(NT)
         } else {
             sv = group_sum_plain<TPR>(s.hi, redf);
         }
+        T* dxrow = dx + (rok ? row : 0) * lddx;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (cok[c]) {
                 float o[V];
 #pragma unroll
                 for (int v = 0; v < V; v++) o[v] = fy[c][v] * (fg[c][v] - sv);
-                st_stream(dx + row * lddx + (int64_t)(l + c * TPR) * V, E::narrow(o));
+                store_chunk<T, U>(dxrow, win, l + c * TPR, o);
             }
         }
     }
@@ -449,10 +544,10 @@ __device__ __forceinline__ float rescale(float a, float b) {
     else return exp2_approx(fmaf(a, kLog2e, -b * kLog2e));
 }
 
-template <typename T, int NT, int S>
+template <typename T, int NT, int S, bool U>
 __global__ void __launch_bounds__(NT, 1024 / NT)
     softmax_fwd_cluster(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
-                        int64_t N, int Dv) {
+                        int64_t N, int D) {
     using E = Elt<T>;
     constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
     constexpr bool kComp = std::is_same<T, float>::value;
@@ -472,27 +567,40 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     pdl_wait();
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
-        if (k < iters) stage_row<T, NT, CPT, NT>(slots + k * CPT * NT, x, ldx, cid + k * ncl, N, Dv, l);
+        if (k < iters) stage_row<T, NT, CPT, NT, U>(slots + k * CPT * NT, x, ldx, cid + k * ncl, N, D, l);
         cp_async_commit();
     }
     for (int64_t k = 0; k < iters; k++) {
         cp_async_wait<S - 2>();
         const int64_t nk = k + S - 1;
         if (nk < iters)
-            stage_row<T, NT, CPT, NT>(slots + (nk % S) * CPT * NT, x, ldx, cid + nk * ncl, N, Dv, l);
+            stage_row<T, NT, CPT, NT, U>(slots + (nk % S) * CPT * NT, x, ldx, cid + nk * ncl, N, D, l);
         cp_async_commit();
         const int64_t row = cid + k * ncl;
-        const Raw16* cur = slots + (k % S) * CPT * NT;
+        Raw16* cur = slots + (k % S) * CPT * NT;
+        const Win<T, U> win{win_off<T, U>(x + row * ldx), D};
         // the warp's maximum and its sum of exp(x − m_w)
         float f[CPT][V];
         float m = -INFINITY;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            if (l + c * NT < Dv) {
+            const int cc = l + c * NT;
+            if (win.has(cc)) {
                 if constexpr (!kComp) {
-                    m = fmaxf(m, chunk_max16<T>(cur[c * NT + threadIdx.x]));
+                    // an edge chunk gets −inf outside the row (in the
+                    // thread's own slot), whose exponential is 0
+                    Raw16 r = cur[c * NT + threadIdx.x];
+                    if (!win.full(cc)) {
+                        r = mask_ninf<T>(r, win.off - cc * V, win.off + D - cc * V);
+                        cur[c * NT + threadIdx.x] = r;
+                    }
+                    m = fmaxf(m, chunk_max16<T>(r));
                 } else {
                     E::widen(cur[c * NT + threadIdx.x], f[c]);
+                    if (!win.full(cc))  // edge chunk: −inf outside the row
+#pragma unroll
+                        for (int v = 0; v < V; v++)
+                            if (!win.elt(cc, v)) f[c][v] = -INFINITY;
 #pragma unroll
                     for (int v = 0; v < V; v++) m = fmaxf(m, f[c][v]);
                 }
@@ -508,7 +616,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
                 E::widen(cur[c * NT + threadIdx.x], f[c]);
-                const bool ok = l + c * NT < Dv;
+                const bool ok = win.has(l + c * NT);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
                     f[c][v] = ok ? exp2_approx(fmaf(f[c][v], kLog2e, -ms)) : 0.f;
@@ -519,9 +627,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
         } else {
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
-                const bool ok = l + c * NT < Dv;
+                const bool ok = win.has(l + c * NT);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
+                    // exp(−inf − m) = 0 outside the row
                     f[c][v] = ok ? exp_diff<false>(f[c][v], m) : 0.f;
                     add_to<true>(s, f[c][v]);
                 }
@@ -560,13 +669,15 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
         __syncthreads();
         const float2 Mi = *out;
         const float sc = rescale<kComp>(m, Mi.x) * Mi.y;
+        T* yrow = y + row * ldy;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            if (l + c * NT < Dv) {
+            const int cc = l + c * NT;
+            if (win.has(cc)) {
                 float o[V];
 #pragma unroll
                 for (int v = 0; v < V; v++) o[v] = f[c][v] * sc;
-                st_stream(y + row * ldy + (int64_t)(l + c * NT) * V, E::narrow(o));
+                store_chunk<T, U>(yrow, win, cc, o);
             }
         }
     }
@@ -575,10 +686,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     pdl_trigger();
 }
 
-template <typename T, int NT, int S>
+template <typename T, int NT, int S, bool U>
 __global__ void __launch_bounds__(NT)
     softmax_bwd_cluster(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy,
-                        int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int Dv) {
+                        int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int D) {
     using E = Elt<T>;
     constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
     constexpr bool kComp = std::is_same<T, float>::value;
@@ -600,8 +711,8 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
     for (int k = 0; k < S - 1; k++) {
         if (k < iters) {
-            stage_row<T, NT, CPT, NT>(ys + k * CPT * NT, y, ldy, cid + k * ncl, N, Dv, l);
-            stage_row<T, NT, CPT, NT>(gs + k * CPT * NT, dy, lddy, cid + k * ncl, N, Dv, l);
+            stage_row<T, NT, CPT, NT, U>(ys + k * CPT * NT, y, ldy, cid + k * ncl, N, D, l);
+            stage_row<T, NT, CPT, NT, U>(gs + k * CPT * NT, dy, lddy, cid + k * ncl, N, D, l);
         }
         cp_async_commit();
     }
@@ -609,20 +720,30 @@ __global__ void __launch_bounds__(NT)
         cp_async_wait<S - 2>();
         const int64_t nk = k + S - 1;
         if (nk < iters) {
-            stage_row<T, NT, CPT, NT>(ys + (nk % S) * CPT * NT, y, ldy, cid + nk * ncl, N, Dv, l);
-            stage_row<T, NT, CPT, NT>(gs + (nk % S) * CPT * NT, dy, lddy, cid + nk * ncl, N, Dv, l);
+            stage_row<T, NT, CPT, NT, U>(ys + (nk % S) * CPT * NT, y, ldy, cid + nk * ncl, N, D, l);
+            stage_row<T, NT, CPT, NT, U>(gs + (nk % S) * CPT * NT, dy, lddy, cid + nk * ncl, N, D, l);
         }
         cp_async_commit();
         const int64_t row = cid + k * ncl;
         const Raw16* cy = ys + (k % S) * CPT * NT;
         const Raw16* cg = gs + (k % S) * CPT * NT;
+        const Win<T, U> win{win_off<T, U>(y + row * ldy), D};
+        // y and dy of chunk cc, zero outside the row
+        auto load = [&](int c, int cc, float (&fy)[V], float (&fg)[V]) {
+            E::widen(cy[c * NT + threadIdx.x], fy);
+            E::widen(cg[c * NT + threadIdx.x], fg);
+            if (!win.full(cc))
+#pragma unroll
+                for (int v = 0; v < V; v++)
+                    if (!win.elt(cc, v)) fy[v] = fg[v] = 0.f;
+        };
         Acc2 s = acc2_zero();
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            if (l + c * NT < Dv) {
+            const int cc = l + c * NT;
+            if (win.has(cc)) {
                 float fy[V], fg[V];
-                E::widen(cy[c * NT + threadIdx.x], fy);
-                E::widen(cg[c * NT + threadIdx.x], fg);
+                load(c, cc, fy, fg);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
                     if constexpr (kComp)
@@ -660,15 +781,16 @@ __global__ void __launch_bounds__(NT)
         }
         __syncthreads();
         const float sv = *out;
+        T* dxrow = dx + row * lddx;
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
-            if (l + c * NT < Dv) {
+            const int cc = l + c * NT;
+            if (win.has(cc)) {
                 float fy[V], fg[V], o[V];
-                E::widen(cy[c * NT + threadIdx.x], fy);
-                E::widen(cg[c * NT + threadIdx.x], fg);
+                load(c, cc, fy, fg);
 #pragma unroll
                 for (int v = 0; v < V; v++) o[v] = fy[v] * (fg[v] - sv);
-                st_stream(dx + row * lddx + (int64_t)(l + c * NT) * V, E::narrow(o));
+                store_chunk<T, U>(dxrow, win, cc, o);
             }
         }
     }
@@ -709,8 +831,19 @@ static cudaError_t with_rows(int64_t N, F&& go) {
 
 // Measured on GB300 for rows of 512 chunks (4096 bf16): forward 128 threads x
 // 4 chunks, backward 64 x 8, two stages; other widths follow the same idea.
-template <bool Fwd, typename F>
+// A windowed row spans one chunk more than its aligned width when it starts
+// inside a 16-byte block; widths just past a power of two then take one more
+// chunk a thread rather than twice the threads.
+template <bool Fwd, bool U = false, typename F>
 static cudaError_t dispatch_rows(int64_t Dv, int64_t N, F&& go) {
+    if constexpr (U) {
+        if (Dv > 64 && Dv <= 96) return with_rows<32, 3, 3>(N, go);
+        if (Dv > 128 && Dv <= 160) return with_rows<32, 5, 3>(N, go);
+        if (Dv > 256 && Dv <= 288) return with_rows<32, 9, 2>(N, go);
+        if (Fwd && Dv > 512 && Dv <= 640) return with_rows<128, 5, 2>(N, go);
+        if (!Fwd && Dv > 512 && Dv <= 576) return with_rows<64, 9, 2>(N, go);
+        if (Dv > 1024 && Dv <= 1152) return with_rows<128, 9, 2>(N, go);
+    }
     if (Dv <= 32) {
         switch (next_pow2(Dv)) {
             case 1: return with_rows<1, 1, 4>(N, go);
@@ -737,9 +870,9 @@ static cudaError_t dispatch_rows(int64_t Dv, int64_t N, F&& go) {
 // CTAs, wider rows 512-thread CTAs, up to 16 a cluster (32768 chunks, 512 KB).
 constexpr int64_t kClusterRowChunks = (int64_t)kClusterMaxCS * 512 * kClusterCPT;
 
-static void cluster_shape(int64_t Dv, int& nt, unsigned& cs) {
-    nt = Dv <= 8 * 256 * kClusterCPT ? 256 : 512;
-    cs = (unsigned)cdiv(Dv, (int64_t)nt * kClusterCPT);
+static void cluster_shape(int64_t Dc, int& nt, unsigned& cs) {
+    nt = Dc <= 8 * 256 * kClusterCPT ? 256 : 512;
+    cs = (unsigned)cdiv(Dc, (int64_t)nt * kClusterCPT);
 }
 
 // Launch `kernel` as clusters of cs CTAs, as many clusters as the device
@@ -755,60 +888,100 @@ static cudaError_t go_cluster(int nt, unsigned cs, size_t smem, int64_t N, cudaS
     return launch_cluster(kernel, clusters, cs, dim3(nt), smem, s, std::forward<Args>(args)...);
 }
 
-template <typename T>
+template <typename T, bool U>
 static cudaError_t softmax_fwd_cluster_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
-                                         int64_t Dv, cudaStream_t s) {
+                                         int64_t D, int64_t Dc, cudaStream_t s) {
     int nt;
     unsigned cs;
-    cluster_shape(Dv, nt, cs);
+    cluster_shape(Dc, nt, cs);
     if (nt == 256) {
         constexpr int S = 3;
-        return go_cluster<softmax_fwd_cluster<T, 256, S>>(256, cs,
-                          (size_t)S * kClusterCPT * 256 * 16, N, s, x, ldx, y, ldy, N, (int)Dv);
+        return go_cluster<softmax_fwd_cluster<T, 256, S, U>>(
+            256, cs, (size_t)S * kClusterCPT * 256 * 16, N, s, x, ldx, y, ldy, N, (int)D);
     }
     constexpr int S = 2;
-    return go_cluster<softmax_fwd_cluster<T, 512, S>>(512, cs, (size_t)S * kClusterCPT * 512 * 16,
-                      N, s, x, ldx, y, ldy, N, (int)Dv);
+    return go_cluster<softmax_fwd_cluster<T, 512, S, U>>(
+        512, cs, (size_t)S * kClusterCPT * 512 * 16, N, s, x, ldx, y, ldy, N, (int)D);
 }
 
-template <typename T>
+template <typename T, bool U>
 static cudaError_t softmax_bwd_cluster_t(const T* y, int64_t ldy, const T* dy, int64_t lddy, T* dx,
-                                         int64_t lddx, int64_t N, int64_t Dv, cudaStream_t s) {
+                                         int64_t lddx, int64_t N, int64_t D, int64_t Dc,
+                                         cudaStream_t s) {
     int nt;
     unsigned cs;
-    cluster_shape(Dv, nt, cs);
+    cluster_shape(Dc, nt, cs);
     constexpr int S = 2;
     if (nt == 256)
-        return go_cluster<softmax_bwd_cluster<T, 256, S>>(256, cs,
-                          (size_t)2 * S * kClusterCPT * 256 * 16, N, s, y, ldy, dy, lddy, dx, lddx,
-                          N, (int)Dv);
-    return go_cluster<softmax_bwd_cluster<T, 512, S>>(512, cs,
-                      (size_t)2 * S * kClusterCPT * 512 * 16, N, s, y, ldy, dy, lddy, dx, lddx, N,
-                      (int)Dv);
+        return go_cluster<softmax_bwd_cluster<T, 256, S, U>>(
+            256, cs, (size_t)2 * S * kClusterCPT * 256 * 16, N, s, y, ldy, dy, lddy, dx, lddx, N,
+            (int)D);
+    return go_cluster<softmax_bwd_cluster<T, 512, S, U>>(
+        512, cs, (size_t)2 * S * kClusterCPT * 512 * 16, N, s, y, ldy, dy, lddy, dx, lddx, N,
+        (int)D);
+}
+
+// Row layouts of the vector paths: aligned (every array's rows start on 16
+// bytes, D a whole number of chunks), or windowed (U: the arrays' rows share
+// their offset inside a 16-byte block, row by row).  Dc = chunks a row spans
+// (at most, for windowed rows).
+template <typename T>
+static bool aligned_rows(const void* p, int64_t ld) {
+    return aligned16(p) && (ld * (int64_t)sizeof(T)) % 16 == 0;
+}
+template <typename T>
+static bool same_offsets(const void* a, int64_t lda, const void* b, int64_t ldb) {
+    return (((uintptr_t)a - (uintptr_t)b) & 15u) == 0 &&
+           ((lda - ldb) * (int64_t)sizeof(T)) % 16 == 0;
+}
+
+template <typename T, bool U>
+static cudaError_t softmax_fwd_vec(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
+                                   int64_t D, int64_t Dc, cudaStream_t s) {
+    if (Dc <= kSoftmaxRowChunks) {
+        return dispatch_rows<true, U>(Dc, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
+            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+            constexpr int S = decltype(st)::value;
+            auto k = softmax_fwd_rows<T, TPR, CPT, 256, S, U>;
+            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(1);
+            cudaError_t e = allow_smem_sm((const void*)k, smem);
+            if (e != cudaSuccess) return e;
+            return launch(k, grid, block, smem, s, true, x, ldx, y, ldy, N, (int)D);
+        });
+    }
+    if (Dc <= kClusterRowChunks && N > 0) return softmax_fwd_cluster_t<T, U>(x, ldx, y, ldy, N, D, Dc, s);
+    return cudaErrorNotSupported;
+}
+
+template <typename T, bool U>
+static cudaError_t softmax_bwd_vec(const T* y, int64_t ldy, const T* dy, int64_t lddy, T* dx,
+                                   int64_t lddx, int64_t N, int64_t D, int64_t Dc, cudaStream_t s) {
+    if (Dc <= kSoftmaxRowChunks) {
+        return dispatch_rows<false, U>(Dc, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
+            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
+            constexpr int S = decltype(st)::value;
+            auto k = softmax_bwd_rows<T, TPR, CPT, 256, S, U>;
+            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(2);
+            cudaError_t e = allow_smem_sm((const void*)k, smem);
+            if (e != cudaSuccess) return e;
+            return launch(k, grid, block, smem, s, true, y, ldy, dy, lddy, dx, lddx, N, (int)D);
+        });
+    }
+    if (Dc <= kClusterRowChunks && N > 0)
+        return softmax_bwd_cluster_t<T, U>(y, ldy, dy, lddy, dx, lddx, N, D, Dc, s);
+    return cudaErrorNotSupported;
 }
 
 template <typename T>
 static cudaError_t softmax_fwd_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N, int64_t D,
                                  cudaStream_t s) {
     constexpr int V = Elt<T>::V;
-    const int64_t Dv = D / V;
-    if (D % V == 0 && ldx % V == 0 && ldy % V == 0 && aligned16(x) && aligned16(y) &&
-        Dv <= kSoftmaxRowChunks) {
-        return dispatch_rows<true>(Dv, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
-            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
-            constexpr int S = decltype(st)::value;
-            auto k = softmax_fwd_rows<T, TPR, CPT, 256, S>;
-            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(1);
-            cudaError_t e = allow_smem_sm((const void*)k, smem);
-            if (e != cudaSuccess) return e;
-            return launch(k, grid, block, smem, s, true, x, ldx, y, ldy, N, (int)Dv);
-        });
-    }
-    if (D % V == 0 && ldx % V == 0 && ldy % V == 0 && aligned16(x) && aligned16(y) &&
-        Dv <= kClusterRowChunks && N > 0) {
-        const cudaError_t e = softmax_fwd_cluster_t(x, ldx, y, ldy, N, Dv, s);
-        if (e != cudaErrorNotSupported) return e;
-    }
+    cudaError_t e = cudaErrorNotSupported;
+    if (D % V == 0 && aligned_rows<T>(x, ldx) && aligned_rows<T>(y, ldy))
+        e = softmax_fwd_vec<T, false>(x, ldx, y, ldy, N, D, D / V, s);
+    else if (same_offsets<T>(x, ldx, y, ldy))
+        e = softmax_fwd_vec<T, true>(x, ldx, y, ldy, N, D, (D + 2 * V - 2) / V, s);
+    if (e != cudaErrorNotSupported) return e;
     constexpr int NT = 256;
     return launch(softmax_fwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
                   dim3(NT), 0, s, true, x, ldx, y, ldy, N, D);
@@ -818,24 +991,13 @@ template <typename T>
 static cudaError_t softmax_bwd_t(const T* y, int64_t ldy, const T* dy, int64_t lddy, T* dx,
                                  int64_t lddx, int64_t N, int64_t D, cudaStream_t s) {
     constexpr int V = Elt<T>::V;
-    const int64_t Dv = D / V;
-    if (D % V == 0 && ldy % V == 0 && lddy % V == 0 && lddx % V == 0 && aligned16(y) &&
-        aligned16(dy) && aligned16(dx) && Dv <= kSoftmaxRowChunks) {
-        return dispatch_rows<false>(Dv, N, [&](auto tpr, auto cpt, auto st, dim3 grid, dim3 block) {
-            constexpr int TPR = decltype(tpr)::value, CPT = decltype(cpt)::value;
-            constexpr int S = decltype(st)::value;
-            auto k = softmax_bwd_rows<T, TPR, CPT, 256, S>;
-            const size_t smem = RowStage<TPR, CPT, 256, S>::bytes(2);
-            cudaError_t e = allow_smem_sm((const void*)k, smem);
-            if (e != cudaSuccess) return e;
-            return launch(k, grid, block, smem, s, true, y, ldy, dy, lddy, dx, lddx, N, (int)Dv);
-        });
-    }
-    if (D % V == 0 && ldy % V == 0 && lddy % V == 0 && lddx % V == 0 && aligned16(y) &&
-        aligned16(dy) && aligned16(dx) && Dv <= kClusterRowChunks && N > 0) {
-        const cudaError_t e = softmax_bwd_cluster_t(y, ldy, dy, lddy, dx, lddx, N, Dv, s);
-        if (e != cudaErrorNotSupported) return e;
-    }
+    cudaError_t e = cudaErrorNotSupported;
+    if (D % V == 0 && aligned_rows<T>(y, ldy) && aligned_rows<T>(dy, lddy) &&
+        aligned_rows<T>(dx, lddx))
+        e = softmax_bwd_vec<T, false>(y, ldy, dy, lddy, dx, lddx, N, D, D / V, s);
+    else if (same_offsets<T>(y, ldy, dy, lddy) && same_offsets<T>(y, ldy, dx, lddx))
+        e = softmax_bwd_vec<T, true>(y, ldy, dy, lddy, dx, lddx, N, D, (D + 2 * V - 2) / V, s);
+    if (e != cudaErrorNotSupported) return e;
     constexpr int NT = 256;
     return launch(softmax_bwd_wide<T, NT>, dim3((unsigned)std::min<int64_t>(N, 8 * kDesignSMs)),
                   dim3(NT), 0, s, true, y, ldy, dy, lddy, dx, lddx, N, D);

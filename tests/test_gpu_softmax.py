@@ -2,7 +2,9 @@
 register rows of every width class, cluster rows (clusters of 3 to 16 CTAs,
 both CTA widths, ragged last slices, more rows than resident clusters), the
 element-wise wide/unaligned path, masked (−inf) logits, row strides, guard
-bands, bit reproducibility, and sampled rows at the measurement size."""
+bands, windowed rows (odd widths and shifted pointers read as the 16-byte
+chunks that cover each row, edges masked), arrays at mixed offsets, bit
+reproducibility, and sampled rows at the measurement size."""
 import numpy as np
 import pytest
 import torch
@@ -154,6 +156,57 @@ def test_softmax_masked_logits(wsf, dt, N, D):
     _check(x, dy, y, dx, yin)
     for i, t in enumerate(keep):
         assert bool((y[i, t:] == 0).all()) and bool((dx[i, t:] == 0).all())
+
+
+# Windowed rows: rows that do not start on 16 bytes or whose width is not a
+# whole number of chunks, with every array at the same offset (contiguous
+# tensors of an odd width, or one shift shared by all); the chunks start at
+# each row's first element rounded down to 16 bytes and the edges are masked.
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D,pad,mis", [
+    (300, 1001, 0, 0),     # register rows, the offset changes from row to row
+    (64, 4097, 0, 0),
+    (37, 5, 0, 1),         # tiny rows, every row shifted by one element
+    (40, 1024, 3, 1),
+    (33, 4096, 0, 1),      # one chunk past a power of two: one more chunk a thread
+    (21, 2048, 0, 1),
+    (30, 512, 0, 1),
+    (50, 50257, 0, 0),     # a GPT-2-sized vocabulary: cluster rows
+    (9, 100003, 5, 1),
+    (3, 262150, 0, 0),     # wider than the cluster rows (element-wise path)
+])
+def test_softmax_windowed_rows(wsf, dt, N, D, pad, mis):
+    x, dy = _inputs(N, D, dt, seed=D % 89)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin, pad=pad, mis=mis)
+    _check(x, dy, y, dx, yin)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [1000, 40000])
+def test_softmax_mixed_offsets(wsf, dt, D):
+    # arrays at different offsets within their 16-byte blocks take the
+    # element-wise path
+    N = 20
+    x, dy = _inputs(N, D, dt, seed=5)
+    _, yin = oracle.softmax_fwd(x)
+
+    def at(t, shift):
+        b = torch.zeros(N * D + 16, dtype=t.dtype, device=DEV)
+        v = b[shift:shift + N * D].view(N, D)
+        v.copy_(t.to(DEV))
+        return v
+
+    yb = torch.full((N * D + 16,), 7.0, dtype=x.dtype, device=DEV)
+    y = yb[2:2 + N * D].view(N, D)
+    dxb = torch.full((N * D + 16,), 7.0, dtype=x.dtype, device=DEV)
+    dxv = dxb[3:3 + N * D].view(N, D)
+    wsf.softmax_fwd(at(x, 1), y=y)
+    wsf.softmax_bwd(at(yin, 0), at(dy, 1), dx=dxv)
+    torch.cuda.synchronize()
+    assert bool((yb[:2] == 7).all()) and bool((yb[2 + N * D:] == 7).all())
+    assert bool((dxb[:3] == 7).all()) and bool((dxb[3 + N * D:] == 7).all())
+    _check(x, dy, y.cpu(), dxv.cpu(), yin)
 
 
 def test_softmax_cluster_no_wait_timeouts(wsf):
