@@ -8,13 +8,17 @@
 // Forward:  y[i,j] = exp(x[i,j] − m_i) / Σ_k exp(x[i,k] − m_i),  m_i = max_k x[i,k]
 // Backward: dx[i,j] = y[i,j] · (dy[i,j] − s_i),  s_i = Σ_k dy[i,k]·y[i,k]
 //
-// Row path (16-byte aligned rows of up to 2048 chunks): a row is held in
-// registers by a group of TPR threads (CPT 16-byte chunks each); the row max
-// and the row sums are combined with xor butterflies inside a warp and, for
-// groups wider than a warp, through shared memory in warp order.  x (or y and
-// dy) is read once and y (dx) written once.  Wide or unaligned rows take a
-// multi-pass path with one CTA per row.  Sums of binary32 rows are
-// compensated and their exponents taken of exactly split differences.
+// Row path (rows of up to 2048 16-byte chunks): a row is held in registers
+// by a group of TPR threads (CPT chunks each); the row max and the row sums
+// are combined with xor butterflies inside a warp and, for groups wider than
+// a warp, through shared memory in warp order.  x (or y and dy) is read once
+// and y (dx) written once.  Rows of up to 32,768 chunks are split over a
+// thread-block cluster (below).  Rows that do not start on 16 bytes, or whose
+// width is not a whole number of chunks, are read as the chunks that cover
+// them, with the edges masked (Win), when every array of the call has the
+// same offset in each row; other rows take a multi-pass element-wise path
+// with one CTA per row.  Sums of binary32 rows are compensated and their
+// exponentials taken of exactly split differences.
 #include <algorithm>
 #include <type_traits>
 
