@@ -34,6 +34,10 @@ lib.wsf_version.argtypes = []
 lib.wsf_version.restype = _int
 lib.wsf_cluster_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint), _int]
 lib.wsf_cluster_wait_timeouts.restype = _int
+lib.wsf_selftest_exchange_timeout.argtypes = [_vp, ctypes.c_uint, _vp]
+lib.wsf_selftest_exchange_timeout.restype = _int
+lib.wsf_selftest_waiting_warps.argtypes = []
+lib.wsf_selftest_waiting_warps.restype = _int
 lib.ws_fwd.argtypes = [_vp, _i64, _vp, _vp, _i64, _i64, _int, _vp]
 lib.ws_fwd.restype = _int
 lib.ws_bwd_workspace_bytes.argtypes = [_i64, _i64, _int, _i64]
@@ -348,7 +352,22 @@ def cluster_wait_timeouts(reset: bool = False) -> int:
     return int(n.value)
 
 
-__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "cluster_wait_timeouts", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
+def selftest_exchange_timeout(count: torch.Tensor, limit_ms: int = 20, stream=None) -> None:
+    """Run the cluster exchange's bounded wait where nothing completes it:
+    adds selftest_waiting_warps() to the device int32/uint32 scalar `count`
+    once the stream reaches it (each waiting warp gives up after limit_ms)."""
+    if count.numel() != 1 or count.element_size() != 4 or not count.is_cuda:
+        raise TypeError("count must be a one-element 4-byte CUDA tensor")
+    _check(lib.wsf_selftest_exchange_timeout(_ptr(count), int(limit_ms), _stream(stream)),
+           "wsf_selftest_exchange_timeout")
+
+
+def selftest_waiting_warps() -> int:
+    return int(lib.wsf_selftest_waiting_warps())
+
+
+__all__ = ["lib", "LIB_PATH", "WsfError", "status_string", "cluster_wait_timeouts",
+           "selftest_exchange_timeout", "selftest_waiting_warps", "ws_fwd", "ws_bwd", "ws_bwd_noalloc",
            "ws_bwd_atomic", "silu_bwd_atomic", "softmax_fwd", "softmax_bwd", "silu_fwd",
            "silu_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "layernorm_fwd", "layernorm_bwd",
            "ws_bwd_workspace_bytes", "silu_bwd_workspace_bytes", "norm_bwd_workspace_bytes", "F32",

@@ -80,6 +80,16 @@ const char* wsf_status_string(int status) {
 
 int wsf_version(void) { return 100; }
 
+int wsf_selftest_exchange_timeout(unsigned* count, unsigned limit_ms, wsf_stream_t stream) {
+    if (!count) return WSF_ERR_NULL_PTR;
+    if (!aligned_to(count, 4)) return WSF_ERR_MISALIGNED;
+    if (limit_ms < 1 || limit_ms > 1000) return WSF_ERR_BAD_ARG;
+    return cuda_status(wsf::launch_exchange_timeout(count, (uint64_t)limit_ms * 1000000ull,
+                                                    (cudaStream_t)stream));
+}
+
+int wsf_selftest_waiting_warps(void) { return wsf::selftest_waiting_warps(); }
+
 int wsf_cluster_wait_timeouts(unsigned* count, int reset) {
     if (!count) return WSF_ERR_NULL_PTR;
     if (reset != 0 && reset != 1) return WSF_ERR_BAD_ARG;

@@ -351,8 +351,9 @@ __device__ __forceinline__ void st_async_f32x4(uint32_t dst, float4 v, uint32_t 
 // before every CTA has finished reading it, provided that each warp pushes
 // turn t + 1 only after this CTA's readers of turn t are done (the callers
 // put a CTA barrier between them) and that every turn is waited for by
-// thread 0.  A wait longer than a second marks the exchange dead for the
-// waiting thread (later waits are skipped) and counts a timeout, so that a
+// thread 0.  A wait longer than limit_ns (a second unless set) marks the
+// exchange dead for the waiting thread (later waits are skipped) and counts a
+// timeout (one a warp), so that a
 // fault in the protocol ends the kernel with wrong results and a raised
 // counter instead of a hang.  Each CTA of a cluster must run the same turns,
 // and every CTA's barriers must be initialised (init(), then a cluster
@@ -364,6 +365,7 @@ struct WarpPush {
     unsigned* timeouts;        // device counter of waits that ran out
     unsigned turn;
     bool live;
+    uint64_t limit_ns = 1000000000ull;  // how long a wait may take
 
     __device__ __forceinline__ void init() {
         if (threadIdx.x == 0) {
@@ -392,7 +394,7 @@ struct WarpPush {
 
     // Wait until turn t is complete; returns its buffer.
     __device__ __forceinline__ const float4 (*wait(unsigned t))[NV] {
-        if (live && !mbar_wait(&bar[t & 1u], (t >> 1) & 1u, 1000000000ull)) {
+        if (live && !mbar_wait(&bar[t & 1u], (t >> 1) & 1u, limit_ns)) {
             live = false;
             if ((threadIdx.x & 31u) == 0) atomicAdd(timeouts, 1u);
         }

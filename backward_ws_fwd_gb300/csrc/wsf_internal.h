@@ -60,6 +60,11 @@ cudaError_t launch_norm_bwd(const void* x, int64_t ldx, const float* w, const vo
 cudaError_t norm_wait_timeouts(unsigned* count, bool reset);
 cudaError_t softmax_wait_timeouts(unsigned* count, bool reset);
 
+// One cluster whose exchange wait nothing completes (selftest.cu): each
+// waiting warp adds one to *count (device memory) after limit_ns.
+cudaError_t launch_exchange_timeout(unsigned* count, uint64_t limit_ns, cudaStream_t s);
+int selftest_waiting_warps();
+
 cudaError_t launch_silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype,
                             cudaStream_t s);
 

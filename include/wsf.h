@@ -100,6 +100,24 @@ int wsf_version(void);
 int wsf_cluster_wait_timeouts(unsigned* count, int reset);
 
 /*
+ * wsf_selftest_exchange_timeout — runs the bounded wait of the cluster
+ * exchange where nothing completes it: one cluster of two CTAs posts the
+ * bytes an exchange turn expects and waits, but no CTA pushes any.  Every
+ * waiting warp gives up after limit_ms milliseconds and adds one to *count;
+ * the kernel then returns and the context stays usable.  count: device
+ * memory, one unsigned (4-byte aligned), owned by the caller, added to (zero
+ * it first); after the stream completes it holds wsf_selftest_waiting_warps()
+ * more than before.  limit_ms: 1..1000.  The counter that
+ * wsf_cluster_wait_timeouts reads is not touched.  Stream-ordered.
+ * Returns WSF_OK, WSF_ERR_NULL_PTR, WSF_ERR_MISALIGNED, WSF_ERR_BAD_ARG or
+ * WSF_ERR_CUDA.
+ */
+int wsf_selftest_exchange_timeout(unsigned* count, unsigned limit_ms, wsf_stream_t stream);
+
+/* Number of warps that wait in wsf_selftest_exchange_timeout (one timeout each). */
+int wsf_selftest_waiting_warps(void);
+
+/*
  * ws_fwd — weighted-sum forward  [WS §1, §2]
  *   y[i] = Σ_{d<D} x[i,d] · w[d]   for 0 <= i < N
  * x: [N, D] dtype, row stride ldx; w: [D] binary32; y: [N] dtype.

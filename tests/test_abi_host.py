@@ -35,6 +35,15 @@ def test_exports_every_declared_symbol(wsf):
         assert hasattr(wsf.lib, n), n
 
 
+def test_selftest_exchange_timeout_rejects(wsf):
+    f = wsf.lib.wsf_selftest_exchange_timeout
+    assert f(None, 20, None) == -1
+    assert f(ctypes.c_void_p(0x1002), 20, None) == -7  # not 4-byte aligned
+    assert f(ctypes.c_void_p(0x1000), 0, None) == -8
+    assert f(ctypes.c_void_p(0x1000), 1001, None) == -8
+    assert wsf.selftest_waiting_warps() == 4
+
+
 def test_cluster_wait_timeouts_rejects(wsf):
     n = ctypes.c_uint(7)
     assert wsf.lib.wsf_cluster_wait_timeouts(None, 0) == -1
