@@ -576,6 +576,10 @@ __global__ void __launch_bounds__(NT, MINB)
 // Every CTA of a cluster runs the same rows, hence the same exchanges.
 // ===========================================================================
 constexpr int kNormClusterNT = 256;
+// Rows of up to this many elements use CTAs of 128 threads (2048 elements,
+// clusters of up to 8, 6 CTAs an SM): at bf16 widths 12,288 / 16,384 this
+// measured 2-6% faster than 256 threads; at 32,768 (clusters of 16) slower.
+constexpr int64_t kNormClusterSmallMaxD = 16384;
 // backward stages (indexed by LayerNorm) and whether w sits in per-thread
 // shared-memory slots, for 16-bit and binary32 rows
 constexpr int kNormBwdStages16[2] = {3, 3};
@@ -696,7 +700,7 @@ __device__ __forceinline__ void center(float (&f)[CPT][V], unsigned valid, const
 }
 
 template <typename T, bool LN, int NT, int S>
-__global__ void __launch_bounds__(NT, 3)
+__global__ void __launch_bounds__(NT, 768 / NT)
     norm_fwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                      const float* __restrict__ b, float eps, T* __restrict__ y, int64_t ldy,
                      int64_t N, int Dv) {
@@ -806,7 +810,7 @@ __device__ __forceinline__ void tile_advance(TileCursor& c, int step, int P, int
 }
 
 template <typename T, bool LN, int NT, int S, bool WS>
-__global__ void __launch_bounds__(NT, 3)
+__global__ void __launch_bounds__(NT, 768 / NT)
     norm_bwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                      const T* __restrict__ dy, int64_t lddy, float eps, T* __restrict__ dx,
                      int64_t lddx, float* __restrict__ part, int64_t N, int Dv, int64_t P) {
@@ -1167,6 +1171,41 @@ static cudaError_t norm_shape(int64_t Dv, F&& go) {
     return pick(integral_constant<int, 512>{});
 }
 
+// Cluster launches with CTAs of NT threads (16 elements a thread);
+// cudaErrorNotSupported when no cluster of that shape fits.
+template <typename T, bool LN, int NT>
+static cudaError_t norm_fwd_cluster_go(const T* x, int64_t ldx, const float* w, const float* b,
+                                       float eps, T* y, int64_t ldy, int64_t N, int64_t Dv,
+                                       cudaStream_t s) {
+    constexpr int V = Elt<T>::V, S = kNormFwdStages[LN], CPT = 16 / V;
+    constexpr auto k = norm_fwd_cluster<T, LN, NT, S>;
+    const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
+    const size_t smem = (size_t)S * CPT * NT * 16;
+    int fit = 0;
+    const cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
+    if (e != cudaSuccess) return e;
+    return launch_cluster(k, (unsigned)std::min<int64_t>(N, fit), cs, dim3(NT), smem, s, x, ldx, w,
+                          b, eps, y, ldy, N, (int)Dv);
+}
+
+template <typename T, bool LN, int NT>
+static cudaError_t norm_bwd_cluster_go(const T* x, int64_t ldx, const float* w, const T* dy,
+                                       int64_t lddy, float eps, T* dx, int64_t lddx, float* part,
+                                       int64_t N, int64_t Dv, int64_t P, cudaStream_t s) {
+    constexpr int V = Elt<T>::V, CPT = 16 / V;
+    constexpr int S = V == 4 ? kNormBwdStages32[LN] : kNormBwdStages16[LN];
+    constexpr bool WS = kNormBwdWSlots[LN];
+    constexpr auto k = norm_bwd_cluster<T, LN, NT, S, WS>;
+    const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
+    // staged x and dy, then (WS) this thread's w slots
+    const size_t smem = (size_t)2 * S * CPT * NT * 16 + (WS ? (size_t)CPT * V * NT * 4 : 0);
+    int fit = 0;
+    const cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
+    if (e != cudaSuccess) return e;
+    return launch_cluster(k, (unsigned)std::min<int64_t>(P, fit), cs, dim3(NT), smem, s, x, ldx, w,
+                          dy, lddy, eps, dx, lddx, part, N, (int)Dv, P);
+}
+
 template <typename T, bool LN>
 static cudaError_t norm_fwd_t(const T* x, int64_t ldx, const float* w, const float* b, float eps,
                               T* y, int64_t ldy, int64_t N, int64_t D, cudaStream_t s) {
@@ -1189,15 +1228,10 @@ static cudaError_t norm_fwd_t(const T* x, int64_t ldx, const float* w, const flo
     }
     if (D % V == 0 && D <= kNormClusterRowMax && ldx % V == 0 && ldy % V == 0 && aligned16(x) &&
         aligned16(y) && aligned16(w) && (!LN || aligned16(b))) {
-        constexpr int NT = kNormClusterNT, S = kNormFwdStages[LN], CPT = 16 / V;
-        constexpr auto k = norm_fwd_cluster<T, LN, NT, S>;
-        const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
-        const size_t smem = (size_t)S * CPT * NT * 16;
-        int fit = 0;
-        cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
-        if (e == cudaSuccess)
-            return launch_cluster(k, (unsigned)std::min<int64_t>(N, fit), cs, dim3(NT), smem, s, x,
-                                  ldx, w, b, eps, y, ldy, N, (int)Dv);
+        const cudaError_t e = D <= kNormClusterSmallMaxD
+                                  ? norm_fwd_cluster_go<T, LN, 128>(x, ldx, w, b, eps, y, ldy, N, Dv, s)
+                                  : norm_fwd_cluster_go<T, LN, kNormClusterNT>(x, ldx, w, b, eps, y,
+                                                                               ldy, N, Dv, s);
         if (e != cudaErrorNotSupported) return e;
     }
     return launch(norm_fwd_scalar<T, LN, 256>,
@@ -1241,19 +1275,11 @@ static cudaError_t norm_bwd_t(const T* x, int64_t ldx, const float* w, const T* 
             e = cudaErrorNotSupported;
             if (D % V == 0 && D <= kNormClusterRowMax && ldx % V == 0 && lddy % V == 0 &&
                 lddx % V == 0 && aligned16(x) && aligned16(dy) && aligned16(dx) && aligned16(w)) {
-                constexpr int NT = kNormClusterNT, CPT = 16 / V;
-                constexpr int S = V == 4 ? kNormBwdStages32[LN] : kNormBwdStages16[LN];
-                constexpr bool WS = kNormBwdWSlots[LN];
-                constexpr auto k = norm_bwd_cluster<T, LN, NT, S, WS>;
-                const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
-                // staged x and dy, then (WS) this thread's w slots
-                const size_t smem =
-                    (size_t)2 * S * CPT * NT * 16 + (WS ? (size_t)CPT * V * NT * 4 : 0);
-                int fit = 0;
-                e = cluster_fit<k>(cs, NT, smem, fit);
-                if (e == cudaSuccess)
-                    e = launch_cluster(k, (unsigned)std::min<int64_t>(P, fit), cs, dim3(NT), smem,
-                                       s, x, ldx, w, dy, lddy, eps, dx, lddx, part, N, (int)Dv, P);
+                e = D <= kNormClusterSmallMaxD
+                        ? norm_bwd_cluster_go<T, LN, 128>(x, ldx, w, dy, lddy, eps, dx, lddx, part,
+                                                          N, Dv, P, s)
+                        : norm_bwd_cluster_go<T, LN, kNormClusterNT>(x, ldx, w, dy, lddy, eps, dx,
+                                                                     lddx, part, N, Dv, P, s);
             }
             if (e == cudaErrorNotSupported)
                 e = launch(norm_bwd_scalar<T, LN, 256>, dim3((unsigned)P), dim3(256), 0, s, true,
