@@ -103,12 +103,13 @@ def test_softmax_large_logits_and_reproducible(wsf):
 
 
 # Cluster rows: 16-byte chunks (8 16-bit or 4 fp32 elements) split over CTAs
-# of 1024 (256 threads) or 2048 (512 threads) chunks.
+# of 1024 chunks (256 threads) for rows of up to 16,384 chunks, else 2048
+# chunks (512 threads).
 @pytest.mark.parametrize("dt", DTS)
 @pytest.mark.parametrize("N,D", [
     (700, 16392),   # 16-bit: 2049 chunks, 3 CTAs, the last holding one chunk; more rows than clusters
-    (50, 65536),    # 16-bit: 8 CTAs of 256; fp32: 8 CTAs of 512
-    (20, 131072),   # 16-bit: 8 CTAs of 512; fp32: 16 CTAs of 512
+    (50, 65536),    # 16-bit: 8 CTAs of 256; fp32: 16 CTAs of 256
+    (20, 131072),   # 16-bit: 16 CTAs of 256; fp32: 16 CTAs of 512
     (9, 262144),    # 16-bit: 16 CTAs of 512; fp32: beyond the cluster rows (element-wise path)
     (31, 100008),   # ragged last slice
     (13, 50264),
