@@ -235,9 +235,9 @@ __device__ __forceinline__ float select(const float (&a)[K], int i) {
 
 // ---------------------------------------------------------------------------
 // Thread-block clusters (sm_90 and later).  A cluster's CTAs are scheduled
-// together and can read one another's shared memory ("distributed shared
+// together and can reach one another's shared memory ("distributed shared
 // memory"): mapa turns a local shared-memory address into the address of the
-// same variable in the CTA of a given rank, and ld.shared::cluster reads it.
+// same variable in the CTA of a given rank (the target of st.async below).
 // cluster_sync() is the hardware cluster barrier (every thread of every CTA
 // of the cluster arrives; .release/.acquire make shared-memory writes made
 // before the arrival visible to reads made after the wait).  It is not a
@@ -274,24 +274,6 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, unsigned r) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(r));
     return out;
 }
-__device__ __forceinline__ float cluster_ld_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ float2 cluster_ld_f32x2(uint32_t a) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 cluster_ld_f32x4(uint32_t a) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
-    return v;
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier-completed pushes into another CTA's shared memory (sm_90 and
 // later).  st.async writes a value into the shared memory of a CTA of the
