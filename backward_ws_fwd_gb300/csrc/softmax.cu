@@ -13,11 +13,12 @@
 // are combined with xor butterflies inside a warp and, for groups wider than
 // a warp, through shared memory in warp order.  x (or y and dy) is read once
 // and y (dx) written once.  Rows of up to 32,768 chunks are split over a
-// thread-block cluster (below).  Rows that do not start on 16 bytes, or whose
-// width is not a whole number of chunks, are read as the chunks that cover
-// them, with the edges masked (Win), when every array of the call has the
-// same offset in each row; other rows take a multi-pass element-wise path
-// with one CTA per row.  Sums of binary32 rows are compensated and their
+// thread-block cluster (below), wider rows over a cluster that streams them
+// twice (two-pass).  Rows that do not start on 16 bytes, or whose width is
+// not a whole number of chunks, are read as the chunks that cover them, with
+// the edges masked (Win), when every array of the call has the same offset in
+// each row; other rows take a multi-pass element-wise path with one CTA per
+// row.  Sums of binary32 rows are compensated and their
 // exponentials taken of exactly split differences.
 #include <algorithm>
 #include <type_traits>
@@ -804,6 +805,281 @@ __global__ void __launch_bounds__(NT)
 }
 
 // ---------------------------------------------------------------------------
+// Two-pass cluster path (rows wider than the cluster path holds: more than
+// 32,768 chunks).  A cluster of CS CTAs takes a row; the CTA of rank r owns
+// the chunks [r·SL, (r+1)·SL), SL = ⌈Dc/CS⌉, which its threads stream from
+// memory twice, a few chunks a thread at a time: the first pass forms each
+// thread's maximum and its sum of exp(x − m) (rescaled when the maximum
+// grows; forward) or its part of Σ dy·y (backward), the warps exchange these
+// as on the cluster path, and the second pass reads the slice again and
+// writes y (dx).  Only the clusters' rows in flight (tens of MB) are read
+// between the passes, so the second read is served by L2; x (y, dy) is read
+// from HBM once.  The forward prefetches its slice of the cluster's next row
+// into L2 (prefetch_slice); in the backward, prefetching y and dy measured
+// slower (twice the L2 footprint).  Elements outside the row (windowed edges, the tail of the
+// last slice) enter as −inf (forward) or 0 (backward).
+constexpr int kTwoPassNT = 256, kTwoPassCS = 16, kTwoPassU = 4;
+
+// Thread 0 prefetches into L2 this CTA's chunks [c0, c0 + SL) of a row (only
+// the 16-byte blocks that hold the row's own elements), so that the next
+// row's first pass reads from L2 while HBM keeps streaming.
+template <typename T, bool U>
+__device__ __forceinline__ void prefetch_slice(const T* row_start, int D, int c0, int SL) {
+    constexpr int V = Elt<T>::V;
+    const int off = win_off<T, U>(row_start);
+    const int nc = (off + D + V - 1) / V;
+    const int e = c0 + SL < nc ? c0 + SL : nc;
+    if (e > c0) prefetch_l2_bulk(row_start - off + (int64_t)c0 * V, (uint32_t)(e - c0) * 16u);
+}
+
+// Chunk cc of a row widened, with −inf (Fwd) or 0 outside the row.
+template <typename T, bool U, bool Fwd>
+__device__ __forceinline__ void load_chunk(const T* row_start, const Win<T, U>& w, int cc,
+                                           float (&f)[Elt<T>::V]) {
+    using E = Elt<T>;
+    if (w.has(cc)) {
+        E::widen(ld_stream(row_start + w.at(cc)), f);
+        if (!w.full(cc))
+#pragma unroll
+            for (int v = 0; v < E::V; v++)
+                if (!w.elt(cc, v)) f[v] = Fwd ? -INFINITY : 0.f;
+    } else {
+#pragma unroll
+        for (int v = 0; v < E::V; v++) f[v] = Fwd ? -INFINITY : 0.f;
+    }
+}
+
+template <typename T, bool U>
+__global__ void __launch_bounds__(kTwoPassNT, 4)
+    softmax_fwd_cluster2(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
+                         int64_t N, int D, int SL) {
+    using E = Elt<T>;
+    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = kTwoPassU;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float2 res[2];  // (row maximum, 1/sum), by turn parity
+    SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
+    xp.init();
+    cluster_sync();
+    const int lane = threadIdx.x & 31;
+    const int total = (int)cluster_nctarank() * W;
+    const int c0 = (int)cluster_ctarank() * SL;  // this CTA's chunks [c0, c0 + SL)
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    pdl_wait();
+    for (int64_t row = cid; row < N; row += ncl) {
+        const T* xr = x + row * ldx;
+        const Win<T, U> win{win_off<T, U>(xr), D};
+        if (threadIdx.x == 0 && row + ncl < N) prefetch_slice<T, U>(xr + ncl * ldx, D, c0, SL);
+        // pass 1: this thread's maximum m and Σ exp(x − m)
+        float m = -INFINITY;
+        Acc2 s = acc2_zero();
+        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+            float f[UU][V];
+#pragma unroll
+            for (int u = 0; u < UU; u++) {
+                const int c = b + u * NT;
+                if (c < SL) {
+                    load_chunk<T, U, true>(xr, win, c0 + c, f[u]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; v++) f[u][v] = -INFINITY;
+                }
+            }
+            float mb = m;
+#pragma unroll
+            for (int u = 0; u < UU; u++)
+#pragma unroll
+                for (int v = 0; v < V; v++) mb = fmaxf(mb, f[u][v]);
+            if (mb == -INFINITY) continue;  // nothing finite yet
+            if (mb > m && s.hi != 0.f) {    // rescale the sum to the new maximum
+                const float g = rescale<kComp>(m, mb);
+                if constexpr (kComp) {
+                    const float hi = __fmul_rn(s.hi, g);
+                    s = Acc2{hi, fmaf(s.lo, g, fmaf(s.hi, g, -hi))};
+                } else {
+                    s.hi *= g;
+                }
+            }
+            m = mb;
+#pragma unroll
+            for (int u = 0; u < UU; u++)
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    const float e = kComp ? exp_diff<false>(f[u][v], m)
+                                          : exp2_approx(fmaf(f[u][v], kLog2e, -m * kLog2e));
+                    add_to<kComp>(s, e);
+                }
+        }
+        // the warp's maximum and its sum relative to it
+        const float mw = warp_max(m);
+        Acc2 sw = acc2_zero();
+        if (s.hi > 0.f) {
+            const float g = rescale<kComp>(m, mw);
+            if constexpr (kComp) {
+                acc2_fma(sw, __fadd_rn(s.hi, s.lo), g);
+            } else {
+                sw.hi = s.hi * g;
+            }
+        }
+        if constexpr (kComp)
+            sw = group_sum2<32>(sw);
+        else
+            sw.hi = group_sum<32>(sw.hi);
+        const float4 mine[1] = {make_float4(mw == -INFINITY ? 0.f : mw, sw.hi, sw.lo, 0.f)};
+        const unsigned turn = xp.template push<1>(mine);
+        float2* out = &res[turn & 1u];
+        if (threadIdx.x < 32) {  // warp 0 combines the turn's entries
+            const float4(*buf)[1] = xp.wait(turn);
+            float M = -INFINITY;
+            for (int j = lane; j < total; j += 32)
+                if (buf[j][0].y > 0.f) M = fmaxf(M, buf[j][0].x);
+            M = warp_max(M);
+            Acc2 t = acc2_zero();
+            for (int j = lane; j < total; j += 32) {
+                const float4 en = buf[j][0];
+                if (en.y > 0.f) {  // skip warps without a finite element
+                    const float g = rescale<kComp>(en.x, M);
+                    if constexpr (kComp)
+                        acc2_fma(t, __fadd_rn(en.y, en.z), g);
+                    else
+                        t.hi = fmaf(en.y, g, t.hi);
+                }
+            }
+            float inv;
+            if constexpr (kComp) {
+                t = group_sum2<32>(t);
+                inv = 1.0f / (t.hi + t.lo);
+            } else {
+                inv = 1.0f / group_sum<32>(t.hi);
+            }
+            if (lane == 0) *out = make_float2(M, inv);
+        }
+        __syncthreads();
+        const float2 Mi = *out;
+        // pass 2: y = exp(x − M)/sum, the slice read again (from L2)
+        T* yr = y + row * ldy;
+        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+#pragma unroll
+            for (int u = 0; u < UU; u++) {
+                const int c = b + u * NT, cc = c0 + c;
+                if (c < SL && win.has(cc)) {
+                    float f[V], o[V];
+                    load_chunk<T, U, true>(xr, win, cc, f);
+#pragma unroll
+                    for (int v = 0; v < V; v++) {
+                        const float e = kComp ? exp_diff<false>(f[v], Mi.x)
+                                              : exp2_approx(fmaf(f[v], kLog2e, -Mi.x * kLog2e));
+                        o[v] = e * Mi.y;
+                    }
+                    store_chunk<T, U>(yr, win, cc, o);
+                }
+            }
+        }
+    }
+    cluster_sync();
+    pdl_trigger();
+}
+
+template <typename T, bool U>
+__global__ void __launch_bounds__(kTwoPassNT, 4)
+    softmax_bwd_cluster2(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy,
+                         int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int D,
+                         int SL) {
+    using E = Elt<T>;
+    // 16 elements of y and of dy a thread in flight
+    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = 16 / V;
+    constexpr bool kComp = std::is_same<T, float>::value;
+    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float res[2];  // Σ dy·y, by turn parity
+    SoftmaxPush<NT> xp{xbuf, xbar, &g_softmax_wait_timeouts, 0u, true};
+    xp.init();
+    cluster_sync();
+    const int lane = threadIdx.x & 31;
+    const int total = (int)cluster_nctarank() * W;
+    const int c0 = (int)cluster_ctarank() * SL;
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    pdl_wait();
+    for (int64_t row = cid; row < N; row += ncl) {
+        const T* yr = y + row * ldy;
+        const T* gr = dy + row * lddy;
+        const Win<T, U> win{win_off<T, U>(yr), D};
+        // pass 1: this thread's part of Σ dy·y
+        Acc2 s = acc2_zero();
+        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+            float fy[UU][V], fg[UU][V];
+#pragma unroll
+            for (int u = 0; u < UU; u++) {
+                const int c = b + u * NT;
+                if (c < SL) {
+                    load_chunk<T, U, false>(yr, win, c0 + c, fy[u]);
+                    load_chunk<T, U, false>(gr, win, c0 + c, fg[u]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; v++) fy[u][v] = fg[u][v] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UU; u++)
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    if constexpr (kComp)
+                        acc2_fma(s, fg[u][v], fy[u][v]);
+                    else
+                        s.hi = fmaf(fg[u][v], fy[u][v], s.hi);
+                }
+        }
+        if constexpr (kComp)
+            s = group_sum2<32>(s);
+        else
+            s.hi = group_sum<32>(s.hi);
+        const float4 mine[1] = {make_float4(s.hi, s.lo, 0.f, 0.f)};
+        const unsigned turn = xp.template push<1>(mine);
+        float* out = &res[turn & 1u];
+        if (threadIdx.x < 32) {  // warp 0 combines the turn's entries
+            const float4(*buf)[1] = xp.wait(turn);
+            Acc2 t = acc2_zero();
+            for (int j = lane; j < total; j += 32) {
+                const float4 o = buf[j][0];
+                if constexpr (kComp)
+                    t = acc2_add(t, Acc2{o.x, o.y});
+                else
+                    t.hi += o.x;
+            }
+            float r;
+            if constexpr (kComp) {
+                t = group_sum2<32>(t);
+                r = t.hi + t.lo;
+            } else {
+                r = group_sum<32>(t.hi);
+            }
+            if (lane == 0) *out = r;
+        }
+        __syncthreads();
+        const float sv = *out;
+        // pass 2: dx = y·(dy − Σ dy·y), y and dy read again (from L2)
+        T* dxr = dx + row * lddx;
+        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+#pragma unroll
+            for (int u = 0; u < UU; u++) {
+                const int c = b + u * NT, cc = c0 + c;
+                if (c < SL && win.has(cc)) {
+                    float fy[V], fg[V], o[V];
+                    load_chunk<T, U, false>(yr, win, cc, fy);
+                    load_chunk<T, U, false>(gr, win, cc, fg);
+#pragma unroll
+                    for (int v = 0; v < V; v++) o[v] = fy[v] * (fg[v] - sv);
+                    store_chunk<T, U>(dxr, win, cc, o);
+                }
+            }
+        }
+    }
+    cluster_sync();
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
 static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline int next_pow2(int64_t v) {
@@ -929,6 +1205,26 @@ static cudaError_t softmax_bwd_cluster_t(const T* y, int64_t ldy, const T* dy, i
         (int)D);
 }
 
+// Two-pass cluster launches (rows over kClusterRowChunks chunks, D < 2^30).
+template <typename T, bool U>
+static cudaError_t softmax_fwd_cluster2_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
+                                          int64_t D, int64_t Dc, cudaStream_t s) {
+    const int SL = (int)cdiv(Dc, kTwoPassCS);
+    return go_cluster<softmax_fwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS, 0, N, s, x, ldx, y, ldy,
+                                                  N, (int)D, SL);
+}
+
+template <typename T, bool U>
+static cudaError_t softmax_bwd_cluster2_t(const T* y, int64_t ldy, const T* dy, int64_t lddy,
+                                          T* dx, int64_t lddx, int64_t N, int64_t D, int64_t Dc,
+                                          cudaStream_t s) {
+    const int SL = (int)cdiv(Dc, kTwoPassCS);
+    return go_cluster<softmax_bwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS, 0, N, s, y, ldy, dy,
+                                                  lddy, dx, lddx, N, (int)D, SL);
+}
+
+constexpr int64_t kTwoPassMaxD = (int64_t)1 << 30;
+
 // Row layouts of the vector paths: aligned (every array's rows start on 16
 // bytes, D a whole number of chunks), or windowed (U: the arrays' rows share
 // their offset inside a 16-byte block, row by row).  Dc = chunks a row spans
@@ -958,6 +1254,7 @@ static cudaError_t softmax_fwd_vec(const T* x, int64_t ldx, T* y, int64_t ldy, i
         });
     }
     if (Dc <= kClusterRowChunks && N > 0) return softmax_fwd_cluster_t<T, U>(x, ldx, y, ldy, N, D, Dc, s);
+    if (D < kTwoPassMaxD && N > 0) return softmax_fwd_cluster2_t<T, U>(x, ldx, y, ldy, N, D, Dc, s);
     return cudaErrorNotSupported;
 }
 
@@ -977,6 +1274,8 @@ static cudaError_t softmax_bwd_vec(const T* y, int64_t ldy, const T* dy, int64_t
     }
     if (Dc <= kClusterRowChunks && N > 0)
         return softmax_bwd_cluster_t<T, U>(y, ldy, dy, lddy, dx, lddx, N, D, Dc, s);
+    if (D < kTwoPassMaxD && N > 0)
+        return softmax_bwd_cluster2_t<T, U>(y, ldy, dy, lddy, dx, lddx, N, D, Dc, s);
     return cudaErrorNotSupported;
 }
 

@@ -68,6 +68,12 @@ __device__ __forceinline__ void st_stream(void* p, const Raw16& r) {
                  : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) from global memory into L2,
+// starting at a 16-byte aligned address; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Asynchronous 16-byte global -> shared copy (cp.async, bypassing L1, with a
 // 256-byte L2 prefetch).  Only the first src_bytes (0..16) are read; the
 // rest of the 16 shared bytes are zero-filled.  A thread waits for its own

@@ -3,7 +3,8 @@ register rows of every width class, cluster rows (clusters of 3 to 16 CTAs,
 both CTA widths, ragged last slices, more rows than resident clusters), the
 element-wise wide/unaligned path, masked (−inf) logits, row strides, guard
 bands, windowed rows (odd widths and shifted pointers read as the 16-byte
-chunks that cover each row, edges masked), arrays at mixed offsets, bit
+chunks that cover each row, edges masked), two-pass cluster rows (wider than
+32,768 chunks), arrays at mixed offsets, bit
 reproducibility, and sampled rows at the measurement size."""
 import numpy as np
 import pytest
@@ -110,7 +111,7 @@ def test_softmax_large_logits_and_reproducible(wsf):
     (700, 16392),   # 16-bit: 2049 chunks, 3 CTAs, the last holding one chunk; more rows than clusters
     (50, 65536),    # 16-bit: 8 CTAs of 256; fp32: 16 CTAs of 256
     (20, 131072),   # 16-bit: 16 CTAs of 256; fp32: 16 CTAs of 512
-    (9, 262144),    # 16-bit: 16 CTAs of 512; fp32: beyond the cluster rows (element-wise path)
+    (9, 262144),    # 16-bit: 16 CTAs of 512; fp32: beyond the cluster rows (two-pass path)
     (31, 100008),   # ragged last slice
     (13, 50264),
     (3, 50257),     # width not a whole number of chunks (element-wise path)
@@ -174,7 +175,7 @@ def test_softmax_masked_logits(wsf, dt, N, D):
     (30, 512, 0, 1),
     (50, 50257, 0, 0),     # a GPT-2-sized vocabulary: cluster rows
     (9, 100003, 5, 1),
-    (3, 262150, 0, 0),     # wider than the cluster rows (element-wise path)
+    (3, 262150, 0, 0),     # wider than the cluster rows (two-pass path)
 ])
 def test_softmax_windowed_rows(wsf, dt, N, D, pad, mis):
     x, dy = _inputs(N, D, dt, seed=D % 89)
@@ -208,6 +209,38 @@ def test_softmax_mixed_offsets(wsf, dt, D):
     assert bool((yb[:2] == 7).all()) and bool((yb[2 + N * D:] == 7).all())
     assert bool((dxb[:3] == 7).all()) and bool((dxb[3 + N * D:] == 7).all())
     _check(x, dy, y.cpu(), dxv.cpu(), yin)
+
+
+# Two-pass cluster rows: wider than 32,768 chunks; every CTA of a 16-CTA
+# cluster streams its slice twice (the second time from L2).
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("N,D,pad,mis", [
+    (5, 300000, 0, 0),
+    (4, 300007, 0, 0),     # windowed: the offset changes from row to row
+    (3, 524288, 8, 1),     # 16-bit: 65,536 chunks; every row shifted by one element
+    (100, 140000, 0, 0),   # fp32: 35,000 chunks; more rows than resident clusters
+])
+def test_softmax_two_pass_rows(wsf, dt, N, D, pad, mis):
+    x, dy = _inputs(N, D, dt, seed=D % 83)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin, pad=pad, mis=mis)
+    _check(x, dy, y, dx, yin)
+
+
+def test_softmax_two_pass_extremes(wsf):
+    # the row maximum in the first and in the last slice, a growing maximum
+    # within one thread's chunks, masked spans covering whole slices
+    N, D = 5, 200000
+    x, dy = _inputs(N, D, "f32", seed=9)
+    x[0, 0] = 50.0
+    x[1, -1] = 50.0
+    x[2] = torch.linspace(-30.0, 30.0, D)
+    x[3, 1000:] = float("-inf")
+    x[4, :150000] = float("-inf")
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+    assert bool((y[3, 1000:] == 0).all()) and bool((y[4, :150000] == 0).all())
 
 
 def test_softmax_cluster_no_wait_timeouts(wsf):
