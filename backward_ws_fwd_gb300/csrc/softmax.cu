@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(NT)
 // Two-pass cluster path (rows wider than the cluster path holds: more than
 // 32,768 chunks).  A cluster of CS CTAs takes a row; the CTA of rank r owns
 // the chunks [r·SL, (r+1)·SL), SL = ⌈Dc/CS⌉, which its threads stream from
-// memory twice, a few chunks a thread at a time: the first pass forms each
+// memory twice, a few chunks a thread a batch: the first pass forms each
 // thread's maximum and its sum of exp(x − m) (rescaled when the maximum
 // grows; forward) or its part of Σ dy·y (backward), the warps exchange these
 // as on the cluster path, and the second pass reads the slice again and
@@ -832,13 +832,26 @@ __device__ __forceinline__ void prefetch_slice(const T* row_start, int D, int c0
     if (e > c0) prefetch_l2_bulk(row_start - off + (int64_t)c0 * V, (uint32_t)(e - c0) * 16u);
 }
 
-// Chunk cc of a row widened, with −inf (Fwd) or 0 outside the row.
+// The raw chunks c0 + b + u·NT (u < NU) of a row: the row's own 16-byte
+// blocks, zeros for chunks past the slice or the row.
+template <typename T, bool U, int NU>
+__device__ __forceinline__ void load_batch(Raw16 (&r)[NU], const T* row_start, const Win<T, U>& w,
+                                           int c0, int b, int SL) {
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+        const int c = b + u * kTwoPassNT;
+        r[u] = (c < SL && w.has(c0 + c)) ? ld_stream(row_start + w.at(c0 + c)) : raw_zero();
+    }
+}
+
+// Chunk c of the slice (row chunk cc = c0 + c) widened, with −inf (Fwd) or 0
+// outside the slice and the row.
 template <typename T, bool U, bool Fwd>
-__device__ __forceinline__ void load_chunk(const T* row_start, const Win<T, U>& w, int cc,
-                                           float (&f)[Elt<T>::V]) {
+__device__ __forceinline__ void widen_chunk(const Raw16& r, const Win<T, U>& w, int c, int cc,
+                                            int SL, float (&f)[Elt<T>::V]) {
     using E = Elt<T>;
-    if (w.has(cc)) {
-        E::widen(ld_stream(row_start + w.at(cc)), f);
+    if (c < SL && w.has(cc)) {
+        E::widen(r, f);
         if (!w.full(cc))
 #pragma unroll
             for (int v = 0; v < E::V; v++)
@@ -849,12 +862,16 @@ __device__ __forceinline__ void load_chunk(const T* row_start, const Win<T, U>& 
     }
 }
 
+// The loads are pipelined in registers: each thread holds the raw chunks of
+// its next batch while it computes the current one; the last batch of the
+// first pass fetches the second pass's first batch (before the exchange),
+// and the last batch of the second pass the next row's first batch.
 template <typename T, bool U>
-__global__ void __launch_bounds__(kTwoPassNT, 4)
+__global__ void __launch_bounds__(kTwoPassNT, 3)
     softmax_fwd_cluster2(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
                          int64_t N, int D, int SL) {
     using E = Elt<T>;
-    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = kTwoPassU;
+    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = kTwoPassU, STEP = NT * UU;
     constexpr bool kComp = std::is_same<T, float>::value;
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
     __shared__ __align__(8) uint64_t xbar[2];
@@ -867,6 +884,11 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
     const int c0 = (int)cluster_ctarank() * SL;  // this CTA's chunks [c0, c0 + SL)
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     pdl_wait();
+    Raw16 nb[UU];  // the next batch's raw chunks
+    if (cid < N) {
+        const T* x0 = x + cid * ldx;
+        load_batch<T, U, UU>(nb, x0, Win<T, U>{win_off<T, U>(x0), D}, c0, threadIdx.x, SL);
+    }
     for (int64_t row = cid; row < N; row += ncl) {
         const T* xr = x + row * ldx;
         const Win<T, U> win{win_off<T, U>(xr), D};
@@ -874,23 +896,20 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
         // pass 1: this thread's maximum m and Σ exp(x − m)
         float m = -INFINITY;
         Acc2 s = acc2_zero();
-        for (int b = threadIdx.x; b < SL; b += NT * UU) {
-            float f[UU][V];
+        for (int b = threadIdx.x; b < SL; b += STEP) {
+            Raw16 cur[UU];
 #pragma unroll
-            for (int u = 0; u < UU; u++) {
-                const int c = b + u * NT;
-                if (c < SL) {
-                    load_chunk<T, U, true>(xr, win, c0 + c, f[u]);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < V; v++) f[u][v] = -INFINITY;
-                }
-            }
+            for (int u = 0; u < UU; u++) cur[u] = nb[u];
+            // the next batch, or the second pass's first
+            load_batch<T, U, UU>(nb, xr, win, c0, b + STEP < SL ? b + STEP : (int)threadIdx.x, SL);
             float mb = m;
 #pragma unroll
-            for (int u = 0; u < UU; u++)
+            for (int u = 0; u < UU; u++) {
+                float f[V];
+                widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
 #pragma unroll
-                for (int v = 0; v < V; v++) mb = fmaxf(mb, f[u][v]);
+                for (int v = 0; v < V; v++) mb = fmaxf(mb, f[v]);
+            }
             if (mb == -INFINITY) continue;  // nothing finite yet
             if (mb > m && s.hi != 0.f) {    // rescale the sum to the new maximum
                 const float g = rescale<kComp>(m, mb);
@@ -903,13 +922,16 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
             }
             m = mb;
 #pragma unroll
-            for (int u = 0; u < UU; u++)
+            for (int u = 0; u < UU; u++) {
+                float f[V];
+                widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
-                    const float e = kComp ? exp_diff<false>(f[u][v], m)
-                                          : exp2_approx(fmaf(f[u][v], kLog2e, -m * kLog2e));
+                    const float e = kComp ? exp_diff<false>(f[v], m)
+                                          : exp2_approx(fmaf(f[v], kLog2e, -m * kLog2e));
                     add_to<kComp>(s, e);
                 }
+            }
         }
         // the warp's maximum and its sum relative to it
         const float mw = warp_max(m);
@@ -959,13 +981,22 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
         const float2 Mi = *out;
         // pass 2: y = exp(x − M)/sum, the slice read again (from L2)
         T* yr = y + row * ldy;
-        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+        for (int b = threadIdx.x; b < SL; b += STEP) {
+            Raw16 cur[UU];
+#pragma unroll
+            for (int u = 0; u < UU; u++) cur[u] = nb[u];
+            if (b + STEP < SL) {
+                load_batch<T, U, UU>(nb, xr, win, c0, b + STEP, SL);
+            } else if (row + ncl < N) {  // the next row's first batch
+                const T* xn = xr + ncl * ldx;
+                load_batch<T, U, UU>(nb, xn, Win<T, U>{win_off<T, U>(xn), D}, c0, threadIdx.x, SL);
+            }
 #pragma unroll
             for (int u = 0; u < UU; u++) {
                 const int c = b + u * NT, cc = c0 + c;
                 if (c < SL && win.has(cc)) {
                     float f[V], o[V];
-                    load_chunk<T, U, true>(xr, win, cc, f);
+                    widen_chunk<T, U, true>(cur[u], win, c, cc, SL, f);
 #pragma unroll
                     for (int v = 0; v < V; v++) {
                         const float e = kComp ? exp_diff<false>(f[v], Mi.x)
@@ -982,13 +1013,13 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
 }
 
 template <typename T, bool U>
-__global__ void __launch_bounds__(kTwoPassNT, 4)
+__global__ void __launch_bounds__(kTwoPassNT, 3)
     softmax_bwd_cluster2(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy,
                          int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int D,
                          int SL) {
     using E = Elt<T>;
-    // 16 elements of y and of dy a thread in flight
-    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = 16 / V;
+    // 16 elements of y and of dy a thread a batch
+    constexpr int V = E::V, NT = kTwoPassNT, W = NT / 32, UU = 16 / V, STEP = NT * UU;
     constexpr bool kComp = std::is_same<T, float>::value;
     __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * W][1];
     __shared__ __align__(8) uint64_t xbar[2];
@@ -1001,34 +1032,43 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
     const int c0 = (int)cluster_ctarank() * SL;
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     pdl_wait();
+    Raw16 ny[UU], ng[UU];  // the next batch's raw chunks of y and dy
+    if (cid < N) {
+        const T* y0 = y + cid * ldy;
+        const Win<T, U> w0{win_off<T, U>(y0), D};
+        load_batch<T, U, UU>(ny, y0, w0, c0, threadIdx.x, SL);
+        load_batch<T, U, UU>(ng, dy + cid * lddy, w0, c0, threadIdx.x, SL);
+    }
     for (int64_t row = cid; row < N; row += ncl) {
         const T* yr = y + row * ldy;
         const T* gr = dy + row * lddy;
         const Win<T, U> win{win_off<T, U>(yr), D};
         // pass 1: this thread's part of Σ dy·y
         Acc2 s = acc2_zero();
-        for (int b = threadIdx.x; b < SL; b += NT * UU) {
-            float fy[UU][V], fg[UU][V];
+        for (int b = threadIdx.x; b < SL; b += STEP) {
+            Raw16 cy[UU], cg[UU];
 #pragma unroll
             for (int u = 0; u < UU; u++) {
-                const int c = b + u * NT;
-                if (c < SL) {
-                    load_chunk<T, U, false>(yr, win, c0 + c, fy[u]);
-                    load_chunk<T, U, false>(gr, win, c0 + c, fg[u]);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < V; v++) fy[u][v] = fg[u][v] = 0.f;
-                }
+                cy[u] = ny[u];
+                cg[u] = ng[u];
             }
+            // the next batch, or the second pass's first
+            const int bn = b + STEP < SL ? b + STEP : (int)threadIdx.x;
+            load_batch<T, U, UU>(ny, yr, win, c0, bn, SL);
+            load_batch<T, U, UU>(ng, gr, win, c0, bn, SL);
 #pragma unroll
-            for (int u = 0; u < UU; u++)
+            for (int u = 0; u < UU; u++) {
+                float fy[V], fg[V];
+                widen_chunk<T, U, false>(cy[u], win, b + u * NT, c0 + b + u * NT, SL, fy);
+                widen_chunk<T, U, false>(cg[u], win, b + u * NT, c0 + b + u * NT, SL, fg);
 #pragma unroll
                 for (int v = 0; v < V; v++) {
                     if constexpr (kComp)
-                        acc2_fma(s, fg[u][v], fy[u][v]);
+                        acc2_fma(s, fg[v], fy[v]);
                     else
-                        s.hi = fmaf(fg[u][v], fy[u][v], s.hi);
+                        s.hi = fmaf(fg[v], fy[v], s.hi);
                 }
+            }
         }
         if constexpr (kComp)
             s = group_sum2<32>(s);
@@ -1060,14 +1100,29 @@ __global__ void __launch_bounds__(kTwoPassNT, 4)
         const float sv = *out;
         // pass 2: dx = y·(dy − Σ dy·y), y and dy read again (from L2)
         T* dxr = dx + row * lddx;
-        for (int b = threadIdx.x; b < SL; b += NT * UU) {
+        for (int b = threadIdx.x; b < SL; b += STEP) {
+            Raw16 cy[UU], cg[UU];
+#pragma unroll
+            for (int u = 0; u < UU; u++) {
+                cy[u] = ny[u];
+                cg[u] = ng[u];
+            }
+            if (b + STEP < SL) {
+                load_batch<T, U, UU>(ny, yr, win, c0, b + STEP, SL);
+                load_batch<T, U, UU>(ng, gr, win, c0, b + STEP, SL);
+            } else if (row + ncl < N) {  // the next row's first batch
+                const T* yn = yr + ncl * ldy;
+                const Win<T, U> wn{win_off<T, U>(yn), D};
+                load_batch<T, U, UU>(ny, yn, wn, c0, threadIdx.x, SL);
+                load_batch<T, U, UU>(ng, gr + ncl * lddy, wn, c0, threadIdx.x, SL);
+            }
 #pragma unroll
             for (int u = 0; u < UU; u++) {
                 const int c = b + u * NT, cc = c0 + c;
                 if (c < SL && win.has(cc)) {
                     float fy[V], fg[V], o[V];
-                    load_chunk<T, U, false>(yr, win, cc, fy);
-                    load_chunk<T, U, false>(gr, win, cc, fg);
+                    widen_chunk<T, U, false>(cy[u], win, c, cc, SL, fy);
+                    widen_chunk<T, U, false>(cg[u], win, c, cc, SL, fg);
 #pragma unroll
                     for (int v = 0; v < V; v++) o[v] = fy[v] * (fg[v] - sv);
                     store_chunk<T, U>(dxr, win, cc, o);
