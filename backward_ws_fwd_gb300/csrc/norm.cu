@@ -561,12 +561,14 @@ __global__ void __launch_bounds__(NT, MINB)
 // its Σx travels one row ahead: the exchange of row k carries the sums of
 // row k and Σx of row k + 1 (staged already), so that the mean of row k + 1
 // is known when its turn comes, and only the first row's Σx is exchanged on
-// its own.  Σx is compensated across threads for every storage type: the
+// its own.  Σx is compensated across warps for every storage type: the
 // plain binary32 row sum that suffices for 16-bit rows of the row path is
 // exact only while Σx stays below 2^24 steps of the data's grid, i.e. up to
 // 2^24/2^11 = 8192 binary16 elements of one binade (2^24/2^8 = 65536 for
 // bfloat16), and wider binary16 rows with a large common offset would shift
-// every x̂ of a row by the rounding of their mean (see staged_sum_x).
+// every x̂ of a row by the rounding of their mean.  A warp's 512 16-bit
+// elements stay below 2^20 steps, so within a warp they are added plainly
+// (see staged_sum_x), as on the row path.
 //
 // The forward takes rows cid, cid + ncl, … (cluster cid of ncl).  The
 // backward keeps the row tiles of the row path (a function of N alone, so
@@ -605,14 +607,17 @@ __device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
 // ℓ+32, …, then an xor butterfly) and posts the sums in `res`; a CTA barrier
 // hands them to the other warps (and orders this turn's reads before any
 // warp's next push).
-template <int NT, int K, unsigned CM>
+// CMW: the sums compensated already inside each warp (a subset of CM); the
+// others are added plainly within a warp and compensated from the exchange on.
+template <int NT, int K, unsigned CM, unsigned CMW = CM>
 __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp,
                                                float4 (*res)[2]) {
     static_assert(K >= 1 && K <= 4, "up to four sums");
+    static_assert((CMW & ~CM) == 0, "warp-level compensation implies exchange-level");
     constexpr int W = NT / 32, NX = (K + 1) / 2;
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CM >> q) & 1u);
+    for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CMW >> q) & 1u);
     float4 e[NX];
 #pragma unroll
     for (int n = 0; n < NX; n++) {
@@ -660,12 +665,12 @@ __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp,
     }
 }
 
-// Σx over this thread's valid chunks of a staged row, exact up to the
-// rounding that the cross-thread levels then compensate: binary32 elements
-// with TwoSum each; 16-bit elements (8 or 11 significant bits) in plain
-// binary32, which is exact unless the thread's 16 elements span more than 12
-// (bfloat16) or 9 (binary16) binades, and then errs by at most 2^-24 of the
-// thread's partial sum — a shift of the mean by 2^-24·max|x|/D at most.
+// Σx over this thread's valid chunks of a staged row: binary32 elements with
+// TwoSum each; 16-bit elements (8 or 11 significant bits) in plain binary32,
+// as are the warp's 512 (fewer than 2^20 steps of one binade's grid): exact
+// unless a warp's elements span more than 7 (bfloat16) or 4 (binary16)
+// binades, and then off by a few roundings of 2^-24 of the warp's partial
+// sum.  The levels above the warp are compensated.
 template <typename E, int CPT, int NT, int V, bool Comp>
 __device__ __forceinline__ Acc2 staged_sum_x(const Raw16* slot, unsigned valid) {
     Acc2 s = acc2_zero();
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
         Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u>(s0, xc, xres);
+        cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
     for (int64_t k = 0; k < iters; k++) {
@@ -764,7 +769,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
             sm[LN ? 1 : 0] = k + 1 < iters
                 ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
                 : acc2_zero();
-            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u>(sm, xc, xres);
+            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u, C ? 3u : 0u>(sm, xc, xres);
         } else {
             cluster_reduce<NT, 1, C ? 1u : 0u>(sm, xc, xres);
         }
@@ -912,7 +917,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
         Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u>(s0, xc, xres);
+        cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
     for (int64_t k = 0; k < iters; k++) {
@@ -956,7 +961,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
             if (k + 1 < iters)
                 sums[LN ? 3 : 0] =
                     staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
-        cluster_reduce<NT, K, CM>(sums, xc, xres);
+        cluster_reduce<NT, K, CM, C ? CM : 0u>(sums, xc, xres);
         const float r = rstd_of<C>(s_val(sums[0]), inv_d, eps);
         const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
         const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;
