@@ -1,7 +1,7 @@
 """The oracle's results do not depend on its thread count: rows run in
 parallel and the long pairwise sums split into tasks at the same points, so
 one thread and four threads give the same bits.  Sizes are chosen so that
-the task recursion is taken (ranges of more than 2^16 terms)."""
+the OpenMP task recursion is taken (ranges of more than 2^16 terms)."""
 import numpy as np
 import pytest
 import torch
