@@ -10,7 +10,9 @@ and the fixed-order stage 2); nothing here computes anything itself.
 
 RMSNorm and LayerNorm follow "Backward in Triton — autograd.Function and
 the backward grid", § Save vs recompute: the forward saves only x and the
-parameters, and the backward recomputes the row statistics from x.
+parameters, and the backward recomputes the row statistics from x.  Softmax
+saves its output y, from which its backward is formed ("Backprop for kernel
+writers", §04 The duality: dx = y ⊙ (dy − Σ dy·y)).
 
 Gradient accumulation across micro-batches ("fp32 accumulation, and why
 gradients use +=") happens in PyTorch's engine, which adds each returned
@@ -23,7 +25,7 @@ from __future__ import annotations
 import torch
 
 from . import (layernorm_bwd, layernorm_fwd, rmsnorm_bwd, rmsnorm_fwd, silu_bwd, silu_fwd,
-               ws_bwd, ws_fwd)
+               softmax_bwd, softmax_fwd, ws_bwd, ws_fwd)
 
 _STORAGE = (torch.float32, torch.float16, torch.bfloat16)
 
@@ -132,6 +134,31 @@ class LayerNormFunction(torch.autograd.Function):
         need_x, need_w, need_b, _ = ctx.needs_input_grad
         return ((dx.reshape(ctx.x_shape) if need_x else None), (grad_w if need_w else None),
                 (grad_b if need_b else None), None)
+
+
+class SoftmaxFunction(torch.autograd.Function):
+    """Softmax over the last dimension for storage types fp32/fp16/bf16; the
+    output has x's type and shape."""
+
+    @staticmethod
+    def forward(ctx, x):
+        if x.dtype not in _STORAGE:
+            raise TypeError("x must be float32/float16/bfloat16")
+        x2 = _rows(x)
+        y = softmax_fwd(x2)
+        ctx.save_for_backward(y)
+        ctx.x_shape = x.shape
+        return y.reshape(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        (y,) = ctx.saved_tensors
+        dy = _rows(dy.reshape(y.shape))
+        return softmax_bwd(y, dy).reshape(ctx.x_shape)
+
+
+def softmax(x: torch.Tensor) -> torch.Tensor:
+    return SoftmaxFunction.apply(x)
 
 
 def rms_norm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-5) -> torch.Tensor:

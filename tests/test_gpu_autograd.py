@@ -1,5 +1,6 @@
 """Autograd glue on the GPU: gradients through torch.autograd against the
-fp64 oracle, one gradient per forward argument (None for the flag),
+fp64 oracle (weighted sum, scaled SiLU, RMSNorm, LayerNorm, softmax), one
+gradient per forward argument (None for the flag),
 accumulation into .grad across micro-batches, the library's accumulate flag,
 non-contiguous inputs, leading batch dimensions, and a finite-difference
 gradcheck in fp32."""
@@ -197,3 +198,29 @@ def test_norm_modules_accumulate_grad(ag):
     r = ag.RMSNorm(256, device=DEV)
     r(x.to(torch.bfloat16)).float().sum().backward()
     assert r.weight.grad is not None and r.weight.grad.shape == (256,)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [1000, 50257])
+def test_softmax_autograd_matches_oracle(ag, dt, D):
+    # leading batch dimensions, a windowed width (50257) on the cluster path,
+    # and a non-contiguous incoming gradient
+    import inputgen
+    x = inputgen.make((2, 3, D), dt, NORMAL, 0, 2, 6, 0)
+    dy = inputgen.make((2, 3, D), dt, NORMAL, 0, 1, 6, 2)
+    xd = x.to(DEV).requires_grad_()
+    y = ag.softmax(xd)
+    assert y.shape == x.shape and y.dtype == x.dtype
+    y.backward(dy.to(DEV).transpose(0, 1).contiguous().transpose(0, 1))
+    x2, dy2 = x.reshape(-1, D), dy.reshape(-1, D)
+    ye, yo = oracle.softmax_fwd(x2)
+    assert check_elementwise(y.detach().cpu().reshape(-1, D), yo, ye)
+    r = oracle.softmax_bwd(y.detach().cpu().reshape(-1, D), dy2)
+    assert check_elementwise(xd.grad.cpu().reshape(-1, D), r["dx"], r["dx_exact"],
+                             scale=r["dx_scale"])
+
+
+def test_softmax_gradcheck_fp32(ag):
+    x = torch.randn(4, 9, device=DEV, dtype=torch.float32, requires_grad=True)
+    assert torch.autograd.gradcheck(ag.softmax, (x,), eps=1e-2, atol=2e-3, rtol=2e-3,
+                                    check_grad_dtypes=False, raise_exception=True)
