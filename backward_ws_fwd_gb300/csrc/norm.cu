@@ -557,6 +557,10 @@ __global__ void __launch_bounds__(NT, MINB)
 // shared memory and a CTA barrier, so every CTA derives the same bits of the
 // row statistics, with the arithmetic of the row path.
 //
+// RMSNorm keeps two rows in flight: the sums of row k + 1 are pushed before
+// the exchange of row k is awaited, so the exchange's latency overlaps the
+// next row's first pass (two turns outstanding: four exchange buffers).
+//
 // One exchange a row.  LayerNorm needs Σx before the sums over d = x − μ;
 // its Σx travels one row ahead: the exchange of row k carries the sums of
 // row k and Σx of row k + 1 (staged already), so that the mean of row k + 1
@@ -585,49 +589,56 @@ constexpr int64_t kNormClusterSmallMaxD = 16384;
 // backward stages (indexed by LayerNorm) and whether w sits in per-thread
 // shared-memory slots, for 16-bit and binary32 rows
 constexpr int kNormBwdStages16[2] = {3, 3};
-constexpr int kNormBwdStages32[2] = {2, 3};
+constexpr int kNormBwdStages32[2] = {3, 3};
 constexpr bool kNormBwdWSlots[2] = {true, true};
-constexpr int kNormFwdStages[2] = {3, 4};
+constexpr int kNormFwdStages[2] = {4, 4};
 constexpr int64_t kNormClusterRowMax = (int64_t)kClusterMaxCS * kNormClusterNT * 16;  // 65536
 
 // Waits of the cluster exchanges that ran out (see WarpPush); zero unless
 // the exchange protocol failed.
 __device__ unsigned g_norm_wait_timeouts;
 
-template <int NT>
-using NormPush = WarpPush<NT / 32, kClusterMaxCS*(NT / 32), 2>;
+template <int NT, int NB = 2, int NV = 2>
+using NormPush = WarpPush<NT / 32, kClusterMaxCS*(NT / 32), NV, NB>;
 
 __device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
     return comp ? group_sum2<32>(v) : Acc2{group_sum<32>(v.hi), 0.f};
 }
 
-// Sum K (up to 4) row sums over the cluster; sum q is compensated if bit q
-// of CM is set.  Every thread of every CTA of the cluster calls it together.
-// Warp 0 waits for the turn, combines the entries (lane ℓ takes entries ℓ,
-// ℓ+32, …, then an xor butterfly) and posts the sums in `res`; a CTA barrier
-// hands them to the other warps (and orders this turn's reads before any
-// warp's next push).
-// CMW: the sums compensated already inside each warp (a subset of CM); the
-// others are added plainly within a warp and compensated from the exchange on.
-template <int NT, int K, unsigned CM, unsigned CMW = CM>
-__device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp,
-                                               float4 (*res)[2]) {
+// Sum K (up to 4) row sums over the cluster in two steps.  cluster_push: each
+// warp's sums (xor butterfly; compensated for the sums in CMW) pushed as the
+// warp's entry; returns the turn.  cluster_finish: warp 0 waits for the turn,
+// combines the entries (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
+// butterfly; compensated for the sums in CM) and posts the sums in `res`; a
+// CTA barrier hands them to every warp (and orders the turn's reads before
+// any warp's later pushes).  Every thread of every CTA of the cluster calls
+// both together; other work may sit between them (another turn's push when
+// NB = 4).
+template <int NT, int K, unsigned CM, unsigned CMW, int NB, int NV>
+__device__ __forceinline__ unsigned cluster_push(Acc2 (&v)[K], NormPush<NT, NB, NV>& xp) {
     static_assert(K >= 1 && K <= 4, "up to four sums");
     static_assert((CMW & ~CM) == 0, "warp-level compensation implies exchange-level");
-    constexpr int W = NT / 32, NX = (K + 1) / 2;
-    const int lane = threadIdx.x & 31;
+    constexpr int NX = (K + 1) / 2;
+    Acc2 w[K];
 #pragma unroll
-    for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CMW >> q) & 1u);
+    for (int q = 0; q < K; q++) w[q] = warp_sum(v[q], (CMW >> q) & 1u);
     float4 e[NX];
 #pragma unroll
     for (int n = 0; n < NX; n++) {
-        const Acc2 a = v[2 * n], b = 2 * n + 1 < K ? v[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
+        const Acc2 a = w[2 * n], b = 2 * n + 1 < K ? w[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
         e[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
     }
-    const unsigned t = xp.template push<NX>(e);
+    return xp.template push<NX>(e);
+}
+
+template <int NT, int K, unsigned CM, int NB, int NV>
+__device__ __forceinline__ void cluster_finish(unsigned t, Acc2 (&v)[K], NormPush<NT, NB, NV>& xp,
+                                               float4 (*res)[2]) {
+    constexpr int W = NT / 32, NX = (K + 1) / 2;
+    const int lane = threadIdx.x & 31;
     float4* out = res[t & 1u];
     if (threadIdx.x < 32) {
-        const float4(*buf)[2] = xp.wait(t);
+        const float4(*buf)[NV] = xp.wait(t);
         const int total = (int)cluster_nctarank() * W;
         Acc2 s[K];
 #pragma unroll
@@ -665,6 +676,13 @@ __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT>& xp,
     }
 }
 
+template <int NT, int K, unsigned CM, unsigned CMW = CM, int NB, int NV>
+__device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT, NB, NV>& xp,
+                                               float4 (*res)[2]) {
+    const unsigned t = cluster_push<NT, K, CM, CMW, NB, NV>(v, xp);
+    cluster_finish<NT, K, CM, NB, NV>(t, v, xp, res);
+}
+
 // Σx over this thread's valid chunks of a staged row: binary32 elements with
 // TwoSum each; 16-bit elements (8 or 11 significant bits) in plain binary32,
 // as are the warp's 512 (fewer than 2^20 steps of one binade's grid): exact
@@ -695,6 +713,23 @@ __device__ __forceinline__ Acc2 staged_sum_x(const Raw16* slot, unsigned valid) 
     return s;
 }
 
+// Σx² over this thread's valid chunks of a staged row (the arithmetic of the
+// in-register Σ d² of RMSNorm).
+template <typename E, int CPT, int NT, int V, bool Comp>
+__device__ __forceinline__ Acc2 staged_sum_sq(const Raw16* slot, unsigned valid) {
+    Acc2 s = acc2_zero();
+#pragma unroll
+    for (int c = 0; c < CPT; c++) {
+        if (valid >> c & 1u) {
+            float f[V];
+            E::widen(slot[c * NT], f);
+#pragma unroll
+            for (int v = 0; v < V; v++) s_fma<Comp>(s, f[v], f[v]);
+        }
+    }
+    return s;
+}
+
 template <int CPT, int V>
 __device__ __forceinline__ void center(float (&f)[CPT][V], unsigned valid, const Mean& m) {
 #pragma unroll
@@ -712,13 +747,18 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     using E = Elt<T>;
     constexpr int V = E::V, CPT = 16 / V;
     constexpr bool C = std::is_same<T, float>::value;
-    static_assert(S >= (LN ? 3 : 2), "LayerNorm holds two staged rows");
+    // RMSNorm keeps two rows in flight: row k + 1's Σx² is pushed before
+    // row k's exchange is awaited (four exchange buffers, see WarpPush)
+    constexpr bool PIPE = !LN;
+    constexpr int NB = PIPE ? 4 : 2;
+    static_assert(S >= 3, "two staged rows");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
-    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
-    __shared__ __align__(8) uint64_t xbar[2];
+    constexpr int NV = LN ? 2 : 1;  // float4 an entry
+    __shared__ __align__(16) float4 xbuf[NB][kClusterMaxCS * (NT / 32)][NV];
+    __shared__ __align__(8) uint64_t xbar[NB];
     __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
-    NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
+    NormPush<NT, NB, NV> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
     xc.init();
     cluster_sync();
     const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;  // chunk l + c·NT
@@ -747,31 +787,40 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
+    if (PIPE && iters > 0) {  // the first row's Σx², turn 0
+        cp_async_wait<S - 2>();
+        Acc2 q[1] = {staged_sum_sq<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
+        cluster_push<NT, 1, C ? 1u : 0u, C ? 1u : 0u>(q, xc);
+    }
     for (int64_t k = 0; k < iters; k++) {
-        if constexpr (LN)
-            cp_async_wait<(LN ? S - 3 : 0)>();  // rows k and k + 1
-        else
-            cp_async_wait<S - 2>();
+        cp_async_wait<S - 3>();  // rows k and k + 1
         if (k + S - 1 < iters) stage_row<NT, CPT, NT>(xs + ((k + S - 1) % S) * CPT * NT, stg, valid);
         cp_async_commit();
         float f[CPT][V];
         load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
         if constexpr (LN) center<CPT, V>(f, valid, mn);
+        if constexpr (PIPE) {
+            if (k + 1 < iters) {  // row k + 1's Σx², turn k + 1
+                Acc2 q[1] = {staged_sum_sq<E, CPT, NT, V, C>(
+                    xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)};
+                cluster_push<NT, 1, C ? 1u : 0u, C ? 1u : 0u>(q, xc);
+            }
+        }
         // Σ d², d = x (RMSNorm) or x − μ (LayerNorm); LayerNorm: Σx of row k + 1
         Acc2 sm[LN ? 2 : 1];
         sm[0] = acc2_zero();
-#pragma unroll
-        for (int c = 0; c < CPT; c++)
-            if (valid >> c & 1u)
-#pragma unroll
-                for (int v = 0; v < V; v++) s_fma<C>(sm[0], f[c][v], f[c][v]);
         if constexpr (LN) {
+#pragma unroll
+            for (int c = 0; c < CPT; c++)
+                if (valid >> c & 1u)
+#pragma unroll
+                    for (int v = 0; v < V; v++) s_fma<C>(sm[0], f[c][v], f[c][v]);
             sm[LN ? 1 : 0] = k + 1 < iters
                 ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
                 : acc2_zero();
             cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u, C ? 3u : 0u>(sm, xc, xres);
         } else {
-            cluster_reduce<NT, 1, C ? 1u : 0u>(sm, xc, xres);
+            cluster_finish<NT, 1, C ? 1u : 0u>((unsigned)k, sm, xc, xres);  // row k's turn
         }
         const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
         if constexpr (LN) mn = mean_of(sm[LN ? 1 : 0], fd, inv_d);
@@ -822,18 +871,22 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     using E = Elt<T>;
     constexpr int V = E::V, CPT = 16 / V;
     constexpr bool C = std::is_same<T, float>::value;
-    static_assert(S >= (LN ? 3 : 2), "LayerNorm holds two staged rows");
+    static_assert(S >= 3, "two staged rows");
     // sums: Σ d², Σ g·d[, Σ g, Σx of the next row]
     constexpr int K = LN ? 4 : 2;
     constexpr unsigned CM = (C ? (LN ? 7u : 3u) : 0u) | (LN ? 8u : 0u);
+    // RMSNorm keeps two rows in flight: row k + 1's sums are pushed before
+    // row k's exchange is awaited (four exchange buffers, see WarpPush)
+    constexpr bool PIPE = !LN;
+    constexpr int NB = PIPE ? 4 : 2, NV = LN ? 2 : 1;
     const int64_t D = (int64_t)Dv * V;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
-    __shared__ __align__(16) float4 xbuf[2][kClusterMaxCS * (NT / 32)][2];
-    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ __align__(16) float4 xbuf[NB][kClusterMaxCS * (NT / 32)][NV];
+    __shared__ __align__(8) uint64_t xbar[NB];
     __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
-    NormPush<NT> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
+    NormPush<NT, NB, NV> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
     xc.init();
     cluster_sync();
     const int l = (int)cluster_ctarank() * NT * CPT + (int)threadIdx.x;
@@ -913,6 +966,27 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         stage(k);
         cp_async_commit();
     }
+    // RMSNorm's sums of the staged row in `slot`: Σ x², Σ g·x, g = dy·w
+    auto rms_sums = [&](int slot, Acc2 (&q)[K]) {
+        const Raw16* px = xs + slot * CPT * NT + threadIdx.x;
+        const Raw16* pg = gs + slot * CPT * NT + threadIdx.x;
+#pragma unroll
+        for (int n = 0; n < K; n++) q[n] = acc2_zero();
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            if (valid >> c & 1u) {
+                float dc[V], gc[V], wc[V];
+                E::widen(px[c * NT], dc);
+                E::widen(pg[c * NT], gc);
+                w_of(c, wc);
+#pragma unroll
+                for (int v = 0; v < V; v++) {
+                    s_fma<C>(q[0], dc[v], dc[v]);
+                    s_fma<C>(q[1], gc[v] * wc[v], dc[v]);
+                }
+            }
+        }
+    };
     Mean mn{0.f, 0.f};
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
@@ -920,11 +994,14 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
         mn = mean_of(s0[0], fd, inv_d);
     }
+    if (PIPE && iters > 0) {  // the first row's sums, turn 0
+        cp_async_wait<S - 2>();
+        Acc2 q[K];
+        rms_sums(0, q);
+        cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
+    }
     for (int64_t k = 0; k < iters; k++) {
-        if constexpr (LN)
-            cp_async_wait<(LN ? S - 3 : 0)>();  // rows k and k + 1
-        else
-            cp_async_wait<S - 2>();
+        cp_async_wait<S - 3>();  // rows k and k + 1
         stage((int)((k + S - 1) % S));
         cp_async_commit();
         const int64_t row = cw.row;
@@ -939,29 +1016,38 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 for (int v = 0; v < V; v++) o[v] = (o[v] - mn.mu0) - mn.c;
         };
         Acc2 sums[K];
+        if constexpr (PIPE) {
+            if (k + 1 < iters) {  // row k + 1's sums, turn k + 1
+                Acc2 q[K];
+                rms_sums((int)((k + 1) % S), q);
+                cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
+            }
+            cluster_finish<NT, K, CM>((unsigned)k, sums, xc, xres);  // row k's turn
+        } else {
 #pragma unroll
-        for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+            for (int q = 0; q < K; q++) sums[q] = acc2_zero();
 #pragma unroll
-        for (int c = 0; c < CPT; c++) {
-            if (valid >> c & 1u) {
-                float dc[V], gc[V], wc[V];
-                d_of(c, dc);
-                E::widen(cg[c * NT], gc);
-                w_of(c, wc);
+            for (int c = 0; c < CPT; c++) {
+                if (valid >> c & 1u) {
+                    float dc[V], gc[V], wc[V];
+                    d_of(c, dc);
+                    E::widen(cg[c * NT], gc);
+                    w_of(c, wc);
 #pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float gg = gc[v] * wc[v];
-                    s_fma<C>(sums[0], dc[v], dc[v]);
-                    s_fma<C>(sums[1], gg, dc[v]);
-                    if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
+                    for (int v = 0; v < V; v++) {
+                        const float gg = gc[v] * wc[v];
+                        s_fma<C>(sums[0], dc[v], dc[v]);
+                        s_fma<C>(sums[1], gg, dc[v]);
+                        if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
+                    }
                 }
             }
+            if constexpr (LN)
+                if (k + 1 < iters)
+                    sums[LN ? 3 : 0] = staged_sum_x<E, CPT, NT, V, C>(
+                        xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
+            cluster_reduce<NT, K, CM, C ? CM : 0u>(sums, xc, xres);
         }
-        if constexpr (LN)
-            if (k + 1 < iters)
-                sums[LN ? 3 : 0] =
-                    staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
-        cluster_reduce<NT, K, CM, C ? CM : 0u>(sums, xc, xres);
         const float r = rstd_of<C>(s_val(sums[0]), inv_d, eps);
         const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
         const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;

@@ -331,25 +331,26 @@ __device__ __forceinline__ void st_async_f32x4(uint32_t dst, float4 v, uint32_t 
 // One entry a warp (NV float4, the same in every lane) exchanged among the
 // CTAs of a cluster: lane q of each warp pushes the warp's entry into slot
 // rank·W + warp of CTA q; a CTA's turn is complete when the entries of all
-// cs·W warps of the cluster have arrived in its own buffer.  Turns alternate
-// between two buffers, each with its own mbarrier (phase parity = turn/2).
+// cs·W warps of the cluster have arrived in its own buffer.  Turns cycle
+// through NB buffers, each with its own mbarrier (phase parity = turn/NB).
 // Thread 0 posts the bytes expected (pushes that land before it leave the
 // phase pending); the threads that wait (wait()) may then read the turn's
-// buffer.  A buffer is written again two turns later, which no CTA can reach
-// before every CTA has finished reading it, provided that each warp pushes
-// turn t + 1 only after this CTA's readers of turn t are done (the callers
-// put a CTA barrier between them) and that every turn is waited for by
-// thread 0.  A wait longer than limit_ns (a second unless set) marks the
-// exchange dead for the waiting thread (later waits are skipped) and counts a
-// timeout (one a warp), so that a
-// fault in the protocol ends the kernel with wrong results and a raised
-// counter instead of a hang.  Each CTA of a cluster must run the same turns,
-// and every CTA's barriers must be initialised (init(), then a cluster
-// barrier) before the first push.
-template <int W, int SLOTS, int NV>
+// buffer.  A buffer is written again NB turns later, which no CTA can reach
+// before every CTA has finished reading it, provided that a warp pushes turn
+// t + NB − 1 only after this CTA's readers of turn t are done (the callers
+// put a CTA barrier between them: NB = 2 when a CTA pushes turn t + 1 after
+// reading turn t, NB = 4 when it pushes turn t + 1 before reading turn t)
+// and that every turn is waited for by thread 0.  A wait longer than
+// limit_ns (a second unless set) marks the exchange dead for the waiting
+// thread (later waits are skipped) and counts a timeout (one a warp), so
+// that a fault in the protocol ends the kernel with wrong results and a
+// raised counter instead of a hang.  Each CTA of a cluster must run the same
+// turns, and every CTA's barriers must be initialised (init(), then a
+// cluster barrier) before the first push.
+template <int W, int SLOTS, int NV, int NB = 2>
 struct WarpPush {
-    float4 (*buf)[SLOTS][NV];  // shared [2][SLOTS][NV]
-    uint64_t* bar;             // shared [2]
+    float4 (*buf)[SLOTS][NV];  // shared [NB][SLOTS][NV]
+    uint64_t* bar;             // shared [NB]
     unsigned* timeouts;        // device counter of waits that ran out
     unsigned turn;
     bool live;
@@ -357,8 +358,8 @@ struct WarpPush {
 
     __device__ __forceinline__ void init() {
         if (threadIdx.x == 0) {
-            mbar_init(&bar[0], 1);
-            mbar_init(&bar[1], 1);
+#pragma unroll
+            for (int i = 0; i < NB; i++) mbar_init(&bar[i], 1);
             mbar_init_fence();
         }
     }
@@ -367,7 +368,7 @@ struct WarpPush {
     template <int NX>
     __device__ __forceinline__ unsigned push(const float4 (&e)[NX]) {
         static_assert(NX >= 1 && NX <= NV, "entry size");
-        const unsigned t = turn++, p = t & 1u;
+        const unsigned t = turn++, p = t % NB;
         const unsigned cs = cluster_nctarank(), me = cluster_ctarank();
         const unsigned lane = threadIdx.x & 31u, wid = threadIdx.x >> 5;
         if (threadIdx.x == 0) mbar_expect_tx(&bar[p], cs * W * NX * 16u);
@@ -382,11 +383,11 @@ struct WarpPush {
 
     // Wait until turn t is complete; returns its buffer.
     __device__ __forceinline__ const float4 (*wait(unsigned t))[NV] {
-        if (live && !mbar_wait(&bar[t & 1u], (t >> 1) & 1u, limit_ns)) {
+        if (live && !mbar_wait(&bar[t % NB], (t / NB) & 1u, limit_ns)) {
             live = false;
             if ((threadIdx.x & 31u) == 0) atomicAdd(timeouts, 1u);
         }
-        return buf[t & 1u];
+        return buf[t % NB];
     }
 };
 
