@@ -105,7 +105,8 @@ def test_capture_and_replay_match_eager(wsf):
 
 
 def test_capture_cluster_paths(wsf):
-    # wide rows take thread-block clusters; run alone, this test makes the
+    # wide rows take thread-block clusters (and fp32 rows of 140,000 the
+    # two-pass cluster kernels); run alone, this test makes the
     # first use of the fp16 softmax cluster kernels inside the capture (their
     # one-time occupancy query and kernel attributes happen there), while the
     # bf16 norm kernels were used eagerly before
@@ -113,6 +114,8 @@ def test_capture_cluster_paths(wsf):
     eps = 2.0 ** -17
     x16 = torch.randn(64, 36000, device=DEV, generator=g).half()
     dy16 = torch.randn(64, 36000, device=DEV, generator=g).half()
+    x32 = torch.randn(6, 140000, device=DEV, generator=g)  # two-pass rows
+    dy32 = torch.randn(6, 140000, device=DEV, generator=g)
     xb = torch.randn(300, 20000, device=DEV, generator=g).bfloat16()
     dyb = torch.randn(300, 20000, device=DEV, generator=g).bfloat16()
     wn = 1 + 0.1 * torch.randn(20000, device=DEV, generator=g)
@@ -123,6 +126,7 @@ def test_capture_cluster_paths(wsf):
 
     def outs():
         return {"ym": torch.empty_like(x16), "dxm": torch.empty_like(x16),
+                "y2": torch.empty_like(x32), "dx2": torch.empty_like(x32),
                 "yn": torch.empty_like(xb), "dxn": torch.empty_like(xb),
                 "gw": torch.empty(20000, device=DEV), "gb": torch.empty(20000, device=DEV),
                 "ws": torch.empty(wsf.norm_bwd_workspace_bytes(300, 20000, torch.bfloat16, True),
@@ -131,6 +135,8 @@ def test_capture_cluster_paths(wsf):
     def step(o, s):
         wsf.softmax_fwd(x16, y=o["ym"], stream=s)
         wsf.softmax_bwd(o["ym"], dy16, dx=o["dxm"], stream=s)
+        wsf.softmax_fwd(x32, y=o["y2"], stream=s)
+        wsf.softmax_bwd(o["y2"], dy32, dx=o["dx2"], stream=s)
         wsf.layernorm_fwd(xb, wn, bn, eps, y=o["yn"], stream=s)
         wsf.layernorm_bwd(xb, wn, dyb, eps, dx=o["dxn"], grad_w=o["gw"], grad_b=o["gb"],
                           workspace=o["ws"], stream=s)

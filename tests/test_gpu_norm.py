@@ -182,7 +182,8 @@ def test_norm_accumulate_reproducible_empty(wsf, layer):
 @pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
 @pytest.mark.parametrize("dt", DTS)
 @pytest.mark.parametrize("N,D", [(300, 8200), (200, 12288), (130, 16384), (40, 32768),
-                                 (37, 36864), (20, 50000), (9, 65536), (3, 65544)])
+                                 (37, 36864), (20, 50000), (9, 65536), (3, 65544),
+                                 (1, 20000), (2, 40000)])  # clusters with no row or one
 def test_norm_cluster_rows(wsf, layer, dt, N, D):
     x, w, dy, b = _inputs(N, D, dt, seed=D % 97)
     _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b))
