@@ -42,7 +42,7 @@ ORDER_BWD = ["c5", "c4", "c3", "c2"]
 KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2, "softmax_fwd": 1,
                   "softmax_bwd": 1, "rmsnorm_fwd": 1, "rmsnorm_bwd": 2, "layernorm_fwd": 1,
                   "layernorm_bwd": 2}
-EXTRA = ["s1", "n1", "n2", "s2", "n3", "n4"]  # measured only when named with --workload
+EXTRA = ["s1", "n1", "n2", "s2", "n3", "n4", "s3", "s4"]  # measured only when named
 NORMS = ("rmsnorm", "layernorm")
 
 
@@ -288,7 +288,9 @@ EXTRA_LABELS = {"s1": "row softmax s1 (bf16 x[65536,4096])",
                 "n2": "LayerNorm n2 (bf16 x[65536,4096])",
                 "s2": "row softmax s2 (bf16 x[4096,131072])",
                 "n3": "RMSNorm n3 (bf16 x[16384,16384])",
-                "n4": "LayerNorm n4 (bf16 x[16384,16384])"}
+                "n4": "LayerNorm n4 (bf16 x[16384,16384])",
+                "s3": "row softmax s3 (bf16 x[8192,50257])",
+                "s4": "row softmax s4 (fp32 x[2048,262144])"}
 
 
 def workload_label(names):
@@ -775,7 +777,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default="all",
-                    help="all (c2..c5) or a comma list of c2,c3,c4,c5,s1,n1,n2,s2,n3,n4")
+                    help="all (c2..c5) or a comma list of c2,c3,c4,c5,s1,n1,n2,s2,n3,n4,s3,s4")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="multiply every workload's row count (profiling on small cases)")
     ap.add_argument("--compare-atomic", action="store_true",

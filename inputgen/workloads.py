@@ -80,6 +80,15 @@ WORKLOADS = {
     "s2": Workload("s2", "softmax", "bf16", 4096, 131072, x=Dist(NORMAL, 0.0, 2.0),
                    dy=Dist(NORMAL, 0.0, 1.0),
                    note="row softmax, bf16 x[4096,131072] ~N(0,2), dy ~N(0,1)"),
+    # softmax rows of an odd width (a GPT-2-sized vocabulary of 50,257: rows
+    # read as the 16-byte chunks that cover them) and fp32 rows wider than the
+    # cluster rows hold (two passes)
+    "s3": Workload("s3", "softmax", "bf16", 8192, 50257, x=Dist(NORMAL, 0.0, 2.0),
+                   dy=Dist(NORMAL, 0.0, 1.0),
+                   note="row softmax, bf16 x[8192,50257] ~N(0,2), dy ~N(0,1)"),
+    "s4": Workload("s4", "softmax", "f32", 2048, 262144, x=Dist(NORMAL, 0.0, 2.0),
+                   dy=Dist(NORMAL, 0.0, 1.0),
+                   note="row softmax, fp32 x[2048,262144] ~N(0,2), dy ~N(0,1)"),
     "n3": Workload("n3", "rmsnorm", "bf16", 16384, 16384, x=Dist(NORMAL, 0.0, 1.0),
                    w=Dist(NORMAL, 1.0, 0.1), dy=Dist(NORMAL, 0.0, 1.0), eps=2.0 ** -17,
                    note="RMSNorm, bf16 x[16384,16384] ~N(0,1), w ~N(1,0.1), eps 2^-17"),

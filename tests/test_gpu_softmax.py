@@ -261,7 +261,7 @@ def test_softmax_cluster_strides(wsf, dt):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["s1", "s2"])
+@pytest.mark.parametrize("name", ["s1", "s2", "s3", "s4"])
 def test_softmax_measurement_size_sampled(wsf, name):
     import inputgen
     from inputgen.workloads import WORKLOADS
