@@ -829,18 +829,20 @@ __device__ __forceinline__ void prefetch_slice(const T* row_start, int D, int c0
     const int off = win_off<T, U>(row_start);
     const int nc = (off + D + V - 1) / V;
     const int e = c0 + SL < nc ? c0 + SL : nc;
-    if (e > c0) prefetch_l2_bulk(row_start - off + (int64_t)c0 * V, (uint32_t)(e - c0) * 16u);
+    if (e > c0)
+        prefetch_l2_bulk(row_start - off + (int64_t)c0 * V, (uint32_t)(e - c0) * 16u,
+                         l2_evict_last());
 }
 
 // The raw chunks c0 + b + u·NT (u < NU) of a row: the row's own 16-byte
 // blocks, zeros for chunks past the slice or the row.
 template <typename T, bool U, int NU>
 __device__ __forceinline__ void load_batch(Raw16 (&r)[NU], const T* row_start, const Win<T, U>& w,
-                                           int c0, int b, int SL) {
+                                           int c0, int b, int SL, uint64_t pol) {
 #pragma unroll
     for (int u = 0; u < NU; u++) {
         const int c = b + u * kTwoPassNT;
-        r[u] = (c < SL && w.has(c0 + c)) ? ld_stream(row_start + w.at(c0 + c)) : raw_zero();
+        r[u] = (c < SL && w.has(c0 + c)) ? ld_policy(row_start + w.at(c0 + c), pol) : raw_zero();
     }
 }
 
@@ -884,10 +886,13 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
     const int c0 = (int)cluster_ctarank() * SL;  // this CTA's chunks [c0, c0 + SL)
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     pdl_wait();
+    // first-pass reads keep their lines in L2 for the second (evict_last);
+    // the second pass is their last use (evict_first)
+    const uint64_t keep = l2_evict_last(), last = l2_evict_first();
     Raw16 nb[UU];  // the next batch's raw chunks
     if (cid < N) {
         const T* x0 = x + cid * ldx;
-        load_batch<T, U, UU>(nb, x0, Win<T, U>{win_off<T, U>(x0), D}, c0, threadIdx.x, SL);
+        load_batch<T, U, UU>(nb, x0, Win<T, U>{win_off<T, U>(x0), D}, c0, threadIdx.x, SL, keep);
     }
     for (int64_t row = cid; row < N; row += ncl) {
         const T* xr = x + row * ldx;
@@ -901,7 +906,10 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
 #pragma unroll
             for (int u = 0; u < UU; u++) cur[u] = nb[u];
             // the next batch, or the second pass's first
-            load_batch<T, U, UU>(nb, xr, win, c0, b + STEP < SL ? b + STEP : (int)threadIdx.x, SL);
+            if (b + STEP < SL)
+                load_batch<T, U, UU>(nb, xr, win, c0, b + STEP, SL, keep);
+            else
+                load_batch<T, U, UU>(nb, xr, win, c0, threadIdx.x, SL, last);
             float mb = m;
 #pragma unroll
             for (int u = 0; u < UU; u++) {
@@ -986,10 +994,11 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
 #pragma unroll
             for (int u = 0; u < UU; u++) cur[u] = nb[u];
             if (b + STEP < SL) {
-                load_batch<T, U, UU>(nb, xr, win, c0, b + STEP, SL);
+                load_batch<T, U, UU>(nb, xr, win, c0, b + STEP, SL, last);
             } else if (row + ncl < N) {  // the next row's first batch
                 const T* xn = xr + ncl * ldx;
-                load_batch<T, U, UU>(nb, xn, Win<T, U>{win_off<T, U>(xn), D}, c0, threadIdx.x, SL);
+                load_batch<T, U, UU>(nb, xn, Win<T, U>{win_off<T, U>(xn), D}, c0, threadIdx.x, SL,
+                                     keep);
             }
 #pragma unroll
             for (int u = 0; u < UU; u++) {
@@ -1032,12 +1041,13 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
     const int c0 = (int)cluster_ctarank() * SL;
     const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
     pdl_wait();
+    const uint64_t keep = l2_evict_last(), last = l2_evict_first();  // as in the forward
     Raw16 ny[UU], ng[UU];  // the next batch's raw chunks of y and dy
     if (cid < N) {
         const T* y0 = y + cid * ldy;
         const Win<T, U> w0{win_off<T, U>(y0), D};
-        load_batch<T, U, UU>(ny, y0, w0, c0, threadIdx.x, SL);
-        load_batch<T, U, UU>(ng, dy + cid * lddy, w0, c0, threadIdx.x, SL);
+        load_batch<T, U, UU>(ny, y0, w0, c0, threadIdx.x, SL, keep);
+        load_batch<T, U, UU>(ng, dy + cid * lddy, w0, c0, threadIdx.x, SL, keep);
     }
     for (int64_t row = cid; row < N; row += ncl) {
         const T* yr = y + row * ldy;
@@ -1053,9 +1063,10 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
                 cg[u] = ng[u];
             }
             // the next batch, or the second pass's first
-            const int bn = b + STEP < SL ? b + STEP : (int)threadIdx.x;
-            load_batch<T, U, UU>(ny, yr, win, c0, bn, SL);
-            load_batch<T, U, UU>(ng, gr, win, c0, bn, SL);
+            const bool more = b + STEP < SL;
+            const int bn = more ? b + STEP : (int)threadIdx.x;
+            load_batch<T, U, UU>(ny, yr, win, c0, bn, SL, more ? keep : last);
+            load_batch<T, U, UU>(ng, gr, win, c0, bn, SL, more ? keep : last);
 #pragma unroll
             for (int u = 0; u < UU; u++) {
                 float fy[V], fg[V];
@@ -1108,13 +1119,13 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
                 cg[u] = ng[u];
             }
             if (b + STEP < SL) {
-                load_batch<T, U, UU>(ny, yr, win, c0, b + STEP, SL);
-                load_batch<T, U, UU>(ng, gr, win, c0, b + STEP, SL);
+                load_batch<T, U, UU>(ny, yr, win, c0, b + STEP, SL, last);
+                load_batch<T, U, UU>(ng, gr, win, c0, b + STEP, SL, last);
             } else if (row + ncl < N) {  // the next row's first batch
                 const T* yn = yr + ncl * ldy;
                 const Win<T, U> wn{win_off<T, U>(yn), D};
-                load_batch<T, U, UU>(ny, yn, wn, c0, threadIdx.x, SL);
-                load_batch<T, U, UU>(ng, gr + ncl * lddy, wn, c0, threadIdx.x, SL);
+                load_batch<T, U, UU>(ny, yn, wn, c0, threadIdx.x, SL, keep);
+                load_batch<T, U, UU>(ng, gr + ncl * lddy, wn, c0, threadIdx.x, SL, keep);
             }
 #pragma unroll
             for (int u = 0; u < UU; u++) {

@@ -68,10 +68,35 @@ __device__ __forceinline__ void st_stream(void* p, const Raw16& r) {
                  : "memory");
 }
 
+// L2 cache policies: lines read under evict_last stay ahead of others, lines
+// read under evict_first are the first to leave.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Read of 16 bytes (read-only path, no L1 allocation) under an L2 policy.
+__device__ __forceinline__ Raw16 ld_policy(const void* p, uint64_t pol) {
+    Raw16 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.u[0]), "=r"(r.u[1]), "=r"(r.u[2]), "=r"(r.u[3])
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16) from global memory into L2,
-// starting at a 16-byte aligned address; nothing waits for it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+// starting at a 16-byte aligned address, under an L2 policy; nothing waits
+// for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p),
+                 "r"(bytes), "l"(pol)
+                 : "memory");
 }
 
 // Asynchronous 16-byte global -> shared copy (cp.async, bypassing L1, with a
