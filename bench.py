@@ -752,18 +752,29 @@ def read_traffic(kernel: str, workload: str):
         with open(path) as f:
             t = json.load(f)
         e = t.get(f"{kernel}:{workload}")
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("source_hash") == source_hash(kernel.rsplit("_", 1)[0]):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
     return None
 
 
-def source_hash() -> str:
+# the kernel source of each operator; every operator also depends on the
+# shared device helpers, the launch helpers and the C entry points
+OP_SOURCES = {"silu": "silu.cu", "ws": "ws.cu", "rmsnorm": "norm.cu", "layernorm": "norm.cu",
+              "softmax": "softmax.cu"}
+SHARED_SOURCES = ("abi.cu", "wsf_device.cuh", "wsf_internal.h")
+
+
+def source_hash(op: str | None = None) -> str:
+    """Hash of the kernel sources an operator is built from (all of them for
+    op=None): a DRAM-traffic capture stays valid while its operator's hash
+    is unchanged."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "backward_ws_fwd_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    files = sorted(os.listdir(d)) if op is None else sorted((OP_SOURCES[op],) + SHARED_SOURCES)
+    for f in files:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
