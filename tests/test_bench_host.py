@@ -76,3 +76,30 @@ def test_max_over_ranks_gloo():
 
 def test_max_over_ranks_single_process():
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_traffic_records_keyed_by_operator_sources(tmp_path, monkeypatch):
+    # every record names a known operator and carries that operator's hash
+    # format; a change to one operator's kernel file voids only its records
+    import json
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        t = json.load(f)
+    ops = {k.split(":")[0].rsplit("_", 1)[0] for k in t if not k.startswith("_")}
+    assert ops <= set(bench.OP_SOURCES)
+    for k, e in t.items():
+        if not k.startswith("_"):
+            assert len(e["source_hash"]) == 16 and int(e["source_hash"], 16) >= 0
+            assert e["dram_bytes_per_launch"] > 0 and e["algorithmic_bytes"] > 0
+    src = os.path.join(bench.ROOT, "backward_ws_fwd_gb300", "csrc")
+    fake = tmp_path / "backward_ws_fwd_gb300" / "csrc"
+    fake.mkdir(parents=True)
+    for name in os.listdir(src):
+        (fake / name).write_bytes(open(os.path.join(src, name), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    before = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
+    (fake / "norm.cu").write_bytes((fake / "norm.cu").read_bytes() + b"\n// edit\n")
+    after = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
+    assert {op for op in before if before[op] != after[op]} == {"rmsnorm", "layernorm"}
+    (fake / "wsf_device.cuh").write_bytes((fake / "wsf_device.cuh").read_bytes() + b"\n")
+    final = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
+    assert all(final[op] != after[op] for op in bench.OP_SOURCES)
