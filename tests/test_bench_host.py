@@ -103,3 +103,27 @@ def test_traffic_records_keyed_by_operator_sources(tmp_path, monkeypatch):
     (fake / "wsf_device.cuh").write_bytes((fake / "wsf_device.cuh").read_bytes() + b"\n")
     final = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
     assert all(final[op] != after[op] for op in bench.OP_SOURCES)
+
+
+def test_reference_arm_line_contract():
+    # the reference arm is the fp64 oracle on the host cores: it needs no
+    # GPU, and its one JSON line carries the fields of the benchmark contract
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=300, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["unit"] == "GB/s" and d["value"] > 0 and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"]
