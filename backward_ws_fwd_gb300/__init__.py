@@ -104,11 +104,36 @@ def _dtype_code(t) -> int:
         raise TypeError(f"unsupported storage type {t.dtype}") from None
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The CUDA stream to launch on: `stream`, else the current stream of
+    `device` (the tensors' device)."""
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on(t):
+    """Make the device of tensor t current for the call: the C entry points
+    launch on the current device (and ws_bwd_noalloc picks that device's
+    scratch array)."""
+    import contextlib
+    import torch
+    if t is not None and t.is_cuda:
+        return torch.cuda.device(t.device)
+    return contextlib.nullcontext()
+
+
+def _scratch(nbytes, device, stream):
+    """A temporary workspace.  It is freed when the call returns, while the
+    kernels may still use it on `stream`: record that use, so the caching
+    allocator does not hand the memory out before `stream` reaches this
+    point (allocations on the device's current stream need nothing)."""
+    import torch
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if stream is not None:
+        t.record_stream(stream)
+    return t
 
 
 def _ptr(t):
@@ -142,8 +167,9 @@ def ws_fwd(x, w, y=None, stream=None):
     N, D = x.shape
     if y is None:
         y = torch.empty(N, dtype=x.dtype, device=x.device)
-    _check(lib.ws_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(y), N, D, _dtype_code(x),
-                      _stream(stream)), "ws_fwd")
+    with _on(x):
+        _check(lib.ws_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(y), N, D, _dtype_code(x),
+                          _stream(stream, x.device)), "ws_fwd")
     return y
 
 
@@ -158,29 +184,32 @@ def ws_bwd(x, w, dy, dx=None, grad_w=None, accumulate=False, workspace=None, blo
     if grad_w is None:
         grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
     need = lib.ws_bwd_workspace_bytes(N, D, code, block_n)
-    if workspace is None and need not in (0, SIZE_MAX):
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib.ws_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
-                      _ptr(grad_w), int(bool(accumulate)), _ptr(workspace), wbytes, block_n, N, D,
-                      code, _stream(stream)), "ws_bwd")
+    with _on(x):
+        if workspace is None and need not in (0, SIZE_MAX):
+            workspace = _scratch(need, x.device, stream)
+        wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(lib.ws_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
+                          _ptr(grad_w), int(bool(accumulate)), _ptr(workspace), wbytes, block_n,
+                          N, D, code, _stream(stream, x.device)), "ws_bwd")
     return dx, grad_w
 
 
 def ws_bwd_noalloc(x, w, dy, dx=None, grad_w=None, accumulate=False, block_n=0, stream=None):
     """ws_bwd without a workspace argument, for callers that cannot allocate
-    device memory: the partials use the library's fixed 4 MiB scratch array
-    (sizes that need more are rejected).  dx and grad_w must be supplied by
-    such callers; they are allocated here only for convenience when None."""
+    device memory: the partials use the library's fixed 8 MiB scratch array
+    on x's device (sizes that need more are rejected).  dx and grad_w must be
+    supplied by such callers; they are allocated here only for convenience
+    when None."""
     import torch
     N, D = x.shape
     if dx is None:
         dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
     if grad_w is None:
         grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
-    _check(lib.ws_bwd_noalloc(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
-                              _ptr(grad_w), int(bool(accumulate)), block_n, N, D, _dtype_code(x),
-                              _stream(stream)), "ws_bwd_noalloc")
+    with _on(x):
+        _check(lib.ws_bwd_noalloc(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx),
+                                  dx.stride(0), _ptr(grad_w), int(bool(accumulate)), block_n, N,
+                                  D, _dtype_code(x), _stream(stream, x.device)), "ws_bwd_noalloc")
     return dx, grad_w
 
 
@@ -193,9 +222,10 @@ def ws_bwd_atomic(x, w, dy, dx=None, grad_w=None, accumulate=False, stream=None)
         dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
     if grad_w is None:
         grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
-    _check(lib.ws_bwd_atomic(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
-                             _ptr(grad_w), int(bool(accumulate)), N, D, _dtype_code(x),
-                             _stream(stream)), "ws_bwd_atomic")
+    with _on(x):
+        _check(lib.ws_bwd_atomic(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), _ptr(dx), dx.stride(0),
+                                 _ptr(grad_w), int(bool(accumulate)), N, D, _dtype_code(x),
+                                 _stream(stream, x.device)), "ws_bwd_atomic")
     return dx, grad_w
 
 
@@ -207,9 +237,11 @@ def silu_bwd_atomic(dy, x, w, dx=None, dw=None, accumulate=False, stream=None):
         dx = torch.empty_like(x)
     if dw is None:
         dw = torch.empty(1, dtype=torch.float32, device=x.device)
-    _check(lib.silu_bwd_atomic(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), ctypes.c_void_p(dw.data_ptr()),
-                               int(bool(accumulate)), x.numel(), _dtype_code(x), _stream(stream)),
-           "silu_bwd_atomic")
+    with _on(x):
+        _check(lib.silu_bwd_atomic(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx),
+                                   ctypes.c_void_p(dw.data_ptr()), int(bool(accumulate)),
+                                   x.numel(), _dtype_code(x), _stream(stream, x.device)),
+               "silu_bwd_atomic")
     return dx, dw
 
 
@@ -219,8 +251,9 @@ def softmax_fwd(x, y=None, stream=None):
     N, D = x.shape
     if y is None:
         y = torch.empty((N, D), dtype=x.dtype, device=x.device)
-    _check(lib.softmax_fwd(_ptr(x), x.stride(0), _ptr(y), y.stride(0), N, D, _dtype_code(x),
-                           _stream(stream)), "softmax_fwd")
+    with _on(x):
+        _check(lib.softmax_fwd(_ptr(x), x.stride(0), _ptr(y), y.stride(0), N, D, _dtype_code(x),
+                               _stream(stream, x.device)), "softmax_fwd")
     return y
 
 
@@ -230,8 +263,10 @@ def softmax_bwd(y, dy, dx=None, stream=None):
     N, D = y.shape
     if dx is None:
         dx = torch.empty((N, D), dtype=y.dtype, device=y.device)
-    _check(lib.softmax_bwd(_ptr(y), y.stride(0), _ptr(dy), dy.stride(0), _ptr(dx), dx.stride(0),
-                           N, D, _dtype_code(y), _stream(stream)), "softmax_bwd")
+    with _on(y):
+        _check(lib.softmax_bwd(_ptr(y), y.stride(0), _ptr(dy), dy.stride(0), _ptr(dx),
+                               dx.stride(0), N, D, _dtype_code(y), _stream(stream, y.device)),
+               "softmax_bwd")
     return dx
 
 
@@ -241,8 +276,9 @@ def silu_fwd(x, w, y=None, stream=None):
     assert x.is_contiguous()
     if y is None:
         y = torch.empty_like(x)
-    _check(lib.silu_fwd(_ptr(x), _ptr(w), _ptr(y), x.numel(), _dtype_code(x), _stream(stream)),
-           "silu_fwd")
+    with _on(x):
+        _check(lib.silu_fwd(_ptr(x), _ptr(w), _ptr(y), x.numel(), _dtype_code(x),
+                            _stream(stream, x.device)), "silu_fwd")
     return y
 
 
@@ -257,12 +293,13 @@ def silu_bwd(dy, x, w, dx=None, dw=None, accumulate=False, workspace=None, strea
     if dw is None:
         dw = torch.empty(1, dtype=torch.float32, device=x.device)
     need = lib.silu_bwd_workspace_bytes(n, code)
-    if workspace is None and need not in (0, SIZE_MAX):
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib.silu_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), ctypes.c_void_p(dw.data_ptr()),
-                        int(bool(accumulate)), _ptr(workspace), wbytes, n, code, _stream(stream)),
-           "silu_bwd")
+    with _on(x):
+        if workspace is None and need not in (0, SIZE_MAX):
+            workspace = _scratch(need, x.device, stream)
+        wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(lib.silu_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), ctypes.c_void_p(dw.data_ptr()),
+                            int(bool(accumulate)), _ptr(workspace), wbytes, n, code,
+                            _stream(stream, x.device)), "silu_bwd")
     return dx, dw
 
 
@@ -279,8 +316,9 @@ def rmsnorm_fwd(x, w, eps=1e-5, y=None, stream=None):
     N, D = x.shape
     if y is None:
         y = torch.empty((N, D), dtype=x.dtype, device=x.device)
-    _check(lib.rmsnorm_fwd(_ptr(x), x.stride(0), _ptr(w), float(eps), _ptr(y), y.stride(0), N, D,
-                           _dtype_code(x), _stream(stream)), "rmsnorm_fwd")
+    with _on(x):
+        _check(lib.rmsnorm_fwd(_ptr(x), x.stride(0), _ptr(w), float(eps), _ptr(y), y.stride(0), N,
+                               D, _dtype_code(x), _stream(stream, x.device)), "rmsnorm_fwd")
     return y
 
 
@@ -290,17 +328,18 @@ def layernorm_fwd(x, w, b, eps=1e-5, y=None, stream=None):
     N, D = x.shape
     if y is None:
         y = torch.empty((N, D), dtype=x.dtype, device=x.device)
-    _check(lib.layernorm_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(b), float(eps), _ptr(y),
-                             y.stride(0), N, D, _dtype_code(x), _stream(stream)), "layernorm_fwd")
+    with _on(x):
+        _check(lib.layernorm_fwd(_ptr(x), x.stride(0), _ptr(w), _ptr(b), float(eps), _ptr(y),
+                                 y.stride(0), N, D, _dtype_code(x), _stream(stream, x.device)),
+               "layernorm_fwd")
     return y
 
 
-def _norm_ws(N, D, code, layer, workspace, device):
-    import torch
+def _norm_ws(N, D, code, layer, workspace, device, stream):
     fn = lib.layernorm_bwd_workspace_bytes if layer else lib.rmsnorm_bwd_workspace_bytes
     need = fn(N, D, code)
     if workspace is None and need not in (0, SIZE_MAX):
-        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+        workspace = _scratch(need, device, stream)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return workspace, wbytes
 
@@ -315,10 +354,12 @@ def rmsnorm_bwd(x, w, dy, eps=1e-5, dx=None, grad_w=None, accumulate=False, work
         dx = torch.empty((N, D), dtype=x.dtype, device=x.device)
     if grad_w is None:
         grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
-    workspace, wbytes = _norm_ws(N, D, code, False, workspace, x.device)
-    _check(lib.rmsnorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0), float(eps),
-                           _ptr(dx), dx.stride(0), _ptr(grad_w), int(bool(accumulate)),
-                           _ptr(workspace), wbytes, N, D, code, _stream(stream)), "rmsnorm_bwd")
+    with _on(x):
+        workspace, wbytes = _norm_ws(N, D, code, False, workspace, x.device, stream)
+        _check(lib.rmsnorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0), float(eps),
+                               _ptr(dx), dx.stride(0), _ptr(grad_w), int(bool(accumulate)),
+                               _ptr(workspace), wbytes, N, D, code, _stream(stream, x.device)),
+               "rmsnorm_bwd")
     return dx, grad_w
 
 
@@ -335,11 +376,12 @@ def layernorm_bwd(x, w, dy, eps=1e-5, dx=None, grad_w=None, grad_b=None, accumul
         grad_w = torch.empty(D, dtype=torch.float32, device=x.device)
     if grad_b is None:
         grad_b = torch.empty(D, dtype=torch.float32, device=x.device)
-    workspace, wbytes = _norm_ws(N, D, code, True, workspace, x.device)
-    _check(lib.layernorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0), float(eps),
-                             _ptr(dx), dx.stride(0), _ptr(grad_w), _ptr(grad_b),
-                             int(bool(accumulate)), _ptr(workspace), wbytes, N, D, code,
-                             _stream(stream)), "layernorm_bwd")
+    with _on(x):
+        workspace, wbytes = _norm_ws(N, D, code, True, workspace, x.device, stream)
+        _check(lib.layernorm_bwd(_ptr(x), x.stride(0), _ptr(w), _ptr(dy), dy.stride(0),
+                                 float(eps), _ptr(dx), dx.stride(0), _ptr(grad_w), _ptr(grad_b),
+                                 int(bool(accumulate)), _ptr(workspace), wbytes, N, D, code,
+                                 _stream(stream, x.device)), "layernorm_bwd")
     return dx, grad_w, grad_b
 
 
@@ -358,8 +400,10 @@ def selftest_exchange_timeout(count: torch.Tensor, limit_ms: int = 20, stream=No
     once the stream reaches it (each waiting warp gives up after limit_ms)."""
     if count.numel() != 1 or count.element_size() != 4 or not count.is_cuda:
         raise TypeError("count must be a one-element 4-byte CUDA tensor")
-    _check(lib.wsf_selftest_exchange_timeout(_ptr(count), int(limit_ms), _stream(stream)),
-           "wsf_selftest_exchange_timeout")
+    with _on(count):
+        _check(lib.wsf_selftest_exchange_timeout(_ptr(count), int(limit_ms),
+                                                 _stream(stream, count.device)),
+               "wsf_selftest_exchange_timeout")
 
 
 def selftest_waiting_warps() -> int:

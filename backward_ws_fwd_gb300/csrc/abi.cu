@@ -123,13 +123,19 @@ size_t ws_bwd_workspace_bytes(int64_t N, int64_t D, int dtype, int64_t block_n) 
     if (!valid_dtype(dtype) || N < 0 || D < 0 || block_n < 0) return SIZE_MAX;
     const int64_t P = wsf::ws_tiles(N, D, dtype, block_n);
     int64_t b;
-    if (!mul_ok(P, D, &b) || !mul_ok(b, 4, &b) || b > INT64_MAX - 255) return SIZE_MAX;
-    return (size_t)((b + 255) / 256 * 256);
+    if (!mul_ok(P, D, &b) || b > INT64_MAX / 16) return SIZE_MAX;
+    return (size_t)(wsf::gradient_plane(P, D) * 4 * 2);  // high and low planes
 }
 
-int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx, int64_t lddx,
-           float* grad_w, int accumulate, void* workspace, size_t workspace_bytes, int64_t block_n,
-           int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+}  // extern "C"
+
+// Validation of ws_bwd's arguments, shared with ws_bwd_noalloc (which has no
+// caller workspace: check_ws = false skips the workspace's alignment, size
+// and overlap checks).  *need receives ws_bwd_workspace_bytes for the sizes.
+int wsf::ws_bwd_check(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                      int64_t lddx, float* grad_w, int accumulate, const void* workspace,
+                      size_t workspace_bytes, bool check_ws, int64_t block_n, int64_t N,
+                      int64_t D, int dtype, size_t* need) {
     if (!valid_dtype(dtype)) return WSF_ERR_BAD_DTYPE;
     if (N < 0 || D < 0) return WSF_ERR_BAD_SHAPE;
     if (block_n < 0 || (accumulate != 0 && accumulate != 1)) return WSF_ERR_BAD_ARG;
@@ -142,18 +148,31 @@ int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
     if (xb < 0 || dxb < 0 || !mul_ok(N, es, &dyb) || !mul_ok(D, 4, &wb)) return WSF_ERR_BAD_SHAPE;
     if ((mat && (!x || !dy || !dx || !w)) || (D > 0 && !grad_w)) return WSF_ERR_NULL_PTR;
     if (!aligned_to(x, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(w, 4) ||
-        !aligned_to(grad_w, 4) || !aligned_to(workspace, 4))
+        !aligned_to(grad_w, 4) || (check_ws && !aligned_to(workspace, 4)))
         return WSF_ERR_MISALIGNED;
-    const size_t need = ws_bwd_workspace_bytes(N, D, dtype, block_n);
-    if (need == SIZE_MAX) return WSF_ERR_BAD_SHAPE;
-    if (need > 0 && (!workspace || workspace_bytes < need)) return WSF_ERR_WORKSPACE;
+    *need = ws_bwd_workspace_bytes(N, D, dtype, block_n);
+    if (*need == SIZE_MAX) return WSF_ERR_BAD_SHAPE;
+    if (check_ws && *need > 0 && (!workspace || workspace_bytes < *need)) return WSF_ERR_WORKSPACE;
     if (D == 0) return WSF_OK;
-    const Span sdx = span(dx, dxb), sg = span(grad_w, wb), sws = span(workspace, (int64_t)need);
+    const Span sdx = span(dx, dxb), sg = span(grad_w, wb);
+    const Span sws = span(check_ws ? workspace : nullptr, check_ws ? (int64_t)*need : 0);
     const Span sx = span(x, xb), sdy = span(dy, mat ? dyb : 0), sw = span(w, mat ? wb : 0);
     if (overlap(sdx, sx) || overlap(sdx, sdy) || overlap(sdx, sw) || overlap(sg, sx) ||
         overlap(sg, sdy) || overlap(sg, sw) || overlap(sws, sx) || overlap(sws, sdy) ||
         overlap(sws, sw) || overlap(sdx, sg) || overlap(sdx, sws) || overlap(sg, sws))
         return WSF_ERR_OVERLAP;
+    return WSF_OK;
+}
+
+extern "C" {
+
+int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx, int64_t lddx,
+           float* grad_w, int accumulate, void* workspace, size_t workspace_bytes, int64_t block_n,
+           int64_t N, int64_t D, int dtype, wsf_stream_t stream) {
+    size_t need = 0;
+    const int rc = wsf::ws_bwd_check(x, ldx, w, dy, dx, lddx, grad_w, accumulate, workspace,
+                                     workspace_bytes, true, block_n, N, D, dtype, &need);
+    if (rc != WSF_OK || D == 0) return rc;
     return cuda_status(wsf::launch_ws_bwd(x, ldx, w, dy, dx, lddx, grad_w, accumulate,
                                           (float*)workspace, block_n, N, D, dtype,
                                           (cudaStream_t)stream));
@@ -176,7 +195,7 @@ int silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype, wsf_s
 size_t silu_bwd_workspace_bytes(int64_t n, int dtype) {
     if (!valid_dtype(dtype) || n < 0) return SIZE_MAX;
     const int64_t P = wsf::silu_tiles(n);
-    return (size_t)((P * 4 + 255) / 256 * 256);
+    return (size_t)(wsf::gradient_plane(P, 1) * 4 * 2);  // high and low planes
 }
 
 int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw, int accumulate,

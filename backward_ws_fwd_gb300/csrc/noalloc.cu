@@ -54,15 +54,21 @@ extern "C" int ws_bwd_noalloc(const void* x, int64_t ldx, const float* w, const 
                               void* dx, int64_t lddx, float* grad_w, int accumulate,
                               int64_t block_n, int64_t N, int64_t D, int dtype,
                               wsf_stream_t stream) {
-    const size_t need = ws_bwd_workspace_bytes(N, D, dtype, block_n);
-    // need == SIZE_MAX means invalid arguments: ws_bwd reports which, without
-    // touching the device.
-    if (need != SIZE_MAX && need > WSF_NOALLOC_SCRATCH_BYTES) return WSF_ERR_WORKSPACE;
+    // the same argument checks, in the same order, as ws_bwd (less the
+    // workspace); only then the scratch limit and the device lookup
+    size_t need = 0;
+    int rc = wsf::ws_bwd_check(x, ldx, w, dy, dx, lddx, grad_w, accumulate, nullptr, 0, false,
+                               block_n, N, D, dtype, &need);
+    if (rc != WSF_OK) return rc;
+    if (need > WSF_NOALLOC_SCRATCH_BYTES) return WSF_ERR_WORKSPACE;
+    if (D == 0) return WSF_OK;
     float* scratch = nullptr;
-    if (need != SIZE_MAX && need > 0) {
-        const int rc = scratch_for_current_device(&scratch);
+    if (need > 0) {
+        rc = scratch_for_current_device(&scratch);
         if (rc != WSF_OK) return rc;
     }
-    return ws_bwd(x, ldx, w, dy, dx, lddx, grad_w, accumulate, scratch,
-                  scratch ? (size_t)WSF_NOALLOC_SCRATCH_BYTES : 0, block_n, N, D, dtype, stream);
+    return wsf::launch_ws_bwd(x, ldx, w, dy, dx, lddx, grad_w, accumulate, scratch, block_n, N, D,
+                              dtype, (cudaStream_t)stream) == cudaSuccess
+               ? WSF_OK
+               : WSF_ERR_CUDA;
 }

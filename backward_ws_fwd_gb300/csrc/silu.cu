@@ -165,31 +165,49 @@ __global__ void __launch_bounds__(NT)
 // accumulates dy·silu(x) over its elements in order, then the block combines:
 // xor butterfly inside each warp, warps added in index order.  The ownership
 // depends only on n, so the partials, and dw, are the same bits every run.
-// With ATOMIC the block's sum is added into *out with one atomic addition
-// (the page's own scheme, kept as a measured comparison: the order of the
-// blocks' additions, and so the bits of dw, depend on scheduling).
-template <int NT, bool ATOMIC = false>
-__device__ __forceinline__ void block_sum_store(float acc, float* out) {
+// Sums are compensated pairs (hi, lo): a thread adds the V terms of each
+// 16-byte vector in binary32 and that vector's sum into its pair with
+// TwoSum; warps, the block and the second stage add pairs.  The binary32
+// vector sums err by a few units of their own last place, random in sign,
+// below the error of the terms themselves (the 16-bit path's approximate
+// exponential and reciprocal).  A block's partial is stored as its high part
+// at part[p] and its low part at part[plane + p].  With ATOMIC the block's
+// sum is added into *out with one atomic addition (the page's own scheme,
+// kept as a measured comparison: the order of the blocks' additions, and so
+// the bits of dw, depend on scheduling).
+template <int NT>
+__device__ __forceinline__ Acc2 block_sum2(Acc2 acc) {  // the result is thread 0's
     constexpr int NW = NT / 32;
-    __shared__ float red[NW];
-    acc = group_sum<32>(acc);
+    __shared__ Acc2 red[NW];
+    acc = group_sum2<32>(acc);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();
+    Acc2 t = red[0];
     if (threadIdx.x == 0) {
-        float s = red[0];
 #pragma unroll
-        for (int q = 1; q < NW; q++) s += red[q];
-        if constexpr (ATOMIC)
-            atomicAdd(out, s);
-        else
-            *out = s;
+        for (int q = 1; q < NW; q++) t = acc2_add(t, red[q]);
+    }
+    return t;
+}
+
+template <int NT, bool ATOMIC = false>
+__device__ __forceinline__ void block_sum_store(Acc2 acc, float* out, int64_t plane) {
+    const Acc2 t = block_sum2<NT>(acc);
+    if (threadIdx.x == 0) {
+        if constexpr (ATOMIC) {
+            atomicAdd(out, acc2_value(t));
+        } else {
+            out[0] = t.hi;
+            out[plane] = t.lo;
+        }
     }
 }
 
 template <typename T, int U, int NT, bool ATOMIC = false>
 __global__ void __launch_bounds__(NT)
     silu_bwd_vec(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
-                 T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
+                 T* __restrict__ dx, float* __restrict__ part, int64_t plane, int64_t n,
+                 int64_t P) {
     using E = Elt<T>;
     constexpr int V = E::V;
     pdl_wait();
@@ -197,7 +215,7 @@ __global__ void __launch_bounds__(NT)
     const int64_t nv = n / V;
     const int64_t p = blockIdx.x;
     const int64_t ve = nv;
-    float acc = 0.f;
+    Acc2 acc = acc2_zero();
     for (int64_t base = p * NT * U; base < ve; base += P * NT * U) {
         Raw16 xr[U], gr[U];
 #pragma unroll
@@ -213,12 +231,14 @@ __global__ void __launch_bounds__(NT)
             float xf[V], gf[V];
             E::widen(xr[u], xf);
             E::widen(gr[u], gf);
+            float vs = 0.f;
 #pragma unroll
             for (int v = 0; v < V; v++) {
                 const SiluTerms st = silu_terms<kFastMath<T>>(xf[v]);
-                acc = fmaf(gf[v], st.silu, acc);
+                vs = fmaf(gf[v], st.silu, vs);
                 xf[v] = (gf[v] * wv) * st.dsilu;
             }
+            acc2_add1(acc, vs);
             if (i < ve) st_stream(dx + i * V, E::narrow(xf));
         }
     }
@@ -227,46 +247,50 @@ __global__ void __launch_bounds__(NT)
         if (k < n) {
             const float xv = E::load1(x + k), gv = E::load1(dy + k);
             const SiluTerms st = silu_terms<kFastMath<T>>(xv);
-            acc = fmaf(gv, st.silu, acc);
+            acc2_add1(acc, __fmul_rn(gv, st.silu));
             E::store1(dx + k, (gv * wv) * st.dsilu);
         }
     }
     pdl_trigger();
-    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p);
+    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p, plane);
 }
 
 template <typename T, int NT, bool ATOMIC = false>
 __global__ void __launch_bounds__(NT)
     silu_bwd_scalar(const T* __restrict__ dy, const T* __restrict__ x, const float* __restrict__ w,
-                    T* __restrict__ dx, float* __restrict__ part, int64_t n, int64_t P) {
+                    T* __restrict__ dx, float* __restrict__ part, int64_t plane, int64_t n,
+                    int64_t P) {
     using E = Elt<T>;
     pdl_wait();
     const float wv = __ldg(w);
     const int64_t p = blockIdx.x;
     const int64_t kb = (p * n) / P, ke = ((p + 1) * n) / P;
-    float acc = 0.f;
+    Acc2 acc = acc2_zero();
     for (int64_t k = kb + threadIdx.x; k < ke; k += NT) {
         const float xv = E::load1(x + k), gv = E::load1(dy + k);
         const SiluTerms st = silu_terms<kFastMath<T>>(xv);
-        acc = fmaf(gv, st.silu, acc);
+        acc2_add1(acc, __fmul_rn(gv, st.silu));
         E::store1(dx + k, (gv * wv) * st.dsilu);
     }
     pdl_trigger();
-    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p);
+    block_sum_store<NT, ATOMIC>(acc, ATOMIC ? part : part + p, plane);
 }
 
-// Backward, stage 2: one block; thread t sums part[t], part[t + NT], ... in
-// order, then the block combines as above.  dw = (accumulate ? dw : 0) + sum.
+// Backward, stage 2: one block; thread t sums the pairs part[t], part[t + NT],
+// ... in order, then the block combines as above; the pair is rounded once to
+// binary32.  dw = (accumulate ? dw : 0) + sum, one binary32 addition.
 template <int NT>
 __global__ void __launch_bounds__(NT)
-    silu_bwd_reduce(const float* __restrict__ part, int64_t P, float* __restrict__ dw,
-                    int accumulate) {
+    silu_bwd_reduce(const float* __restrict__ part, int64_t plane, int64_t P,
+                    float* __restrict__ dw, int accumulate) {
     pdl_wait();
-    float s = 0.f;
-    for (int64_t i = threadIdx.x; i < P; i += NT) s += part[i];
-    __shared__ float total;
-    block_sum_store<NT>(s, &total);
-    if (threadIdx.x == 0) *dw = accumulate ? *dw + total : total;
+    Acc2 s = acc2_zero();
+    for (int64_t i = threadIdx.x; i < P; i += NT) s = acc2_add(s, Acc2{part[i], part[plane + i]});
+    const Acc2 t = block_sum2<NT>(s);
+    if (threadIdx.x == 0) {
+        const float total = acc2_value(t);
+        *dw = accumulate ? *dw + total : total;
+    }
     pdl_trigger();
 }
 
@@ -301,22 +325,23 @@ template <typename T>
 static cudaError_t silu_bwd_t(const T* dy, const T* x, const float* w, T* dx, float* dw,
                               int accumulate, float* part, int64_t n, cudaStream_t s) {
     const int64_t P = silu_tiles(n);
+    const int64_t plane = gradient_plane(P, 1);
     cudaError_t e = cudaSuccess;
     if (P > 0) {
         if (aligned16(dy) && aligned16(x) && aligned16(dx)) {
             constexpr int NT = 256, U = 2;
             e = launch(silu_bwd_vec<T, U, NT>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
-                       dx, part, n, P);
+                       dx, part, plane, n, P);
         } else {
             constexpr int NT = 256;
             e = launch(silu_bwd_scalar<T, NT>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
-                       dx, part, n, P);
+                       dx, part, plane, n, P);
         }
         if (e != cudaSuccess) return e;
     }
     constexpr int NT = 1024;
-    return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, true, (const float*)part, P, dw,
-                  accumulate);
+    return launch(silu_bwd_reduce<NT>, dim3(1), dim3(NT), 0, s, true, (const float*)part, plane,
+                  P, dw, accumulate);
 }
 
 __global__ void __launch_bounds__(32) zero_one_f32(float* __restrict__ p) {
@@ -338,9 +363,9 @@ static cudaError_t silu_bwd_atomic_t(const T* dy, const T* x, const float* w, T*
     constexpr int NT = 256;
     if (aligned16(dy) && aligned16(x) && aligned16(dx))
         return launch(silu_bwd_vec<T, 2, NT, true>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x,
-                      w, dx, dw, n, P);
+                      w, dx, dw, (int64_t)0, n, P);
     return launch(silu_bwd_scalar<T, NT, true>, dim3((unsigned)P), dim3(NT), 0, s, true, dy, x, w,
-                  dx, dw, n, P);
+                  dx, dw, (int64_t)0, n, P);
 }
 
 cudaError_t launch_silu_bwd_atomic(const void* dy, const void* x, const float* w, void* dx,

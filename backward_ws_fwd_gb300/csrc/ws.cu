@@ -5,8 +5,10 @@
 // Backward (same page, §3 Backward: Deriving Gradients First; §4 Triton
 // Backward Kernel): dx[i,d] = dy[i]·w[d] is elementwise and parallel over
 // rows; grad_w[d] = Σ_i x[i,d]·dy[i] reduces over the batch axis, done in two
-// stages: each row tile writes one fp32 partial row, then a fixed-order sum
-// over tiles.
+// stages: each row tile writes one partial row, then a fixed-order sum over
+// tiles.  Every grad_w sum is a compensated fp32 pair (TwoSum of each
+// product into a running sum, the rounding errors collected beside it), so
+// the result is as accurate as a sum in twice the precision, rounded once.
 //
 // Kernel families, chosen on the host by row width and alignment:
 //  * forward, register path (rows of <= 4 KB, 16-byte aligned): a row is
@@ -83,6 +85,13 @@ int64_t ws_tiles(int64_t N, int64_t D, int dtype, int64_t block_n) {
 // that error and use plain fp32 accumulation.
 template <typename T>
 constexpr bool kCompensated = std::is_same<T, float>::value;
+
+// grad_w sums are compensated for every storage type (the stated 1e-5 bound
+// holds for the exact value even where a column's sum cancels); the product
+// x·dy is exact in binary32 for 16-bit storage and split with an FMA for
+// binary32.
+template <typename T>
+constexpr bool kExactProduct = !std::is_same<T, float>::value;
 
 // Load the lane's CPL chunks of w (V fp32 values each) into registers.
 template <int LPR, int CPL, int V>
@@ -271,43 +280,57 @@ __global__ void __launch_bounds__(NT)
 // Backward, stage 1: dx and the per-tile partial rows of grad_w
 // ===========================================================================
 
-// Write the CTA's partial row for columns [slice·LPRC·V, ...): G == 1 writes
-// each thread's V sums directly; otherwise the G row groups are added in
-// index order through shared memory `red` (G·LPRC·V floats).  With ATOMIC the
-// row is instead added into grad_w with atomic additions (the measured
-// comparison variant: the order of the additions, and so the bits of the
-// result, then depend on scheduling).
+// Write the CTA's partial row for columns [slice·LPRC·V, ...) as compensated
+// pairs: the high parts to out[0, ncols), the low parts to out[plane, plane +
+// ncols).  G == 1 writes each thread's V pairs directly; otherwise the G row
+// groups are added in index order (double-float additions) through shared
+// memory `red` (2·G·LPRC·V floats).  With ATOMIC the row is instead added
+// into grad_w (`out`) with atomic additions of each pair's value (the
+// measured comparison variant: the order of the additions, and so the bits
+// of the result, then depend on scheduling).
 template <int LPRC, int G, int V, int NT, bool ATOMIC = false>
-__device__ __forceinline__ void write_partial(const float (&acc)[V], float* __restrict__ out,
-                                              int g, int l, bool cok, int64_t ncols,
-                                              float* red) {
+__device__ __forceinline__ void write_partial(const Acc2 (&acc)[V], float* __restrict__ out,
+                                              int64_t plane, int g, int l, bool cok,
+                                              int64_t ncols, float* red) {
     if constexpr (G == 1) {
         if (cok) {
 #pragma unroll
             for (int q = 0; q < V / 4; q++) {
                 if constexpr (ATOMIC) {
                     atomicAdd(reinterpret_cast<float4*>(out + l * V + 4 * q),
-                              make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+                              make_float4(acc2_value(acc[4 * q]), acc2_value(acc[4 * q + 1]),
+                                          acc2_value(acc[4 * q + 2]), acc2_value(acc[4 * q + 3])));
                 } else {
-                    Raw16 r;
+                    Raw16 h, o;
 #pragma unroll
-                    for (int i = 0; i < 4; i++) r.u[i] = __float_as_uint(acc[4 * q + i]);
-                    *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = r;
+                    for (int i = 0; i < 4; i++) {
+                        h.u[i] = __float_as_uint(acc[4 * q + i].hi);
+                        o.u[i] = __float_as_uint(acc[4 * q + i].lo);
+                    }
+                    *reinterpret_cast<Raw16*>(out + l * V + 4 * q) = h;
+                    *reinterpret_cast<Raw16*>(out + plane + l * V + 4 * q) = o;
                 }
             }
         }
     } else {
+        constexpr int H = G * LPRC * V;
 #pragma unroll
-        for (int v = 0; v < V; v++) red[(g * LPRC + l) * V + v] = acc[v];
+        for (int v = 0; v < V; v++) {
+            red[(g * LPRC + l) * V + v] = acc[v].hi;
+            red[H + (g * LPRC + l) * V + v] = acc[v].lo;
+        }
         __syncthreads();
         for (int j = threadIdx.x; j < ncols; j += NT) {
-            float s = red[j];
+            Acc2 t{red[j], red[H + j]};
 #pragma unroll
-            for (int q = 1; q < G; q++) s += red[q * LPRC * V + j];
-            if constexpr (ATOMIC)
-                atomicAdd(out + j, s);
-            else
-                out[j] = s;
+            for (int q = 1; q < G; q++)
+                t = acc2_add(t, Acc2{red[q * LPRC * V + j], red[H + q * LPRC * V + j]});
+            if constexpr (ATOMIC) {
+                atomicAdd(out + j, acc2_value(t));
+            } else {
+                out[j] = t.hi;
+                out[plane + j] = t.lo;
+            }
         }
         __syncthreads();
     }
@@ -325,14 +348,15 @@ template <typename T, int LPRC, int U, int S, int NT, int MINB, bool ATOMIC = fa
 __global__ void __launch_bounds__(NT, MINB)
     ws_bwd_staged(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                   const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
-                  float* __restrict__ partial, int64_t N, int64_t Dv, int64_t D,
-                  int64_t block_n, int64_t P) {
+                  float* __restrict__ partial, int64_t plane, int64_t N, int64_t Dv,
+                  int64_t D, int64_t block_n, int64_t P) {
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int G = NT / LPRC;
     constexpr int SR = G * U;                 // rows per step
     constexpr int DYB = SR * (int)sizeof(T);  // dy bytes per step
     static_assert(DYB % 16 == 0, "dy step must be whole 16-byte copies");
+    static_assert(S * U * 16 >= 8 * V, "staging buffer must hold the partial combine");
     extern __shared__ __align__(16) unsigned char smem[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem);                                // [S][U][NT]
     T* dys = reinterpret_cast<T*>(smem + (size_t)S * U * NT * sizeof(Raw16));  // [S][SR]
@@ -345,16 +369,17 @@ __global__ void __launch_bounds__(NT, MINB)
     const bool cok = c < Dv;
     pdl_wait();
 
-    float wv[V];
+    // weights and accumulators as packed pairs of columns (f32x2 arithmetic)
+    uint64_t w2[V / 2];
 #pragma unroll
     for (int q = 0; q < V / 4; q++) {
         Raw16 r = cok ? ld_keep(w + c * V + 4 * q) : raw_zero();
-#pragma unroll
-        for (int i = 0; i < 4; i++) wv[4 * q + i] = __uint_as_float(r.u[i]);
+        w2[2 * q] = f2_pack(__uint_as_float(r.u[0]), __uint_as_float(r.u[1]));
+        w2[2 * q + 1] = f2_pack(__uint_as_float(r.u[2]), __uint_as_float(r.u[3]));
     }
-    float acc[V];
+    Acc2x2 acc[V / 2];
 #pragma unroll
-    for (int v = 0; v < V; v++) acc[v] = 0.f;
+    for (int k = 0; k < V / 2; k++) acc[k] = Acc2x2{0ull, 0ull};
 
     const int64_t nsteps = (rb - ra + SR - 1) / SR;
     auto issue = [&](int64_t k) {
@@ -392,17 +417,19 @@ __global__ void __launch_bounds__(NT, MINB)
             const int64_t row = r0 + u * G + g;
             const bool ok = row < rb;
             const float gv = ok ? E::widen1(dys[slot * SR + u * G + g]) : 0.f;
+            const uint64_t g2 = f2_pack(gv, gv), ng2 = f2_pack(-gv, -gv);
             const Raw16 xr = xs[(slot * U + u) * NT + tid];
             if (ok && cok) {
                 float f[V];
 #pragma unroll
-                for (int v = 0; v < V; v++) f[v] = gv * wv[v];
+                for (int k = 0; k < V / 2; k++) f2_unpack(f2_mul(g2, w2[k]), f[2 * k], f[2 * k + 1]);
                 st_stream(dx + row * lddx + c * V, E::narrow(f));
             }
             float f[V];
             E::widen(xr, f);
 #pragma unroll
-            for (int v = 0; v < V; v++) acc[v] = fmaf(f[v], gv, acc[v]);
+            for (int k = 0; k < V / 2; k++)
+                acc2x2_prod<kExactProduct<T>>(acc[k], f2_pack(f[2 * k], f[2 * k + 1]), g2, ng2);
         }
     }
     cp_async_wait<0>();  // no copy may still target shared memory when the CTA ends
@@ -412,7 +439,10 @@ __global__ void __launch_bounds__(NT, MINB)
     const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
     // ATOMIC: `partial` is grad_w itself and every tile adds into the same row
     float* out = partial + (ATOMIC ? 0 : (int64_t)blockIdx.x * D) + col0;
-    write_partial<LPRC, G, V, NT, ATOMIC>(acc, out, g, l, cok, ncols,
+    Acc2 sums[V];
+#pragma unroll
+    for (int k = 0; k < V / 2; k++) acc2x2_unpack(acc[k], sums[2 * k], sums[2 * k + 1]);
+    write_partial<LPRC, G, V, NT, ATOMIC>(sums, out, plane, g, l, cok, ncols,
                                           reinterpret_cast<float*>(smem));
 }
 
@@ -423,12 +453,12 @@ template <typename T, int LPRC, int U, int NT>
 __global__ void __launch_bounds__(NT)
     ws_bwd_tile(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                 const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
-                float* __restrict__ partial, int64_t N, int64_t Dv, int64_t D, int64_t block_n,
-                int64_t P) {
+                float* __restrict__ partial, int64_t plane, int64_t N, int64_t Dv, int64_t D,
+                int64_t block_n, int64_t P) {
     using E = Elt<T>;
     constexpr int V = E::V;
     constexpr int G = NT / LPRC;
-    __shared__ float red[G > 1 ? G * LPRC * V : 1];
+    __shared__ float red[G > 1 ? 2 * G * LPRC * V : 1];
     const int g = threadIdx.x / LPRC, l = threadIdx.x % LPRC;
     int64_t ra, rb;
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
@@ -437,16 +467,16 @@ __global__ void __launch_bounds__(NT)
     for (int64_t slice = blockIdx.y; slice < nslices; slice += gridDim.y) {
         const int64_t c = slice * LPRC + l;
         const bool cok = c < Dv;
-        float wv[V];
+        uint64_t w2[V / 2];
 #pragma unroll
         for (int q = 0; q < V / 4; q++) {
             Raw16 r = cok ? ld_keep(w + c * V + 4 * q) : raw_zero();
-#pragma unroll
-            for (int i = 0; i < 4; i++) wv[4 * q + i] = __uint_as_float(r.u[i]);
+            w2[2 * q] = f2_pack(__uint_as_float(r.u[0]), __uint_as_float(r.u[1]));
+            w2[2 * q + 1] = f2_pack(__uint_as_float(r.u[2]), __uint_as_float(r.u[3]));
         }
-        float acc[V];
+        Acc2x2 acc[V / 2];
 #pragma unroll
-        for (int v = 0; v < V; v++) acc[v] = 0.f;
+        for (int k = 0; k < V / 2; k++) acc[k] = Acc2x2{0ull, 0ull};
         for (int64_t base = ra + g; base < rb; base += (int64_t)G * U) {
             Raw16 xr[U];
             float gv[U];
@@ -460,22 +490,28 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
             for (int u = 0; u < U; u++) {
                 const int64_t row = base + (int64_t)u * G;
+                const uint64_t g2 = f2_pack(gv[u], gv[u]), ng2 = f2_pack(-gv[u], -gv[u]);
                 if (row < rb && cok) {
                     float f[V];
 #pragma unroll
-                    for (int v = 0; v < V; v++) f[v] = gv[u] * wv[v];
+                    for (int k = 0; k < V / 2; k++)
+                        f2_unpack(f2_mul(g2, w2[k]), f[2 * k], f[2 * k + 1]);
                     st_stream(dx + row * lddx + c * V, E::narrow(f));
                 }
                 float f[V];
                 E::widen(xr[u], f);
 #pragma unroll
-                for (int v = 0; v < V; v++) acc[v] = fmaf(f[v], gv[u], acc[v]);
+                for (int k = 0; k < V / 2; k++)
+                    acc2x2_prod<kExactProduct<T>>(acc[k], f2_pack(f[2 * k], f[2 * k + 1]), g2, ng2);
             }
         }
         const int64_t col0 = slice * LPRC * V;
         const int64_t ncols = (D - col0) < LPRC * V ? D - col0 : LPRC * V;
-        write_partial<LPRC, G, V, NT>(acc, partial + (int64_t)blockIdx.x * D + col0, g, l, cok,
-                                      ncols, red);
+        Acc2 sums[V];
+#pragma unroll
+        for (int k = 0; k < V / 2; k++) acc2x2_unpack(acc[k], sums[2 * k], sums[2 * k + 1]);
+        write_partial<LPRC, G, V, NT>(sums, partial + (int64_t)blockIdx.x * D + col0, plane, g, l,
+                                      cok, ncols, red);
     }
     pdl_trigger();
 }
@@ -486,7 +522,8 @@ template <typename T, int NT>
 __global__ void __launch_bounds__(NT)
     ws_bwd_scalar(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                   const T* __restrict__ dy, T* __restrict__ dx, int64_t lddx,
-                  float* __restrict__ partial, int64_t N, int64_t D, int64_t block_n, int64_t P) {
+                  float* __restrict__ partial, int64_t plane, int64_t N, int64_t D,
+                  int64_t block_n, int64_t P) {
     using E = Elt<T>;
     int64_t ra, rb;
     tile_rows(blockIdx.x, P, N, block_n, ra, rb);
@@ -494,45 +531,51 @@ __global__ void __launch_bounds__(NT)
     for (int64_t col = (int64_t)blockIdx.y * NT + threadIdx.x; col < D;
          col += (int64_t)gridDim.y * NT) {
         const float wv = __ldg(w + col);
-        float acc = 0.f;
+        Acc2 acc = acc2_zero();
         for (int64_t row = ra; row < rb; row++) {
             const float gv = E::load1(dy + row);
             E::store1(dx + row * lddx + col, gv * wv);
-            acc = fmaf(E::load1(x + row * ldx + col), gv, acc);
+            acc2_prod<kExactProduct<T>>(acc, E::load1(x + row * ldx + col), gv);
         }
-        partial[(int64_t)blockIdx.x * D + col] = acc;
+        partial[(int64_t)blockIdx.x * D + col] = acc.hi;
+        partial[plane + (int64_t)blockIdx.x * D + col] = acc.lo;
     }
     pdl_trigger();
 }
 
 // ===========================================================================
 // Backward, stage 2: grad_w[d] = (accumulate ? grad_w[d] : 0) + Σ_p partial[p,d]
-// Thread (tx, ty) sums p = ty, ty + RY, ... in ascending order; the RY
-// stripe sums are then combined by a fixed halving tree.  RY is 32 for rows
-// of up to 4096 columns and 8 above; either way the order is fixed by D.
+// Each partial is a compensated pair (high plane at `partial`, low plane
+// `plane` floats further on), and so is every sum here.  Thread (tx, ty) sums
+// p = ty, ty + RY, ... in ascending order; the RY stripe sums are then
+// combined by a fixed halving tree; the pair is rounded once to binary32 and,
+// when accumulating, added to the old value in one binary32 addition.  RY is
+// 32 for rows of up to 4096 columns and 8 above; either way the order is
+// fixed by D.
 // ===========================================================================
 template <int RY>
 __global__ void __launch_bounds__(32 * RY)
-    ws_bwd_reduce(const float* __restrict__ partial, int64_t P, int64_t D,
+    ws_bwd_reduce(const float* __restrict__ partial, int64_t plane, int64_t P, int64_t D,
                   float* __restrict__ grad_w, int accumulate) {
-    __shared__ float sm[RY][33];
+    __shared__ Acc2 sm[RY][33];
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int64_t col = (int64_t)blockIdx.x * 32 + tx;
     pdl_wait();
-    float s = 0.f;
+    Acc2 s = acc2_zero();
     if (col < D) {
 #pragma unroll 8
-        for (int64_t p = ty; p < P; p += RY) s += partial[p * D + col];
+        for (int64_t p = ty; p < P; p += RY)
+            s = acc2_add(s, Acc2{partial[p * D + col], partial[plane + p * D + col]});
     }
     sm[ty][tx] = s;
     __syncthreads();
 #pragma unroll
     for (int h = RY / 2; h > 0; h >>= 1) {
-        if (ty < h) sm[ty][tx] += sm[ty + h][tx];
+        if (ty < h) sm[ty][tx] = acc2_add(sm[ty][tx], sm[ty + h][tx]);
         __syncthreads();
     }
     if (ty == 0 && col < D) {
-        const float v = sm[0][tx];
+        const float v = acc2_value(sm[0][tx]);
         grad_w[col] = accumulate ? grad_w[col] + v : v;
     }
     pdl_trigger();
@@ -633,7 +676,7 @@ struct BwdArgs {
     T* dx;
     int64_t lddx;
     float* partial;
-    int64_t N, Dv, D, block_n, P;
+    int64_t plane, N, Dv, D, block_n, P;
 };
 
 template <typename T, int LPRC, int U, int S, int NT, int MINB, bool ATOMIC = false>
@@ -644,7 +687,7 @@ static cudaError_t bwd_staged(const BwdArgs<T>& a, cudaStream_t s) {
     cudaError_t e = allow_smem((const void*)kernel, smem);
     if (e != cudaSuccess) return e;
     return launch(kernel, dim3((unsigned)a.P, (unsigned)cdiv(a.Dv, LPRC)), dim3(NT), smem, s,
-                  true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
+                  true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.plane, a.N, a.Dv, a.D,
                   a.block_n, a.P);
 }
 
@@ -653,27 +696,30 @@ static cudaError_t bwd_tile(const BwdArgs<T>& a, cudaStream_t s) {
     constexpr int NT = LPRC < 128 ? 128 : LPRC, U = 4;
     const int64_t slices = std::min<int64_t>(cdiv(a.Dv, LPRC), 65535);
     return launch(ws_bwd_tile<T, LPRC, U, NT>, dim3((unsigned)a.P, (unsigned)slices), dim3(NT), 0,
-                  s, true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.N, a.Dv, a.D,
-                  a.block_n, a.P);
+                  s, true, a.x, a.ldx, a.w, a.dy, a.dx, a.lddx, a.partial, a.plane, a.N, a.Dv,
+                  a.D, a.block_n, a.P);
 }
 
-// Staged-path shapes (measured on GB300): rows of <= 64 chunks use 128
-// threads, 8 rows per thread per step and 3 steps in flight; rows of 128
-// chunks 128 threads and 4 steps; wider rows 256-chunk slices with 16 bytes
-// of dy per step.
+// Staged-path shapes (measured on GB300 with the compensated accumulation):
+// rows of <= 64 chunks use 128 threads, 4 rows per thread per step and 2
+// steps in flight (16 KB of staging, 6 CTAs per SM); rows of 128 chunks 256
+// threads as two row groups, 4 rows each and 2 steps (32 KB, 3 CTAs per SM);
+// wider rows 256-chunk slices with 16 bytes of dy per step.  At c3's and
+// c4's sizes these shapes beat the deeper staging they replaced (3-4 steps of
+// 8 rows: 48-64 KB, 3-4 CTAs per SM) by 8% and 2.5%.
 template <typename T, bool ATOMIC = false>
 static cudaError_t bwd_staged_any(const BwdArgs<T>& a, int lprc, cudaStream_t s) {
     constexpr int UW = 16 / (int)sizeof(T);
     switch (lprc) {
-        case 1: return bwd_staged<T, 1, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 2: return bwd_staged<T, 2, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 4: return bwd_staged<T, 4, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 8: return bwd_staged<T, 8, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 16: return bwd_staged<T, 16, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 32: return bwd_staged<T, 32, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 64: return bwd_staged<T, 64, 8, 3, 128, 6, ATOMIC>(a, s);
-        case 128: return bwd_staged<T, 128, 8, 4, 128, 6, ATOMIC>(a, s);
-        default: return bwd_staged<T, 256, UW, 3, 256, 4, ATOMIC>(a, s);
+        case 1: return bwd_staged<T, 1, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 2: return bwd_staged<T, 2, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 4: return bwd_staged<T, 4, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 8: return bwd_staged<T, 8, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 16: return bwd_staged<T, 16, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 32: return bwd_staged<T, 32, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 64: return bwd_staged<T, 64, 4, 2, 128, 6, ATOMIC>(a, s);
+        case 128: return bwd_staged<T, 128, 4, 2, 256, 3, ATOMIC>(a, s);
+        default: return bwd_staged<T, 256, UW, 3, 256, (sizeof(T) == 4 ? 4 : 3), ATOMIC>(a, s);
     }
 }
 
@@ -699,6 +745,7 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
                             int64_t block_n, int64_t N, int64_t D, int dtype, cudaStream_t s) {
     constexpr int V = Elt<T>::V;
     const int64_t P = ws_tiles(N, D, dtype, block_n);
+    const int64_t plane = gradient_plane(P, D);
     cudaError_t e = cudaSuccess;
     if (P > 0) {
         const int64_t Dv = D / V;
@@ -709,13 +756,13 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
             // staged path: every step's dy slice must start on a 16-byte boundary
             const bool staged = aligned16(dy) && (block_n * (int64_t)sizeof(T)) % 16 == 0 &&
                                 cdiv(Dv, lprc) <= 65535;
-            BwdArgs<T> a{x, ldx, w, dy, dx, lddx, partial, N, Dv, D, block_n, P};
+            BwdArgs<T> a{x, ldx, w, dy, dx, lddx, partial, plane, N, Dv, D, block_n, P};
             e = bwd_vec<T>(a, lprc, staged, s);
         } else {
             constexpr int NT = 128;
             const int64_t slices = std::min<int64_t>(cdiv(D, NT), 65535);
             e = launch(ws_bwd_scalar<T, NT>, dim3((unsigned)P, (unsigned)slices), dim3(NT), 0, s,
-                       true, x, ldx, w, dy, dx, lddx, partial, N, D, block_n, P);
+                       true, x, ldx, w, dy, dx, lddx, partial, plane, N, D, block_n, P);
         }
         if (e != cudaSuccess) return e;
     }
@@ -724,10 +771,10 @@ static cudaError_t ws_bwd_t(const T* x, int64_t ldx, const float* w, const T* dy
         // handful of CTAs still keep many loads in flight
         if (D <= 4096)
             e = launch(ws_bwd_reduce<32>, dim3((unsigned)cdiv(D, 32)), dim3(32, 32), 0, s, true,
-                       (const float*)partial, P, D, grad_w, accumulate);
+                       (const float*)partial, plane, P, D, grad_w, accumulate);
         else
             e = launch(ws_bwd_reduce<8>, dim3((unsigned)cdiv(D, 32)), dim3(32, 8), 0, s, true,
-                       (const float*)partial, P, D, grad_w, accumulate);
+                       (const float*)partial, plane, P, D, grad_w, accumulate);
     }
     return e;
 }
@@ -768,7 +815,7 @@ static cudaError_t ws_bwd_atomic_t(const T* x, int64_t ldx, const float* w, cons
     if (P == 0) return e;
     const int64_t Dv = D / V;
     const int lprc = Dv <= kSliceChunks ? next_pow2(Dv) : kSliceChunks;
-    BwdArgs<T> a{x, ldx, w, dy, dx, lddx, grad_w, N, Dv, D, 0, P};
+    BwdArgs<T> a{x, ldx, w, dy, dx, lddx, grad_w, 0, N, Dv, D, 0, P};
     return bwd_staged_any<T, true>(a, lprc, s);
 }
 

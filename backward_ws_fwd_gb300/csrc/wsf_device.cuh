@@ -215,7 +215,10 @@ __device__ __forceinline__ float group_sum(float v) {
 // into its rounded sum and exact error (Knuth's TwoSum); the errors are
 // collected in `lo`.  The result hi + lo is as accurate as if computed in
 // twice the working precision, then rounded.  Used where a binary32 output
-// must stay within 1e-6 of the exact sum over up to 65,536 terms.
+// must stay within 1e-6 of the exact sum over up to 65,536 terms, and for
+// every parameter-gradient sum (grad_w, dw), whose stated bound is 1e-5 of
+// the exact value even where the sum cancels to a small fraction of its
+// terms' magnitudes.
 struct Acc2 {
     float hi, lo;
 };
@@ -243,6 +246,101 @@ __device__ __forceinline__ Acc2 acc2_add(Acc2 a, Acc2 b) {
     float s, e;
     two_sum(a.hi, b.hi, s, e);
     return Acc2{s, a.lo + b.lo + e};
+}
+
+// Add one binary32 value whose own rounding is not in question (an exact
+// product, or a term taken as given): TwoSum into hi, the error into lo.
+__device__ __forceinline__ void acc2_add1(Acc2& a, float p) {
+    float s, e;
+    two_sum(a.hi, p, s, e);
+    a.hi = s;
+    a.lo += e;
+}
+
+// Compensated accumulation of the product x·g.  The product of two values of
+// a 16-bit storage type is exact in binary32 (at most 11 + 11 significant
+// bits, within the exponent range unless it falls below 2^-126), so only the
+// addition needs its error kept; a binary32 product is split with an FMA.
+template <bool ExactProduct>
+__device__ __forceinline__ void acc2_prod(Acc2& a, float x, float g) {
+    if constexpr (ExactProduct)
+        acc2_add1(a, __fmul_rn(x, g));
+    else
+        acc2_fma(a, x, g);
+}
+
+// Value of a compensated pair, rounded once to binary32.
+__device__ __forceinline__ float acc2_value(Acc2 a) { return __fadd_rn(a.hi, a.lo); }
+
+// ---------------------------------------------------------------------------
+// Packed binary32 pairs (sm_100 and later: add/sub/mul/fma.rn.f32x2 operate
+// on two binary32 values held in one 64-bit register, each lane rounded to
+// nearest-even on its own, exactly as the scalar instruction would).  Lane 0
+// is the low half.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t d, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Two compensated pairs, packed: hi holds the two running sums, lo their
+// collected rounding errors.
+struct Acc2x2 {
+    uint64_t hi, lo;
+};
+
+// acc2_prod on two columns at once: a += x·g lane by lane (x2 the two
+// values of x, g2 = (g, g), ng2 = (−g, −g)).  The steps are Knuth's TwoSum
+// written with b − b' as fma(x, g, −b') where the product is exact (and with
+// an FMA split of the product where it is not), so every lane gets the bits
+// that acc2_prod gives.
+template <bool ExactProduct>
+__device__ __forceinline__ void acc2x2_prod(Acc2x2& a, uint64_t x2, uint64_t g2, uint64_t ng2) {
+    if constexpr (ExactProduct) {
+        const uint64_t s = f2_fma(x2, g2, a.hi);    // fl(hi + x·g)
+        const uint64_t nbp = f2_sub(a.hi, s);       // −(s − hi)
+        const uint64_t ap = f2_add(s, nbp);         // s − (s − hi)
+        const uint64_t e = f2_add(f2_sub(a.hi, ap), f2_fma(x2, g2, nbp));
+        a.hi = s;
+        a.lo = f2_add(a.lo, e);
+    } else {
+        const uint64_t np = f2_mul(x2, ng2);        // −fl(x·g)
+        const uint64_t ep = f2_fma(x2, g2, np);     // x·g − fl(x·g), exact
+        const uint64_t s = f2_sub(a.hi, np);        // fl(hi + p)
+        const uint64_t nbp = f2_sub(a.hi, s);
+        const uint64_t ap = f2_add(s, nbp);
+        const uint64_t e = f2_add(f2_sub(a.hi, ap), f2_sub(nbp, np));
+        a.hi = s;
+        a.lo = f2_add(a.lo, f2_add(e, ep));
+    }
+}
+
+__device__ __forceinline__ void acc2x2_unpack(const Acc2x2& a, Acc2& first, Acc2& second) {
+    f2_unpack(a.hi, first.hi, second.hi);
+    f2_unpack(a.lo, first.lo, second.lo);
 }
 
 template <int Width>

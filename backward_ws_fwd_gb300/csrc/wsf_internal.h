@@ -20,8 +20,21 @@ int64_t ws_tiles(int64_t N, int64_t D, int dtype, int64_t block_n);
 // Number of per-block partials of the scaled-SiLU backward.
 int64_t silu_tiles(int64_t n);
 
+// The partial sums of a parameter gradient are compensated pairs: the
+// workspace holds a plane of high parts [P, D] and, `gradient_plane(P, D)`
+// floats further on (a 256-byte multiple), a plane of low parts.
+inline int64_t gradient_plane(int64_t P, int64_t D) { return (P * D + 63) / 64 * 64; }
+
 cudaError_t launch_ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N,
                           int64_t D, int dtype, cudaStream_t s);
+
+// Host-side validation of ws_bwd's arguments (abi.cu); check_ws = false
+// leaves out the workspace (ws_bwd_noalloc).  Returns a WSF_* status and sets
+// *need to the workspace bytes the sizes require.
+int ws_bwd_check(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
+                 int64_t lddx, float* grad_w, int accumulate, const void* workspace,
+                 size_t workspace_bytes, bool check_ws, int64_t block_n, int64_t N, int64_t D,
+                 int dtype, size_t* need);
 
 cudaError_t launch_ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
                           int64_t lddx, float* grad_w, int accumulate, float* partial,

@@ -17,8 +17,14 @@ parameter gradient) divided by device time.  `value` is measured with CUDA
 events around K steps on resident inputs; `e2e` runs the same step through
 the public API with host buffers, the host<->device copies included.
 
+The worked 100 x 64 example (c1, 32-row tiles) is latency-bound: it is timed
+alone, outside the step (device time per op from CUDA graphs, and the host's
+call-to-result latency), and reported beside the isolated per-op table.
+`cpu_baseline` times the fp64 oracle per workload and per op on the host's
+cores.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
-       [--workload all|c2|c3|c4|c5]
+       [--workload all|c1,c2,c3,c4,c5,...]
 Under torchrun each rank runs its own replica of the workload (weak scaling,
 no collective on the data path); rank 0 prints one JSON line.
 """
@@ -43,6 +49,7 @@ KERNELS_PER_OP = {"ws_fwd": 1, "ws_bwd": 2, "silu_fwd": 1, "silu_bwd": 2, "softm
                   "softmax_bwd": 1, "rmsnorm_fwd": 1, "rmsnorm_bwd": 2, "layernorm_fwd": 1,
                   "layernorm_bwd": 2}
 EXTRA = ["s1", "n1", "n2", "s2", "n3", "n4", "s3", "s4"]  # measured only when named
+LATENCY = ["c1"]  # latency-bound: timed alone, outside the step
 NORMS = ("rmsnorm", "layernorm")
 
 
@@ -158,13 +165,17 @@ def oracle_sample(names, frac: float):
     """Host inputs for a bounded sample of each workload: the first
     max(1, round(N·frac)) rows (for the scaled SiLU, rows of the [8192, 4096]
     tensor)."""
+    from inputgen.workloads import WORKLOADS
+    return oracle_sample_wl([(WORKLOADS[n], max(1, int(round(WORKLOADS[n].N * frac))))
+                             for n in names])
+
+
+def oracle_sample_wl(pairs):
+    """Host inputs of the first `rows` rows of each (workload, rows) pair."""
     import torch
     import inputgen
-    from inputgen.workloads import WORKLOADS
     samples = []
-    for n in names:
-        wl = WORKLOADS[n]
-        rows = max(1, int(round(wl.N * frac)))
+    for wl, rows in pairs:
         x = inputgen.make((rows, wl.D), wl.dtype, wl.x.kind, wl.x.a, wl.x.b, 0, 0)
         if wl.op == "ws":
             w = inputgen.make((wl.D,), "f32", wl.w.kind, wl.w.a, wl.w.b, 0, 1)
@@ -219,35 +230,81 @@ def calibrated_fraction(names, budget_s: float, max_frac: float = 1 / 16):
     return max(f0, min(max_frac, f0 * budget_s / dt))
 
 
-def cpu_baseline(names):
-    """The oracle on this host: all cores (OpenMP; the main figure) and one
-    core, each on a bounded sample of the workloads (about 10 s of work)."""
+def _time_repeated(fn, budget_s: float) -> float:
+    """Mean seconds of one call of fn, repeated until budget_s have passed."""
+    reps = 0
+    t = time.perf_counter()
+    while reps == 0 or time.perf_counter() - t < budget_s:
+        fn()
+        reps += 1
+    return (time.perf_counter() - t) / reps
+
+
+def oracle_ops(wl, rows):
+    """The oracle's forward and backward of the first `rows` rows of wl (host
+    inputs generated here, outside any timing), as two callables."""
     import oracle
+    (_, _, x, w, dy), = oracle_sample_wl([(wl, rows)])
+    if wl.op == "ws":
+        return (lambda: oracle.ws_fwd(x, w)), (lambda: oracle.ws_bwd(x, w, dy))
+    if wl.op == "softmax":
+        _, y = oracle.softmax_fwd(x)
+        return (lambda: oracle.softmax_fwd(x)), (lambda: oracle.softmax_bwd(y, dy))
+    if wl.op in NORMS:
+        layer = wl.op == "layernorm"
+        return (lambda: oracle.norm_fwd(x, w[0], w[1], wl.eps, layer),
+                lambda: oracle.norm_bwd(x, w[0], dy, wl.eps, layer))
+    xf, gf = x.reshape(-1), dy.reshape(-1)
+    return (lambda: oracle.silu_fwd(xf, wl.w_scalar)), (lambda: oracle.silu_bwd(gf, xf, wl.w_scalar))
+
+
+def cpu_baseline(names, per_op_budget_s: float = 0.4):
+    """The oracle on this host, per workload and per op: forward, backward and
+    fwd+bwd as effective bytes/s and elements/s, on all cores (OpenMP) and on
+    one.  Each workload runs on a bounded sample (its first rows: at most a
+    sixteenth of a large workload, sized so that an op takes ~per_op_budget_s
+    on all cores), every op repeated for ~per_op_budget_s.  `value` is the
+    sum of the sampled bytes over the sum of the times on all cores."""
+    import oracle
+    from inputgen.workloads import WORKLOADS
     oracle.build()
     cores = oracle.threads()
-    out = {}
-    for label, n in (("all", cores), ("one", 1)):
-        old = oracle.set_threads(n)
-        try:
-            frac = calibrated_fraction(names, budget_s=8.0)
-            samples = oracle_sample(names, frac)
-            # the sample is bounded (at most 1/16 of each workload); it is
-            # repeated until about 8 s of work have been timed
-            nbytes, reps = 0, 0
-            t = time.perf_counter()
-            while reps == 0 or time.perf_counter() - t < 8.0:
-                nbytes += oracle_step(samples)
-                reps += 1
-            dt = time.perf_counter() - t
-        finally:
-            oracle.set_threads(old)
-        out[label] = (nbytes / dt / 1e9, dt, samples, reps)
-    v, dt, samples, reps = out["all"]
-    v1, dt1, samples1, reps1 = out["one"]
-    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": sample_desc(samples) + f", {reps}x; {dt:.1f} s of fp64 CPU work on {cores} threads",
-            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
-                              "sample": sample_desc(samples1) + f", {reps1}x; {dt1:.1f} s"}}
+    per_op, desc = {}, []
+    tot = {"all": [0, 0.0], "one": [0, 0.0]}
+    for n in names:
+        wl = WORKLOADS[n]
+        cap = wl.N if wl.N <= 1600 else wl.N // 16
+        rows0 = max(1, min(cap, wl.N // 4096))
+        fwd, bwd = oracle_ops(wl, rows0)
+        t0 = time.perf_counter()
+        fwd()
+        bwd()
+        t0 = max(time.perf_counter() - t0, 1e-5)
+        rows = max(1, min(cap, int(rows0 * 2 * per_op_budget_s / t0)))
+        fwd, bwd = oracle_ops(wl, rows) if rows != rows0 else (fwd, bwd)
+        bf, bb, el = op_bytes(wl, "fwd", rows), op_bytes(wl, "bwd", rows), op_elems(wl, rows)
+        for label, threads in (("all", cores), ("one", 1)):
+            old = oracle.set_threads(threads)
+            try:
+                tf = _time_repeated(fwd, per_op_budget_s)
+                tb = _time_repeated(bwd, per_op_budget_s)
+            finally:
+                oracle.set_threads(old)
+            sfx = "" if label == "all" else "_1core"
+            for op, b, t in (("fwd", bf, tf), ("bwd", bb, tb), ("fwd+bwd", bf + bb, tf + tb)):
+                row = per_op.setdefault(f"{n}.{op}", {})
+                row["GB/s" + sfx] = round(b / t / 1e9, 4)
+                row["elements_per_s" + sfx] = round(el / t, 1)
+            tot[label][0] += bf + bb
+            tot[label][1] += tf + tb
+        desc.append(f"{n}: first {rows} of {wl.N} rows")
+    return {"value": round(tot["all"][0] / tot["all"][1] / 1e9, 4), "unit": "GB/s",
+            "cores": cores, "kind": "oracle",
+            "sample": ", ".join(desc) + f"; each op repeated for ~{per_op_budget_s} s on "
+                      f"{cores} threads and on 1 (fp64 CPU work)",
+            "single_thread": {"value": round(tot["one"][0] / tot["one"][1] / 1e9, 4),
+                              "unit": "GB/s", "cores": 1},
+            "per_op": per_op}
 
 
 def run_reference(args, names):
@@ -343,7 +400,7 @@ class Buffers:
         if wl.op == "ws":
             self.y = torch.empty(wl.N, dtype=tdt, device=dev)
             self.gw = torch.empty(wl.D, dtype=torch.float32, device=dev)
-            nbytes = wsf.ws_bwd_workspace_bytes(wl.N, wl.D, tdt, 0)
+            nbytes = wsf.ws_bwd_workspace_bytes(wl.N, wl.D, tdt, wl.block_n)
         elif wl.op == "softmax":
             self.y = torch.empty(shape, dtype=tdt, device=dev)
             self.gw = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -402,7 +459,7 @@ class Buffers:
         elif self.wl.op == "ws":
             wsf.ws_fwd(x, self.w, y=y, stream=stream)
             wsf.ws_bwd(x, self.w, dy, dx=dx, grad_w=self.gw, accumulate=accumulate,
-                       workspace=self.ws, stream=stream)
+                       workspace=self.ws, block_n=self.wl.block_n, stream=stream)
         else:
             wsf.silu_fwd(x, self.w, y=y, stream=stream)
             wsf.silu_bwd(dy, x, self.w, dx=dx, dw=self.gw, accumulate=accumulate,
@@ -421,7 +478,7 @@ class Buffers:
                 wsf.ws_fwd(self.x, self.w, y=self.y)
             else:
                 wsf.ws_bwd(self.x, self.w, self.dy, dx=self.dx, grad_w=self.gw,
-                           workspace=self.ws)
+                           workspace=self.ws, block_n=self.wl.block_n)
         else:
             if op == "fwd":
                 wsf.silu_fwd(self.x, self.w, y=self.y)
@@ -508,6 +565,10 @@ def run_cuda(args, names):
     # written back before the op starts) before every timed op, 5 warm-ups,
     # the median of 20; fwd+bwd is the two ops back to back after one flush
     isolated = isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS) if args.isolated else None
+    if args.latency_names:
+        lat = latency_per_op(lambda n: Buffers(WORKLOADS[n], dev, wsf, False), args.latency_names,
+                             wsf, dev, WORKLOADS)
+        isolated = dict(isolated or {}, **lat)
 
     # end to end through the public API with host buffers: every input is
     # copied from pinned host memory and every output back, inside the timed
@@ -629,7 +690,15 @@ def run_cuda(args, names):
     if isolated is not None:
         line["per_op_isolated"] = isolated
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(names)
+        cpu = cpu_baseline(args.latency_names + names)
+        line["cpu_baseline"] = cpu
+        # the oracle's rate beside each GPU row of the isolated protocol
+        for k, row in (line.get("per_op_isolated") or {}).items():
+            o = cpu["per_op"].get(k)
+            if o and isinstance(row, dict):
+                row["oracle_GB/s"] = o["GB/s"]
+                row["oracle_GB/s_1core"] = o["GB/s_1core"]
+                row["oracle_elements_per_s"] = o["elements_per_s"]
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -673,6 +742,65 @@ def isolated_per_op(bufs, names, wsf, dev, stream, WORKLOADS, warmup=5, reps=20)
     out["_how"] = (f"L2 flush before every timed op: a write of {2 * l2 >> 20} MiB, then a read of "
                    f"another {2 * l2 >> 20} MiB (no dirty lines left for the op to write back); "
                    f"{warmup} warm-ups, median of {reps}; fwd+bwd = both ops back to back after one flush")
+    return out
+
+
+def latency_per_op(bufs_for, names, wsf, dev, WORKLOADS, reps=100, rounds=7, host_reps=50):
+    """Small workloads that a launch's latency, not HBM, bounds (c1: the
+    worked 100 x 64 shape with 32-row tiles), timed alone.  `ms` is the
+    device time of one op: a CUDA graph of `reps` back-to-back calls is
+    replayed `rounds` times (median), so no host launch cost is included;
+    `host_us` is the wall-clock latency a caller sees for one call followed by
+    a device synchronisation (median of host_reps)."""
+    import torch
+    out = {}
+    for n in names:
+        wl = WORKLOADS[n]
+        b = bufs_for(n)
+        ops = {"fwd": lambda: b.run(wsf, "fwd"), "bwd": lambda: b.run(wsf, "bwd"),
+               "fwd+bwd": lambda: (b.run(wsf, "fwd"), b.run(wsf, "bwd"))}
+        for op, fn in ops.items():
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    fn()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(rounds):
+                a = torch.cuda.Event(enable_timing=True)
+                c = torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                c.record()
+                c.synchronize()
+                ts.append(a.elapsed_time(c) / reps)
+            hs = []
+            for _ in range(host_reps):
+                t = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                hs.append(time.perf_counter() - t)
+            del g
+            ms = statistics.median(ts)
+            nb = (op_bytes(wl, "fwd") + op_bytes(wl, "bwd")) if op == "fwd+bwd" else op_bytes(wl, op)
+            out[f"{n}.{op}"] = {"ms": round(ms, 5), "us": round(ms * 1e3, 2),
+                                "GB/s": round(nb / (ms * 1e-3) / 1e9, 2),
+                                "frac_of_8TBs": round(nb / (ms * 1e-3) / 1e9 / 8000.0, 6),
+                                "elements_per_s": round(op_elems(wl) / (ms * 1e-3), 1),
+                                "host_us": round(statistics.median(hs) * 1e6, 1),
+                                "protocol": "latency"}
+    out["_how_latency"] = (f"latency-bound workloads ({', '.join(names)}): ms = device time of one "
+                           f"op from a CUDA graph of {reps} back-to-back calls (median of {rounds} "
+                           f"replays); host_us = wall clock of one call plus a device sync "
+                           f"(median of {host_reps})")
     return out
 
 
@@ -797,9 +925,16 @@ def main(argv=None):
     ap.add_argument("--isolated", action=argparse.BooleanOptionalAction, default=True,
                     help="also time every op alone after an L2 flush (median of 20)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-latency", action="store_true",
+                    help="skip the latency-bound workload c1 (timed alone, outside the step)")
     args = ap.parse_args(argv)
     names = ORDER_FWD if args.workload == "all" else [s.strip() for s in args.workload.split(",")]
-    assert all(n in ORDER_FWD + EXTRA for n in names), names
+    assert all(n in ORDER_FWD + EXTRA + LATENCY for n in names), names
+    args.latency_names = [] if args.no_latency else (
+        LATENCY if args.workload == "all" else [n for n in names if n in LATENCY])
+    names = [n for n in names if n not in LATENCY]
+    if not names:
+        ap.error("name at least one workload of the step (c2..c5 or a row workload) besides c1")
     if args.warmup < 3 and args.impl == "cuda":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

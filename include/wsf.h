@@ -128,9 +128,10 @@ int ws_fwd(const void* x, int64_t ldx, const float* w, void* y, int64_t N, int64
            wsf_stream_t stream);
 
 /*
- * ws_bwd_workspace_bytes — size in bytes of the fp32 partial buffer that
- * ws_bwd needs for these sizes: P·D·4 rounded up to 256, where P is the
- * number of row tiles.  block_n > 0 forces tiles of block_n consecutive rows
+ * ws_bwd_workspace_bytes — size in bytes of the partial buffer that ws_bwd
+ * needs for these sizes: two binary32 planes (high and low parts of the
+ * compensated partial sums) of P·D values, each rounded up to 256 bytes,
+ * where P is the number of row tiles.  block_n > 0 forces tiles of block_n consecutive rows
  * (P = ceil(N / block_n)), as in [WS §3]'s BLOCK_N; block_n == 0 lets the
  * library choose.  Returns 0 when no workspace is needed, and SIZE_MAX for
  * invalid arguments.  Host-only; touches no device.
@@ -144,8 +145,10 @@ size_t ws_bwd_workspace_bytes(int64_t N, int64_t D, int dtype, int64_t block_n);
  * Inputs: x [N, D] dtype (row stride ldx), w [D] binary32, dy [N] dtype.
  * Outputs: dx [N, D] dtype (row stride lddx), grad_w [D] binary32.
  * Stage 1 writes dx and, for each row tile p, partial[p, d] = Σ over the
- * tile's rows of x[i,d]·dy[i] into `workspace` (binary32, [P, D]).
- * Stage 2 sums partial[0..P-1, d] in a fixed order; with accumulate == 1 the
+ * tile's rows of x[i,d]·dy[i] into `workspace` as a compensated binary32
+ * pair (high and low planes, [P, D] each).  Stage 2 sums partial[0..P-1, d]
+ * in a fixed order, again as a pair, and rounds it once: grad_w is as
+ * accurate as a sum in twice binary32's precision.  With accumulate == 1 the
  * result is added to the existing grad_w[d] (old + sum, one binary32 add),
  * with accumulate == 0 it replaces it ([SILU] § fp32 accumulation ...: a
  * gradient accumulates with += across micro-batches).  N == 0 gives
@@ -164,12 +167,12 @@ int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
  * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
  * synchronisation.  Same arguments, results and errors as ws_bwd, minus the
  * workspace: the per-tile partials go to a scratch array of
- * WSF_NOALLOC_SCRATCH_BYTES (4 MiB) that lives in the library's own device
+ * WSF_NOALLOC_SCRATCH_BYTES (8 MiB) that lives in the library's own device
  * memory, one copy per device that loads the library, held until the
  * process exits.  The call allocates nothing.
  *   - Sizes whose ws_bwd_workspace_bytes(N, D, dtype, block_n) exceeds
  *     WSF_NOALLOC_SCRATCH_BYTES are rejected with WSF_ERR_WORKSPACE before
- *     anything is enqueued (the five benchmark workloads need at most 3.6 MiB).
+ *     anything is enqueued (the five benchmark workloads need at most 7.2 MiB).
  *   - The first call on a device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with the device current); make that first call
  *     before any stream capture.
@@ -177,7 +180,7 @@ int ws_bwd(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
  *     nothing in it needs clearing, but calls whose kernels overlap on the
  *     GPU (e.g. issued on two streams) race on it: serialise them.
  */
-#define WSF_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define WSF_NOALLOC_SCRATCH_BYTES (8u << 20)
 int ws_bwd_noalloc(const void* x, int64_t ldx, const float* w, const void* dy, void* dx,
                    int64_t lddx, float* grad_w, int accumulate, int64_t block_n, int64_t N,
                    int64_t D, int dtype, wsf_stream_t stream);
@@ -190,9 +193,10 @@ int ws_bwd_noalloc(const void* x, int64_t ldx, const float* w, const void* dy, v
 int silu_fwd(const void* x, const float* w, void* y, int64_t n, int dtype, wsf_stream_t stream);
 
 /*
- * silu_bwd_workspace_bytes — bytes of the fp32 per-block partial buffer for
- * silu_bwd (P·4 rounded up to 256); 0 when none is needed, SIZE_MAX for
- * invalid arguments.  Host-only.
+ * silu_bwd_workspace_bytes — bytes of the per-block partial buffer for
+ * silu_bwd (two binary32 planes of P values, high and low parts, each rounded
+ * up to 256 bytes); 0 when none is needed, SIZE_MAX for invalid arguments.
+ * Host-only.
  */
 size_t silu_bwd_workspace_bytes(int64_t n, int dtype);
 
@@ -202,9 +206,10 @@ size_t silu_bwd_workspace_bytes(int64_t n, int dtype);
  *   dx = dy · w · (s + x·s·(1 - s))             elementwise (written)
  *   dw = Σ_k dy_k · x_k · s_k                    scalar reduction over all n
  * s is recomputed from x (nothing from the forward is needed but x and w).
- * Stage 1 writes dx and one binary32 partial of dw per block into
- * `workspace`; stage 2 reduces the partials in a fixed tree order into *dw
- * (added to the existing value when accumulate == 1).  n == 0 gives dw = 0
+ * Stage 1 writes dx and one compensated binary32 pair, the partial of dw, per
+ * block into `workspace`; stage 2 reduces the pairs in a fixed tree order,
+ * rounds once and writes *dw (added to the existing value when
+ * accumulate == 1).  n == 0 gives dw = 0
  * (or leaves it when accumulating).
  */
 int silu_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw, int accumulate,

@@ -58,24 +58,34 @@ def test_status_strings(wsf):
     assert wsf.status_string(-100) == "unknown status"
 
 
+def _plane_bytes(P, D):
+    """One binary32 plane of P·D partial sums, rounded up to 256 bytes."""
+    return (P * D + 63) // 64 * 64 * 4
+
+
 def test_workspace_queries(wsf):
     q = wsf.lib.ws_bwd_workspace_bytes
-    # the worked shape: 100 rows in 32-row tiles -> 4 partial rows of 64 fp32
-    assert q(100, 64, wsf.F32, 32) == 4 * 64 * 4
-    assert q(100, 64, wsf.F32, 1) == ((100 * 64 * 4 + 255) // 256) * 256
+    # the worked shape: 100 rows in 32-row tiles -> 4 partial rows of 64,
+    # held as compensated pairs (a plane of high parts, one of low parts)
+    assert q(100, 64, wsf.F32, 32) == 2 * 4 * 64 * 4
+    assert q(100, 64, wsf.F32, 1) == 2 * _plane_bytes(100, 64)
     assert q(0, 64, wsf.F32, 0) == 0 and q(5, 0, wsf.F16, 0) == 0
     assert q(-1, 4, wsf.F32, 0) == wsf.SIZE_MAX
     assert q(4, 4, 7, 0) == wsf.SIZE_MAX and q(4, 4, wsf.F32, -1) == wsf.SIZE_MAX
     for N, D, dt in [(1 << 20, 1024, wsf.BF16), (1 << 24, 64, wsf.F16), (4096, 65536, wsf.F32),
                      (7, 5, wsf.F32), (1, 1, wsf.F16)]:
-        b = q(N, D, dt, 0)
-        assert b % 256 == 0 and b >= 4 * D and b <= max(4 * D * N, 256) + 255
-        # at most 912 tiles and at most one tile per 64 rows
-        P = b // (4 * D)
-        assert P <= 912 and (P <= max(1, -(-N // 64)) or b - 4 * D * max(1, -(-N // 64)) < 256)
+        # at most 912 CTAs per launch (tiles x 256-chunk column slices), at
+        # most one tile per 64 rows, at least one
+        es = 4 if dt == wsf.F32 else 2
+        slices = -(-(-(-(D * es) // 16)) // 256)
+        P = max(1, min(-(-N // 64), 912 // slices))
+        assert q(N, D, dt, 0) == 2 * _plane_bytes(P, D), (N, D, dt)
+    # the measurement workloads fit the no-allocation entry point's scratch
+    assert max(q(1 << 20, 1024, wsf.BF16, 0), q(1 << 24, 64, wsf.F16, 0),
+               q(4096, 65536, wsf.F32, 0)) <= 8 << 20
     s = wsf.lib.silu_bwd_workspace_bytes
-    assert s(0, wsf.F16) == 0 and s(1, wsf.F16) == 256 and s(-1, wsf.F16) == wsf.SIZE_MAX
-    assert s(8192 * 4096, wsf.F16) == 1216 * 4 // 256 * 256 + (256 if 1216 * 4 % 256 else 0)
+    assert s(0, wsf.F16) == 0 and s(1, wsf.F16) == 2 * 256 and s(-1, wsf.F16) == wsf.SIZE_MAX
+    assert s(8192 * 4096, wsf.F16) == 2 * _plane_bytes(1216, 1)
 
 
 F = 0x10000000  # fake, well-aligned device addresses; never dereferenced
@@ -136,6 +146,27 @@ def test_ws_bwd_rejects(wsf):
     assert call(gw=3 * F) == wsf.ERR_OVERLAP
     assert call(ws=4 * F + 128) == wsf.ERR_OVERLAP
     assert call(dx=4 * F + 2) == wsf.ERR_MISALIGNED
+
+
+def test_ws_bwd_noalloc_rejects(wsf):
+    """The no-allocation entry point checks its arguments as ws_bwd does, in
+    the same order, before its scratch limit and before touching a device."""
+    L = wsf.lib
+    N, D = 2048, 1024  # one-row tiles of 1024 fp32 need 16 MiB, over the 8 MiB scratch
+
+    def call(x=F, N=N, bn=0, dt=0, acc=0, ld=D):
+        return L.ws_bwd_noalloc(_p(x) if x else None, ld, _p(2 * F), _p(3 * F), _p(4 * F), ld,
+                                _p(5 * F), acc, bn, N, D, dt, None)
+
+    assert call(bn=1) == wsf.ERR_WORKSPACE
+    assert call(x=0, bn=1) == wsf.ERR_NULL_PTR          # a NULL pointer wins, as from ws_bwd
+    assert call(dt=7, bn=1) == wsf.ERR_BAD_DTYPE
+    assert call(N=-1) == wsf.ERR_BAD_SHAPE
+    assert call(acc=3, bn=1) == wsf.ERR_BAD_ARG
+    assert call(ld=D - 1, bn=1) == wsf.ERR_BAD_STRIDE
+    assert call(x=4 * F + 64) == wsf.ERR_OVERLAP         # dx over x
+    assert call(x=F + 1, dt=1, bn=1) == wsf.ERR_MISALIGNED
+    assert L.ws_bwd_noalloc(None, 0, None, None, None, 0, None, 0, 0, 0, 0, 0, None) == wsf.OK
 
 
 def test_silu_rejects(wsf):

@@ -54,8 +54,9 @@ def test_ws_full_size(wsf, name):
     assert res and res.clause2 == 0, ("dx", res)
     full = oracle.ws_bwd(x, w, dy, want_dx=False)
     res = check_reduction(gw.cpu(), full["grad_w"], full["grad_w_abs"], N, GRAD_TOL)
-    print(name, "grad_w", res)
-    assert res, ("grad_w", res)
+    # compensated sums: every column within 1e-5 of the exact value, none
+    # passing only by the cancellation clause
+    assert res and res.clause2 == 0, ("grad_w", res)
 
 
 def test_silu_full_size(wsf):
@@ -75,9 +76,7 @@ def test_silu_full_size(wsf):
     assert res and res.clause2 == 0, ("y", res)
     r = oracle.silu_bwd(dy, x, wl.w_scalar)
     res = check_elementwise(dx.cpu(), r["dx"], r["dx_exact"], scale=r["dx_scale"])
-    print("c2 dx", res)
-    assert res, ("dx", res)
+    assert res and res.clause2 == 0, ("dx", res)
     res = check_reduction(np.array([float(dw)]), np.array([r["dw"]]), np.array([r["dw_abs"]]), n,
                           GRAD_TOL)
-    print("c2 dw", res, float(dw), r["dw"])
-    assert res, ("dw", res)
+    assert res and res.clause2 == 0, ("dw", res, float(dw), r["dw"])

@@ -49,7 +49,7 @@ def test_ws_more_than_2_31_elements(wsf):
     assert res and res.clause2 == 0, ("dx", res)
     full = oracle.ws_bwd(x, w, dy, want_dx=False)
     res = check_reduction(gw.cpu(), full["grad_w"], full["grad_w_abs"], N, GRAD_TOL)
-    assert res, ("grad_w", res)
+    assert res and res.clause2 == 0, ("grad_w", res)
 
 
 def test_silu_more_than_2_31_elements(wsf):
