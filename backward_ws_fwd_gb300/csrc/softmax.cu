@@ -31,21 +31,70 @@ namespace wsf {
 template <typename T>
 constexpr bool kSoftmaxFast = !std::is_same<T, float>::value;
 
-// exp(a − b).  For binary32 storage the difference is split exactly into
-// s + e (TwoSum) and exp(s)·(1 + e) is returned, so the rounding of a − b
-// (up to |a − b|·2^-24 in the exponent) does not reach the result; 16-bit
-// storage uses the hardware exponential of the rounded difference.
+// ---------------------------------------------------------------------------
+// exp(a − b) for binary32 rows, within a few units of 2^-24 relative, built
+// on the hardware base-2 exponential:
+//  1. d = a − b exactly, as dh + dl (Knuth's TwoSum), so the rounding of the
+//     difference (up to |d|·2^-24 in the exponent) never reaches the result;
+//  2. t = d·log2(e) as th + tl, with log2(e) carried as L1 + L2 (L1 = log2 e
+//     rounded to binary32, L2 = the remainder rounded to binary32): th is
+//     dh·L1 rounded, its rounding error is recovered exactly with an FMA
+//     (Dekker's exact product), and dl·L1 + dh·L2 are added to that error;
+//  3. exp(d) = 2^th · 2^tl: 2^th from ex2.approx (subnormal results kept),
+//     2^tl = 1 + tl·ln 2 to first order (|tl| < 2^-15 wherever 2^th does
+//     not underflow, so the neglected term is below 2^-31 of the result).
+// A masked logit (a = −inf) is first raised to −2^100, whose exponential
+// underflows to +0 as exp(−inf) does, without the NaN that −inf − (−inf)
+// would leave in the split.
+constexpr float kLog2eHi = 1.44269502162933349609375f;  // 0x3FB8AA3B
+constexpr float kLog2eLo = 1.925963033500011e-08f;      // log2(e) − kLog2eHi, rounded
+constexpr float kLn2f = 0.693147182464599609375f;       // ln 2 rounded to binary32
+constexpr float kMaskFloor = 0x1p100f;
+
+__device__ __forceinline__ float ex2_keep_subnormal(float v) {
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ float exp_diff_f32(float a, float b) {
+    float dh, dl;
+    two_sum(fmaxf(a, -kMaskFloor), -b, dh, dl);
+    const float nth = __fmul_rn(dh, -kLog2eHi);  // −th
+    const float tl = fmaf(dh, kLog2eLo, fmaf(dl, kLog2eHi, fmaf(dh, kLog2eHi, nth)));
+    const float r = ex2_keep_subnormal(-nth);
+    return fmaf(r, __fmul_rn(tl, kLn2f), r);
+}
+
+// exp_diff_f32 on two lanes at once (packed f32x2 arithmetic; the same
+// operations in the same order, so each lane gets the scalar function's
+// bits).  a2: two values of a; nb2 = (−b, −b).
+__device__ __forceinline__ uint64_t exp_diff_f32x2(uint64_t a2, uint64_t nb2) {
+    float a0, a1;
+    f2_unpack(a2, a0, a1);
+    a2 = f2_pack(fmaxf(a0, -kMaskFloor), fmaxf(a1, -kMaskFloor));
+    // TwoSum(a, −b)
+    const uint64_t dh = f2_add(a2, nb2);
+    const uint64_t bp = f2_sub(dh, a2);
+    const uint64_t dl = f2_add(f2_sub(a2, f2_sub(dh, bp)), f2_sub(nb2, bp));
+    const uint64_t L1 = f2_pack(kLog2eHi, kLog2eHi), L2 = f2_pack(kLog2eLo, kLog2eLo);
+    const uint64_t nth = f2_mul(dh, f2_pack(-kLog2eHi, -kLog2eHi));
+    const uint64_t tl = f2_fma(dh, L2, f2_fma(dl, L1, f2_fma(dh, L1, nth)));
+    float n0, n1;
+    f2_unpack(nth, n0, n1);
+    const uint64_t r = f2_pack(ex2_keep_subnormal(-n0), ex2_keep_subnormal(-n1));
+    return f2_fma(r, f2_mul(tl, f2_pack(kLn2f, kLn2f)), r);
+}
+
+// exp(a − b).  Binary32 storage: exp_diff_f32 above.  16-bit storage: the
+// hardware exponential of the rounded difference (its error is far below a
+// 16-bit unit).
 template <bool Fast>
 __device__ __forceinline__ float exp_diff(float a, float b) {
-    if constexpr (Fast) {
+    if constexpr (Fast)
         return __expf(a - b);
-    } else {
-        float d, e;
-        two_sum(a, -b, d, e);
-        const float r = expf(d);
-        // a = −inf (a masked logit) makes e NaN; exp(−inf) = 0 stands as is
-        return r > 0.f ? fmaf(r, e, r) : r;
-    }
+    else
+        return exp_diff_f32(a, b);
 }
 
 // Reductions over a group of TPR threads (aligned, consecutive).  Groups of
@@ -818,7 +867,7 @@ __global__ void __launch_bounds__(NT)
 // into L2 (prefetch_slice); in the backward, prefetching y and dy measured
 // slower (twice the L2 footprint).  Elements outside the row (windowed edges, the tail of the
 // last slice) enter as −inf (forward) or 0 (backward).
-constexpr int kTwoPassNT = 256, kTwoPassCS = 16, kTwoPassU = 4;
+constexpr int kTwoPassNT = 256, kTwoPassCS = 8, kTwoPassU = 4;
 
 // Thread 0 prefetches into L2 this CTA's chunks [c0, c0 + SL) of a row (only
 // the 16-byte blocks that hold the row's own elements), so that the next
@@ -898,9 +947,12 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
         const T* xr = x + row * ldx;
         const Win<T, U> win{win_off<T, U>(xr), D};
         if (threadIdx.x == 0 && row + ncl < N) prefetch_slice<T, U>(xr + ncl * ldx, D, c0, SL);
-        // pass 1: this thread's maximum m and Σ exp(x − m)
+        // pass 1: this thread's maximum m and Σ exp(x − m) (binary32 rows:
+        // two compensated lanes in packed f32x2 arithmetic, added together at
+        // the end)
         float m = -INFINITY;
         Acc2 s = acc2_zero();
+        Acc2x2 s2{0ull, 0ull};
         for (int b = threadIdx.x; b < SL; b += STEP) {
             Raw16 cur[UU];
 #pragma unroll
@@ -919,27 +971,49 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
                 for (int v = 0; v < V; v++) mb = fmaxf(mb, f[v]);
             }
             if (mb == -INFINITY) continue;  // nothing finite yet
-            if (mb > m && s.hi != 0.f) {    // rescale the sum to the new maximum
-                const float g = rescale<kComp>(m, mb);
-                if constexpr (kComp) {
-                    const float hi = __fmul_rn(s.hi, g);
-                    s = Acc2{hi, fmaf(s.lo, g, fmaf(s.hi, g, -hi))};
-                } else {
-                    s.hi *= g;
+            if constexpr (kComp) {
+                if (mb > m) {  // rescale both lanes to the new maximum (0 while m = −inf)
+                    const float g = exp_diff_f32(m, mb);
+                    const uint64_t g2 = f2_pack(g, g), ng2 = f2_pack(-g, -g);
+                    const uint64_t nhi = f2_mul(s2.hi, ng2);  // −fl(hi·g)
+                    s2.lo = f2_fma(s2.lo, g2, f2_fma(s2.hi, g2, nhi));
+                    s2.hi = f2_mul(s2.hi, g2);
+                }
+                m = mb;
+                const uint64_t nm2 = f2_pack(-m, -m);
+#pragma unroll
+                for (int u = 0; u < UU; u++) {
+                    float f[V];
+                    widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+#pragma unroll
+                    for (int q = 0; q < V / 2; q++) {
+                        const uint64_t e = exp_diff_f32x2(f2_pack(f[2 * q], f[2 * q + 1]), nm2);
+                        // TwoSum of each lane's running sum and e
+                        const uint64_t t = f2_add(s2.hi, e);
+                        const uint64_t bp = f2_sub(t, s2.hi);
+                        const uint64_t err =
+                            f2_add(f2_sub(s2.hi, f2_sub(t, bp)), f2_sub(e, bp));
+                        s2.hi = t;
+                        s2.lo = f2_add(s2.lo, err);
+                    }
+                }
+            } else {
+                if (mb > m && s.hi != 0.f) s.hi *= rescale<kComp>(m, mb);
+                m = mb;
+#pragma unroll
+                for (int u = 0; u < UU; u++) {
+                    float f[V];
+                    widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+#pragma unroll
+                    for (int v = 0; v < V; v++)
+                        add_to<kComp>(s, exp2_approx(fmaf(f[v], kLog2e, -m * kLog2e)));
                 }
             }
-            m = mb;
-#pragma unroll
-            for (int u = 0; u < UU; u++) {
-                float f[V];
-                widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
-#pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float e = kComp ? exp_diff<false>(f[v], m)
-                                          : exp2_approx(fmaf(f[v], kLog2e, -m * kLog2e));
-                    add_to<kComp>(s, e);
-                }
-            }
+        }
+        if constexpr (kComp) {
+            Acc2 l0, l1;
+            acc2x2_unpack(s2, l0, l1);
+            s = acc2_add(l0, l1);
         }
         // the warp's maximum and its sum relative to it
         const float mw = warp_max(m);
@@ -1006,11 +1080,17 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
                 if (c < SL && win.has(cc)) {
                     float f[V], o[V];
                     widen_chunk<T, U, true>(cur[u], win, c, cc, SL, f);
+                    if constexpr (kComp) {
+                        const uint64_t nM2 = f2_pack(-Mi.x, -Mi.x), inv2 = f2_pack(Mi.y, Mi.y);
 #pragma unroll
-                    for (int v = 0; v < V; v++) {
-                        const float e = kComp ? exp_diff<false>(f[v], Mi.x)
-                                              : exp2_approx(fmaf(f[v], kLog2e, -Mi.x * kLog2e));
-                        o[v] = e * Mi.y;
+                        for (int q = 0; q < V / 2; q++)
+                            f2_unpack(f2_mul(exp_diff_f32x2(f2_pack(f[2 * q], f[2 * q + 1]), nM2),
+                                             inv2),
+                                      o[2 * q], o[2 * q + 1]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < V; v++)
+                            o[v] = exp2_approx(fmaf(f[v], kLog2e, -Mi.x * kLog2e)) * Mi.y;
                     }
                     store_chunk<T, U>(yr, win, cc, o);
                 }
@@ -1022,7 +1102,7 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
 }
 
 template <typename T, bool U>
-__global__ void __launch_bounds__(kTwoPassNT, 3)
+__global__ void __launch_bounds__(kTwoPassNT, 2)
     softmax_bwd_cluster2(const T* __restrict__ y, int64_t ldy, const T* __restrict__ dy,
                          int64_t lddy, T* __restrict__ dx, int64_t lddx, int64_t N, int D,
                          int SL) {

@@ -243,6 +243,31 @@ def test_softmax_two_pass_extremes(wsf):
     assert bool((y[3, 1000:] == 0).all()) and bool((y[4, :150000] == 0).all())
 
 
+@pytest.mark.parametrize("N,D,mis", [(64, 64, 0), (16, 1001, 0), (8, 40000, 0), (4, 300000, 0),
+                                     (4, 300007, 1)])
+def test_softmax_f32_exponential_range(wsf, N, D, mis):
+    """The binary32 exponential (TwoSum-split difference, double-float
+    product with log2 e, hardware 2^x, first-order correction) over its
+    whole range, on the row, windowed, cluster and two-pass paths: each row
+    holds a 0 (its maximum) and logits spread evenly over [−110, 0], so that
+    y runs from normal values through subnormal ones to underflow.  Every y
+    within 1e-6 of the exact value (or of the binary32 subnormal quantum)."""
+    j = np.arange(D, dtype=np.float64)
+    frac = (j * 0.6180339887498949 + np.arange(N)[:, None] * 0.137) % 1.0
+    x = torch.from_numpy((-110.0 * frac).astype(np.float32))
+    x[:, 0] = 0.0
+    dy = torch.randn(N, D, generator=torch.Generator().manual_seed(D))
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin, mis=mis)
+    _check(x, dy, y, dx, yin)
+    ye, _ = oracle.softmax_fwd(x)
+    normal = np.abs(ye) >= 2.0 ** -126
+    rel = np.abs(y.double().numpy() - ye)[normal] / np.abs(ye)[normal]
+    print(f"N={N} D={D}: max relative error of normal y {rel.max():.3g}, "
+          f"{int((~normal & (ye > 0)).sum())} subnormal")
+    assert rel.max() <= 1e-6
+
+
 def test_softmax_cluster_no_wait_timeouts(wsf):
     # every cluster launch so far exchanged its partial sums without a wait
     # running out (the counter is per process and device)
