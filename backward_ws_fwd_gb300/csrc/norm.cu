@@ -718,14 +718,28 @@ __device__ __forceinline__ Acc2 staged_sum_x(const Raw16* slot, unsigned valid) 
 template <typename E, int CPT, int NT, int V, bool Comp>
 __device__ __forceinline__ Acc2 staged_sum_sq(const Raw16* slot, unsigned valid) {
     Acc2 s = acc2_zero();
+    uint64_t a = 0ull;  // 16-bit rows: even and odd columns in two packed lanes
 #pragma unroll
     for (int c = 0; c < CPT; c++) {
         if (valid >> c & 1u) {
             float f[V];
             E::widen(slot[c * NT], f);
+            if constexpr (Comp) {
 #pragma unroll
-            for (int v = 0; v < V; v++) s_fma<Comp>(s, f[v], f[v]);
+                for (int v = 0; v < V; v++) s_fma<Comp>(s, f[v], f[v]);
+            } else {
+#pragma unroll
+                for (int h = 0; h < V / 2; h++) {
+                    const uint64_t d = f2_pack(f[2 * h], f[2 * h + 1]);
+                    a = f2_fma(d, d, a);
+                }
+            }
         }
+    }
+    if constexpr (!Comp) {
+        float a0, a1;
+        f2_unpack(a, a0, a1);
+        s.hi = a0 + a1;
     }
     return s;
 }
@@ -737,6 +751,44 @@ __device__ __forceinline__ void center(float (&f)[CPT][V], unsigned valid, const
         if (valid >> c & 1u)
 #pragma unroll
             for (int v = 0; v < V; v++) f[c][v] = (f[c][v] - m.mu0) - m.c;
+}
+
+// center on packed pairs: (x − μ₀) − c per lane, the bits of `center`.
+template <int CPT, int V>
+__device__ __forceinline__ void center2(float (&f)[CPT][V], unsigned valid, const Mean& m) {
+    const uint64_t mu2 = f2_pack(m.mu0, m.mu0), c2 = f2_pack(m.c, m.c);
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+        if (valid >> c & 1u)
+#pragma unroll
+            for (int q = 0; q < V / 2; q++)
+                f2_unpack(f2_sub(f2_sub(f2_pack(f[c][2 * q], f[c][2 * q + 1]), mu2), c2),
+                          f[c][2 * q], f[c][2 * q + 1]);
+}
+
+// Plain binary32 Σ f² over the valid chunks, even and odd columns in two
+// packed lanes, the lanes added at the end (16-bit rows).
+template <int CPT, int V>
+__device__ __forceinline__ Acc2 sum_sq2(const float (&f)[CPT][V], unsigned valid) {
+    uint64_t a = 0ull;
+#pragma unroll
+    for (int c = 0; c < CPT; c++)
+        if (valid >> c & 1u)
+#pragma unroll
+            for (int q = 0; q < V / 2; q++) {
+                const uint64_t d = f2_pack(f[c][2 * q], f[c][2 * q + 1]);
+                a = f2_fma(d, d, a);
+            }
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    return Acc2{a0 + a1, 0.f};
+}
+
+// The sum of a packed pair's two lanes as a (plain) row sum.
+__device__ __forceinline__ Acc2 lanes_sum(uint64_t a) {
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    return Acc2{a0 + a1, 0.f};
 }
 
 template <typename T, bool LN, int NT, int S>
@@ -798,7 +850,12 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         cp_async_commit();
         float f[CPT][V];
         load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
-        if constexpr (LN) center<CPT, V>(f, valid, mn);
+        if constexpr (LN) {
+            if constexpr (C)
+                center<CPT, V>(f, valid, mn);
+            else
+                center2<CPT, V>(f, valid, mn);
+        }
         if constexpr (PIPE) {
             if (k + 1 < iters) {  // row k + 1's Σx², turn k + 1
                 Acc2 q[1] = {staged_sum_sq<E, CPT, NT, V, C>(
@@ -810,11 +867,15 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         Acc2 sm[LN ? 2 : 1];
         sm[0] = acc2_zero();
         if constexpr (LN) {
+            if constexpr (C) {
 #pragma unroll
-            for (int c = 0; c < CPT; c++)
-                if (valid >> c & 1u)
+                for (int c = 0; c < CPT; c++)
+                    if (valid >> c & 1u)
 #pragma unroll
-                    for (int v = 0; v < V; v++) s_fma<C>(sm[0], f[c][v], f[c][v]);
+                        for (int v = 0; v < V; v++) s_fma<C>(sm[0], f[c][v], f[c][v]);
+            } else {
+                sm[0] = sum_sq2<CPT, V>(f, valid);
+            }
             sm[LN ? 1 : 0] = k + 1 < iters
                 ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
                 : acc2_zero();
@@ -824,14 +885,20 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         }
         const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
         if constexpr (LN) mn = mean_of(sm[LN ? 1 : 0], fd, inv_d);
+        const uint64_t r2 = f2_pack(r, r);
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
                 float o[V];
 #pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float xh = f[c][v] * r;
-                    o[v] = LN ? fmaf(xh, wv[c][v], bv[c][v]) : xh * wv[c][v];
+                for (int q = 0; q < V / 2; q++) {
+                    // x̂·w (+ b) on two columns at once, each lane rounded as the
+                    // scalar form would be
+                    const uint64_t xh = f2_mul(f2_pack(f[c][2 * q], f[c][2 * q + 1]), r2);
+                    const uint64_t w2 = f2_pack(wv[c][2 * q], wv[c][2 * q + 1]);
+                    f2_unpack(LN ? f2_fma(xh, w2, f2_pack(bv[c][2 * q], bv[c][2 * q + 1]))
+                                 : f2_mul(xh, w2),
+                              o[2 * q], o[2 * q + 1]);
                 }
                 st_stream(yrow + (int64_t)c * NT * V, E::narrow(o));
             }
@@ -972,6 +1039,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         const Raw16* pg = gs + slot * CPT * NT + threadIdx.x;
 #pragma unroll
         for (int n = 0; n < K; n++) q[n] = acc2_zero();
+        uint64_t a0 = 0ull, a1 = 0ull;  // 16-bit rows: packed lanes of Σ x², Σ g·x
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
@@ -979,12 +1047,27 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 E::widen(px[c * NT], dc);
                 E::widen(pg[c * NT], gc);
                 w_of(c, wc);
+                if constexpr (C) {
 #pragma unroll
-                for (int v = 0; v < V; v++) {
-                    s_fma<C>(q[0], dc[v], dc[v]);
-                    s_fma<C>(q[1], gc[v] * wc[v], dc[v]);
+                    for (int v = 0; v < V; v++) {
+                        s_fma<C>(q[0], dc[v], dc[v]);
+                        s_fma<C>(q[1], gc[v] * wc[v], dc[v]);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < V / 2; h++) {
+                        const uint64_t d2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
+                        const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
+                                                   f2_pack(wc[2 * h], wc[2 * h + 1]));
+                        a0 = f2_fma(d2, d2, a0);
+                        a1 = f2_fma(g2, d2, a1);
+                    }
                 }
             }
+        }
+        if constexpr (!C) {
+            q[0] = lanes_sum(a0);
+            q[1] = lanes_sum(a1);
         }
     };
     Mean mn{0.f, 0.f};
@@ -1009,11 +1092,20 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         const Raw16* cg = gs + (k % S) * CPT * NT + threadIdx.x;
         // d of chunk c (x, or x − μ), widened from the staged slot in each
         // pass rather than held across the exchange
+        const uint64_t mu2 = f2_pack(mn.mu0, mn.mu0), mc2 = f2_pack(mn.c, mn.c);
         auto d_of = [&](int c, float (&o)[V]) {
             E::widen(cx[c * NT], o);
-            if constexpr (LN)
+            if constexpr (LN) {
+                if constexpr (C) {
 #pragma unroll
-                for (int v = 0; v < V; v++) o[v] = (o[v] - mn.mu0) - mn.c;
+                    for (int v = 0; v < V; v++) o[v] = (o[v] - mn.mu0) - mn.c;
+                } else {
+#pragma unroll
+                    for (int h = 0; h < V / 2; h++)
+                        f2_unpack(f2_sub(f2_sub(f2_pack(o[2 * h], o[2 * h + 1]), mu2), mc2),
+                                  o[2 * h], o[2 * h + 1]);
+                }
+            }
         };
         Acc2 sums[K];
         if constexpr (PIPE) {
@@ -1026,6 +1118,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         } else {
 #pragma unroll
             for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+            uint64_t a0 = 0ull, a1 = 0ull, a2 = 0ull;  // 16-bit rows: packed lanes
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
                 if (valid >> c & 1u) {
@@ -1033,14 +1126,31 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                     d_of(c, dc);
                     E::widen(cg[c * NT], gc);
                     w_of(c, wc);
+                    if constexpr (C) {
 #pragma unroll
-                    for (int v = 0; v < V; v++) {
-                        const float gg = gc[v] * wc[v];
-                        s_fma<C>(sums[0], dc[v], dc[v]);
-                        s_fma<C>(sums[1], gg, dc[v]);
-                        if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
+                        for (int v = 0; v < V; v++) {
+                            const float gg = gc[v] * wc[v];
+                            s_fma<C>(sums[0], dc[v], dc[v]);
+                            s_fma<C>(sums[1], gg, dc[v]);
+                            if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < V / 2; h++) {
+                            const uint64_t d2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
+                            const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
+                                                       f2_pack(wc[2 * h], wc[2 * h + 1]));
+                            a0 = f2_fma(d2, d2, a0);
+                            a1 = f2_fma(g2, d2, a1);
+                            if constexpr (LN) a2 = f2_add(a2, g2);
+                        }
                     }
                 }
+            }
+            if constexpr (!C) {
+                sums[0] = lanes_sum(a0);
+                sums[1] = lanes_sum(a1);
+                if constexpr (LN) sums[LN ? 2 : 0] = lanes_sum(a2);
             }
             if constexpr (LN)
                 if (k + 1 < iters)
@@ -1052,6 +1162,8 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
         const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;
         T* dxrow = dx + row * lddx + (int64_t)l * V;
+        const uint64_t r2 = f2_pack(r, r), nrmgx2 = f2_pack(-rmgx, -rmgx),
+                       nrmg2 = f2_pack(-rmg, -rmg);
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
@@ -1059,14 +1171,19 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 d_of(c, dc);
                 E::widen(cg[c * NT], gc);
                 w_of(c, wc);
+                // dx = r·((g − mean g) − x̂·mean(g·x̂)), g = dy·w, two columns
+                // an instruction (each lane rounded as the scalar form would be)
 #pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float xh = dc[v] * r;
-                    const float gg = gc[v] * wc[v];
-                    // r·((g − mean g) − x̂·mean(g·x̂))
-                    o[v] = fmaf(-xh, rmgx, fmaf(gg, r, -rmg));
-                    aw[c][v] = fmaf(gc[v], xh, aw[c][v]);
-                    if constexpr (LN) ab[c][v] += gc[v];
+                for (int h = 0; h < V / 2; h++) {
+                    const uint64_t dy2 = f2_pack(gc[2 * h], gc[2 * h + 1]);
+                    const uint64_t xh = f2_mul(f2_pack(dc[2 * h], dc[2 * h + 1]), r2);
+                    const uint64_t gg = f2_mul(dy2, f2_pack(wc[2 * h], wc[2 * h + 1]));
+                    f2_unpack(f2_fma(xh, nrmgx2, f2_fma(gg, r2, nrmg2)), o[2 * h], o[2 * h + 1]);
+                    f2_unpack(f2_fma(dy2, xh, f2_pack(aw[c][2 * h], aw[c][2 * h + 1])),
+                              aw[c][2 * h], aw[c][2 * h + 1]);
+                    if constexpr (LN)
+                        f2_unpack(f2_add(f2_pack(ab[c][2 * h], ab[c][2 * h + 1]), dy2),
+                                  ab[c][2 * h], ab[c][2 * h + 1]);
                 }
                 st_stream(dxrow + (int64_t)c * NT * V, E::narrow(o));
             }
