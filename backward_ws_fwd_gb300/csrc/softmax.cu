@@ -863,25 +863,20 @@ __global__ void __launch_bounds__(NT)
 // as on the cluster path, and the second pass reads the slice again and
 // writes y (dx).  Only the clusters' rows in flight (tens of MB) are read
 // between the passes, so the second read is served by L2; x (y, dy) is read
-// from HBM once.  The forward prefetches its slice of the cluster's next row
-// into L2 (prefetch_slice); in the backward, prefetching y and dy measured
-// slower (twice the L2 footprint).  Elements outside the row (windowed edges, the tail of the
-// last slice) enter as −inf (forward) or 0 (backward).
-constexpr int kTwoPassNT = 256, kTwoPassCS = 8, kTwoPassU = 4;
-
-// Thread 0 prefetches into L2 this CTA's chunks [c0, c0 + SL) of a row (only
-// the 16-byte blocks that hold the row's own elements), so that the next
-// row's first pass reads from L2 while HBM keeps streaming.
-template <typename T, bool U>
-__device__ __forceinline__ void prefetch_slice(const T* row_start, int D, int c0, int SL) {
-    constexpr int V = Elt<T>::V;
-    const int off = win_off<T, U>(row_start);
-    const int nc = (off + D + V - 1) / V;
-    const int e = c0 + SL < nc ? c0 + SL : nc;
-    if (e > c0)
-        prefetch_l2_bulk(row_start - off + (int64_t)c0 * V, (uint32_t)(e - c0) * 16u,
-                         l2_evict_last());
-}
+// from HBM once.  Bulk L2 prefetches of the cluster's next row measured slower
+// once clusters were small and many (bf16 [1024, 524288]: 3957 GB/s with,
+// 5461 without; the backward's likewise, earlier).  Elements outside the row
+// (windowed edges, the tail of the last slice) enter as −inf (forward) or 0
+// (backward).
+constexpr int kTwoPassNT = 256, kTwoPassU = 4;
+// CTAs a cluster (a row's slices).  Measured at s4 (fp32 [2048, 262144]) and
+// bf16 [1024, 524288], forward GB/s: binary32 rows 3136 / 3972 / 4194 with
+// clusters of 16 / 8 / 4 (4 CTAs an SM), 16-bit rows 5046 / 5490 / 4785;
+// more resident clusters keep more loads in flight, fewer CTAs a cluster
+// make each exchange cheaper.  The backward (s4): 4745 / 5278 / 4309 with
+// clusters of 16 / 8 (two CTAs an SM) / 4 (three).
+template <typename T, bool Fwd>
+constexpr int kTwoPassCS = (Fwd && std::is_same<T, float>::value) ? 4 : 8;
 
 // The raw chunks c0 + b + u·NT (u < NU) of a row: the row's own 16-byte
 // blocks, zeros for chunks past the slice or the row.
@@ -918,7 +913,7 @@ __device__ __forceinline__ void widen_chunk(const Raw16& r, const Win<T, U>& w, 
 // first pass fetches the second pass's first batch (before the exchange),
 // and the last batch of the second pass the next row's first batch.
 template <typename T, bool U>
-__global__ void __launch_bounds__(kTwoPassNT, 3)
+__global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 : 3)
     softmax_fwd_cluster2(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
                          int64_t N, int D, int SL) {
     using E = Elt<T>;
@@ -946,7 +941,6 @@ __global__ void __launch_bounds__(kTwoPassNT, 3)
     for (int64_t row = cid; row < N; row += ncl) {
         const T* xr = x + row * ldx;
         const Win<T, U> win{win_off<T, U>(xr), D};
-        if (threadIdx.x == 0 && row + ncl < N) prefetch_slice<T, U>(xr + ncl * ldx, D, c0, SL);
         // pass 1: this thread's maximum m and Σ exp(x − m) (binary32 rows:
         // two compensated lanes in packed f32x2 arithmetic, added together at
         // the end)
@@ -1355,18 +1349,18 @@ static cudaError_t softmax_bwd_cluster_t(const T* y, int64_t ldy, const T* dy, i
 template <typename T, bool U>
 static cudaError_t softmax_fwd_cluster2_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
                                           int64_t D, int64_t Dc, cudaStream_t s) {
-    const int SL = (int)cdiv(Dc, kTwoPassCS);
-    return go_cluster<softmax_fwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS, 0, N, s, x, ldx, y, ldy,
-                                                  N, (int)D, SL);
+    const int SL = (int)cdiv(Dc, kTwoPassCS<T, true>);
+    return go_cluster<softmax_fwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS<T, true>, 0, N, s, x, ldx,
+                                                  y, ldy, N, (int)D, SL);
 }
 
 template <typename T, bool U>
 static cudaError_t softmax_bwd_cluster2_t(const T* y, int64_t ldy, const T* dy, int64_t lddy,
                                           T* dx, int64_t lddx, int64_t N, int64_t D, int64_t Dc,
                                           cudaStream_t s) {
-    const int SL = (int)cdiv(Dc, kTwoPassCS);
-    return go_cluster<softmax_bwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS, 0, N, s, y, ldy, dy,
-                                                  lddy, dx, lddx, N, (int)D, SL);
+    const int SL = (int)cdiv(Dc, kTwoPassCS<T, false>);
+    return go_cluster<softmax_bwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS<T, false>, 0, N, s, y, ldy,
+                                                  dy, lddy, dx, lddx, N, (int)D, SL);
 }
 
 constexpr int64_t kTwoPassMaxD = (int64_t)1 << 30;
