@@ -90,6 +90,13 @@ __device__ __forceinline__ Acc2 s_comb(Acc2 a, Acc2 b) {
 
 __device__ __forceinline__ float s_val(const Acc2& a) { return a.hi + a.lo; }
 
+// The sum of a packed pair's two lanes as a (plain) row sum.
+__device__ __forceinline__ Acc2 lanes_sum(uint64_t a) {
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    return Acc2{a0 + a1, 0.f};
+}
+
 // Reduce K sums over each aligned group of TPR threads: xor butterfly inside
 // a warp; for groups wider than a warp, lane 0 of each warp posts its sums to
 // `red` (K·NT/32 float2) and, after a barrier, every warp loads the group's
@@ -209,23 +216,34 @@ __device__ __forceinline__ void center_row(float (&f)[CPT][V], unsigned valid, f
 #pragma unroll
             for (int v = 0; v < V; v++) s_add<true>(s[0], f[c][v]);  // invalid chunks are zero
     } else {
-        float s1 = 0.f;
+        // even and odd columns in the two lanes of a packed pair
+        uint64_t a = 0ull;
 #pragma unroll
         for (int c = 0; c < CPT; c++)
 #pragma unroll
-            for (int v = 0; v < V; v += 2) {
-                s[0].hi += f[c][v];
-                s1 += f[c][v + 1];
-            }
-        s[0].hi += s1;
+            for (int v = 0; v < V; v += 2) a = f2_add(a, f2_pack(f[c][v], f[c][v + 1]));
+        float s0, s1;
+        f2_unpack(a, s0, s1);
+        s[0].hi = s0 + s1;
     }
     group_reduce<TPR, NT, 1, C>(s, red);
     const Mean m = mean_of(s[0], fd, inv_d);
+    if constexpr (C) {
 #pragma unroll
-    for (int c = 0; c < CPT; c++)
-        if (valid >> c & 1u)
+        for (int c = 0; c < CPT; c++)
+            if (valid >> c & 1u)
 #pragma unroll
-            for (int v = 0; v < V; v++) f[c][v] = (f[c][v] - m.mu0) - m.c;
+                for (int v = 0; v < V; v++) f[c][v] = (f[c][v] - m.mu0) - m.c;
+    } else {
+        const uint64_t mu2 = f2_pack(m.mu0, m.mu0), c2 = f2_pack(m.c, m.c);
+#pragma unroll
+        for (int c = 0; c < CPT; c++)
+            if (valid >> c & 1u)
+#pragma unroll
+                for (int v = 0; v < V; v += 2)
+                    f2_unpack(f2_sub(f2_sub(f2_pack(f[c][v], f[c][v + 1]), mu2), c2), f[c][v],
+                              f[c][v + 1]);
+    }
 }
 
 // Per-thread cp.async staging of one row at a time: chunk c of the thread is
@@ -470,39 +488,73 @@ __global__ void __launch_bounds__(NT, MINB)
         Acc2 sums[K];
 #pragma unroll
         for (int q = 0; q < K; q++) sums[q] = acc2_zero();
+        uint64_t a0 = 0ull, a1 = 0ull, a2 = 0ull;  // 16-bit rows: packed lanes
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
                 float gc[V], wc[V];
                 dy_of(c, gc);
                 w_of(c, wc);
+                if constexpr (C) {
 #pragma unroll
-                for (int v = 0; v < V; v++) {
-                    const float gg = gc[v] * wc[v];
-                    s_fma<C>(sums[0], f[c][v], f[c][v]);
-                    s_fma<C>(sums[1], gg, f[c][v]);
-                    if constexpr (LN) s_add<C>(sums[2], gg);
+                    for (int v = 0; v < V; v++) {
+                        const float gg = gc[v] * wc[v];
+                        s_fma<C>(sums[0], f[c][v], f[c][v]);
+                        s_fma<C>(sums[1], gg, f[c][v]);
+                        if constexpr (LN) s_add<C>(sums[2], gg);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < V / 2; h++) {
+                        const uint64_t d2 = f2_pack(f[c][2 * h], f[c][2 * h + 1]);
+                        const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
+                                                   f2_pack(wc[2 * h], wc[2 * h + 1]));
+                        a0 = f2_fma(d2, d2, a0);
+                        a1 = f2_fma(g2, d2, a1);
+                        if constexpr (LN) a2 = f2_add(a2, g2);
+                    }
                 }
             }
+        }
+        if constexpr (!C) {
+            sums[0] = lanes_sum(a0);
+            sums[1] = lanes_sum(a1);
+            if constexpr (LN) sums[LN ? 2 : 0] = lanes_sum(a2);
         }
         group_reduce<TPR, NT, K, C>(sums, red.take());
         const BwdStats st = bwd_stats<LN, C>(sums, inv_d, eps);
         if (row < rb) {
             const float r = st.r, rmg = st.r * st.mg, rmgx = st.r * st.mgx;
+            const uint64_t r2 = f2_pack(r, r), nrmgx2 = f2_pack(-rmgx, -rmgx),
+                           nrmg2 = f2_pack(-rmg, -rmg);
 #pragma unroll
             for (int c = 0; c < CPT; c++) {
                 if (valid >> c & 1u) {
                     float o[V], gc[V], wc[V];
                     dy_of(c, gc);
                     w_of(c, wc);
+                    // r·((g − mean g) − x̂·mean(g·x̂)); the LayerNorm form (three
+                    // accumulators a column) stays scalar: packed, it spills
+                    if constexpr (LN) {
 #pragma unroll
-                    for (int v = 0; v < V; v++) {
-                        const float xh = f[c][v] * r;
-                        const float gg = gc[v] * wc[v];
-                        // r·((g − mean g) − x̂·mean(g·x̂))
-                        o[v] = fmaf(-xh, rmgx, fmaf(gg, r, -rmg));
-                        aw[c][v] = fmaf(gc[v], xh, aw[c][v]);
-                        if constexpr (LN) ab[c][v] += gc[v];
+                        for (int v = 0; v < V; v++) {
+                            const float xh = f[c][v] * r;
+                            const float gg = gc[v] * wc[v];
+                            o[v] = fmaf(-xh, rmgx, fmaf(gg, r, -rmg));
+                            aw[c][v] = fmaf(gc[v], xh, aw[c][v]);
+                            ab[c][v] += gc[v];
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < V / 2; h++) {
+                            const uint64_t dy2 = f2_pack(gc[2 * h], gc[2 * h + 1]);
+                            const uint64_t xh = f2_mul(f2_pack(f[c][2 * h], f[c][2 * h + 1]), r2);
+                            const uint64_t gg = f2_mul(dy2, f2_pack(wc[2 * h], wc[2 * h + 1]));
+                            f2_unpack(f2_fma(xh, nrmgx2, f2_fma(gg, r2, nrmg2)), o[2 * h],
+                                      o[2 * h + 1]);
+                            f2_unpack(f2_fma(dy2, xh, f2_pack(aw[c][2 * h], aw[c][2 * h + 1])),
+                                      aw[c][2 * h], aw[c][2 * h + 1]);
+                        }
                     }
                     st_stream(dxrow + (int64_t)c * TPR * V, E::narrow(o));
                 }
@@ -779,13 +831,6 @@ __device__ __forceinline__ Acc2 sum_sq2(const float (&f)[CPT][V], unsigned valid
                 const uint64_t d = f2_pack(f[c][2 * q], f[c][2 * q + 1]);
                 a = f2_fma(d, d, a);
             }
-    float a0, a1;
-    f2_unpack(a, a0, a1);
-    return Acc2{a0 + a1, 0.f};
-}
-
-// The sum of a packed pair's two lanes as a (plain) row sum.
-__device__ __forceinline__ Acc2 lanes_sum(uint64_t a) {
     float a0, a1;
     f2_unpack(a, a0, a1);
     return Acc2{a0 + a1, 0.f};
