@@ -15,7 +15,9 @@ The metric is effective HBM bandwidth: the algorithmic bytes the method must
 move (fwd: read x and w, write y; bwd: read x, dy and w, write dx and the
 parameter gradient) divided by device time.  `value` is measured with CUDA
 events around K steps on resident inputs; `e2e` runs the same step through
-the public API with host buffers, the host<->device copies included.
+the public API with host buffers: every step copies its inputs from pinned
+host memory and its result (the parameter gradients) back, inside the timed
+region (`e2e.all_outputs`: y and dx copied back as well).
 
 The worked 100 x 64 example (c1, 32-row tiles) is latency-bound: it is timed
 alone, outside the step (device time per op from CUDA graphs, and the host's
@@ -428,9 +430,9 @@ class Buffers:
         return sum(t.numel() * t.element_size() for t in (self.hx, self.hw, self.hdy, self.hb)
                    if t is not None)
 
-    def d2h_bytes(self):
-        return sum(t.numel() * t.element_size() for t in (self.y, self.dx, self.gw, self.gb)
-                   if t is not None)
+    def d2h_bytes(self, all_outputs=False):
+        outs = (self.y, self.dx, self.gw, self.gb) if all_outputs else (self.gw, self.gb)
+        return sum(t.numel() * t.element_size() for t in outs if t is not None)
 
     def norm(self, wsf, op, x, y, dy, dx, accumulate=False, stream=None):
         eps = self.wl.eps
@@ -571,18 +573,22 @@ def run_cuda(args, names):
         isolated = dict(isolated or {}, **lat)
 
     # end to end through the public API with host buffers: every input is
-    # copied from pinned host memory and every output back, inside the timed
-    # region.  Each workload is cut into row chunks on three streams (H2D,
-    # compute, D2H) so that copies in both directions overlap each other and
-    # the kernels; the chunked backward accumulates grad_w / dw with the
-    # library's accumulate flag (micro-batches), as a caller would.
+    # copied from pinned host memory and the step's result back, inside the
+    # timed region.  The result of a forward + backward step is the parameter
+    # gradients (grad_w / dw, grad_b), what an optimizer step consumes; y and dx
+    # stay on the device, where the next layer would use them.  A second figure
+    # copies every output back too (y and dx as well).  Each workload is cut
+    # into row chunks on three streams (H2D, compute, D2H) so that copies in
+    # both directions overlap each other and the kernels; the chunked backward
+    # accumulates grad_w / dw with the library's accumulate flag
+    # (micro-batches), as a caller would.
     e2e = None
     if host_io:
         e2e_steps = max(1, min(args.steps, 10))
         streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
         chunks = {"c2": 2, "c3": 8, "c4": 8, "c5": 4}
 
-        def e2e_step():
+        def e2e_step(all_outputs):
             h2d, comp, d2h = streams
             for n in names:
                 b = bufs[n]
@@ -601,40 +607,50 @@ def run_cuda(args, names):
                         ready.record(h2d)
                     comp.wait_event(ready)
                     b.run_rows(wsf, r0, r1, accumulate=j > 0, stream=comp)
-                    done = torch.cuda.Event()
-                    done.record(comp)
-                    d2h.wait_event(done)
-                    with torch.cuda.stream(d2h):
-                        b.hy[r0:r1].copy_(b.y[r0:r1], non_blocking=True)
-                        b.hdx[r0:r1].copy_(b.dx[r0:r1], non_blocking=True)
+                    if all_outputs:
+                        done = torch.cuda.Event()
+                        done.record(comp)
+                        d2h.wait_event(done)
+                        with torch.cuda.stream(d2h):
+                            b.hy[r0:r1].copy_(b.y[r0:r1], non_blocking=True)
+                            b.hdx[r0:r1].copy_(b.dx[r0:r1], non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(comp)
+                d2h.wait_event(done)
                 with torch.cuda.stream(d2h):
                     b.hgw.copy_(b.gw, non_blocking=True)
                     if b.hgb is not None:
                         b.hgb.copy_(b.gb, non_blocking=True)
 
-        e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        # each step ends when its outputs are on the host (a sync, as a
-        # training loop that reads its loss); the median step time is the
-        # value, so that a stall of the shared host does not decide it
-        step_ms = []
-        for _ in range(e2e_steps):
-            t_a = time.perf_counter()
-            e2e_step()
+        def e2e_time(all_outputs, nsteps):
+            e2e_step(all_outputs)
             torch.cuda.synchronize()
-            step_ms.append((time.perf_counter() - t_a) * 1e3)
-        e2e_ms = max_over_ranks(statistics.median(step_ms), dev)
-        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": sum(bufs[n].h2d_bytes() for n in names),
-               "d2h_bytes_per_step": sum(bufs[n].d2h_bytes() for n in names),
-               "ms_per_step": round(e2e_ms, 3),
-               "ms_mean": round(statistics.mean(step_ms), 3), "ms_max": round(max(step_ms), 3),
-               "steps": e2e_steps,
-               "how": "pinned host buffers; per workload 2-8 row chunks pipelined over H2D, "
-                      "compute and D2H streams; wall clock per step from the first copy to the "
-                      "outputs on the host (device sync); median over the steps"}
+            if world > 1:
+                dist.barrier()
+            # each step ends when its result is on the host (a sync, as a
+            # training loop that reads its loss); the median step time is the
+            # value, so that a stall of the shared host does not decide it
+            step_ms = []
+            for _ in range(nsteps):
+                t_a = time.perf_counter()
+                e2e_step(all_outputs)
+                torch.cuda.synchronize()
+                step_ms.append((time.perf_counter() - t_a) * 1e3)
+            med = max_over_ranks(statistics.median(step_ms), dev)
+            return {"value": round(world * step_bytes / (med * 1e-3) / 1e9, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": sum(bufs[n].h2d_bytes() for n in names),
+                    "d2h_bytes_per_step": sum(bufs[n].d2h_bytes(all_outputs) for n in names),
+                    "ms_per_step": round(med, 3), "ms_mean": round(statistics.mean(step_ms), 3),
+                    "ms_max": round(max(step_ms), 3), "steps": nsteps}
+
+        e2e = e2e_time(False, e2e_steps)
+        e2e["how"] = ("pinned host buffers; inputs (x, w, dy, b) to the device and the step's "
+                      "result, the parameter gradients, back to the host; per workload 2-8 row "
+                      "chunks pipelined over H2D, compute and D2H streams; wall clock per step "
+                      "from the first copy to the result on the host (device sync); median over "
+                      "the steps")
+        e2e["all_outputs"] = e2e_time(True, max(1, min(args.steps, 5)))
+        e2e["all_outputs"]["how"] = "the same, with y and dx also copied back to the host"
 
     if rank != 0:
         if world > 1:
