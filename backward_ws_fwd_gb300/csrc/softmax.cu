@@ -890,6 +890,22 @@ __device__ __forceinline__ void load_batch(Raw16 (&r)[NU], const T* row_start, c
     }
 }
 
+// max(a, b, c) in one instruction (sm_100 and later; a NaN operand is
+// ignored as by fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Whether every chunk b + u·NT (u < NU) of a batch lies inside the slice and,
+// for aligned rows, inside the row: such a batch needs no per-chunk masking.
+template <typename T, bool U, int NU>
+__device__ __forceinline__ bool full_batch(const Win<T, U>& w, int c0, int b, int SL) {
+    const int last = b + (NU - 1) * kTwoPassNT;
+    return !U && last < SL && w.has(c0 + last);
+}
+
 // Chunk c of the slice (row chunk cc = c0 + c) widened, with −inf (Fwd) or 0
 // outside the slice and the row.
 template <typename T, bool U, bool Fwd>
@@ -956,13 +972,22 @@ __global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 
                 load_batch<T, U, UU>(nb, xr, win, c0, b + STEP, SL, keep);
             else
                 load_batch<T, U, UU>(nb, xr, win, c0, threadIdx.x, SL, last);
+            const bool full = full_batch<T, U, UU>(win, c0, b, SL);
+            // chunk u of the batch, widened (masked only when the batch is not full)
+            auto chunk = [&](int u, float (&f)[V]) {
+                if (full)
+                    E::widen(cur[u], f);
+                else
+                    widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+            };
             float mb = m;
 #pragma unroll
             for (int u = 0; u < UU; u++) {
                 float f[V];
-                widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+                chunk(u, f);
 #pragma unroll
-                for (int v = 0; v < V; v++) mb = fmaxf(mb, f[v]);
+                for (int v = 0; v + 1 < V; v += 2) mb = max3(mb, f[v], f[v + 1]);
+                if constexpr (V % 2) mb = fmaxf(mb, f[V - 1]);
             }
             if (mb == -INFINITY) continue;  // nothing finite yet
             if constexpr (kComp) {
@@ -978,7 +1003,7 @@ __global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 
 #pragma unroll
                 for (int u = 0; u < UU; u++) {
                     float f[V];
-                    widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+                    chunk(u, f);
 #pragma unroll
                     for (int q = 0; q < V / 2; q++) {
                         const uint64_t e = exp_diff_f32x2(f2_pack(f[2 * q], f[2 * q + 1]), nm2);
@@ -997,7 +1022,7 @@ __global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 
 #pragma unroll
                 for (int u = 0; u < UU; u++) {
                     float f[V];
-                    widen_chunk<T, U, true>(cur[u], win, b + u * NT, c0 + b + u * NT, SL, f);
+                    chunk(u, f);
 #pragma unroll
                     for (int v = 0; v < V; v++)
                         add_to<kComp>(s, exp2_approx(fmaf(f[v], kLog2e, -m * kLog2e)));
@@ -1068,12 +1093,16 @@ __global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 
                 load_batch<T, U, UU>(nb, xn, Win<T, U>{win_off<T, U>(xn), D}, c0, threadIdx.x, SL,
                                      keep);
             }
+            const bool full = full_batch<T, U, UU>(win, c0, b, SL);
 #pragma unroll
             for (int u = 0; u < UU; u++) {
                 const int c = b + u * NT, cc = c0 + c;
-                if (c < SL && win.has(cc)) {
+                if (full || (c < SL && win.has(cc))) {
                     float f[V], o[V];
-                    widen_chunk<T, U, true>(cur[u], win, c, cc, SL, f);
+                    if (full)
+                        E::widen(cur[u], f);
+                    else
+                        widen_chunk<T, U, true>(cur[u], win, c, cc, SL, f);
                     if constexpr (kComp) {
                         const uint64_t nM2 = f2_pack(-Mi.x, -Mi.x), inv2 = f2_pack(Mi.y, Mi.y);
 #pragma unroll
