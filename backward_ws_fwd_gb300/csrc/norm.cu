@@ -606,8 +606,9 @@ __global__ void __launch_bounds__(NT, MINB)
 // entries of all CS·NT/32 warps of the cluster in its own shared memory;
 // warp 0 combines them (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
 // butterfly over the lanes) and hands the sums to the other warps through
-// shared memory and a CTA barrier, so every CTA derives the same bits of the
-// row statistics, with the arithmetic of the row path.
+// shared memory and a CTA barrier (RMSNorm's backward: every warp combines
+// them itself, without the barrier), so every CTA derives the same bits of
+// the row statistics, with the arithmetic of the row path.
 //
 // RMSNorm keeps two rows in flight: the sums of row k + 1 are pushed before
 // the exchange of row k is awaited, so the exchange's latency overlaps the
@@ -726,6 +727,42 @@ __device__ __forceinline__ void cluster_finish(unsigned t, Acc2 (&v)[K], NormPus
         v[2 * n] = Acc2{r.x, r.y};
         if (2 * n + 1 < K) v[2 * n + 1 < K ? 2 * n + 1 : 0] = Acc2{r.z, r.w};
     }
+}
+
+// cluster_finish without the CTA barrier: every warp waits for turn t and
+// combines the entries itself, in the same order, so every warp of every CTA
+// derives the same bits.  The __syncwarp orders the warp's reads of the
+// turn's buffer before its later pushes, whose release lets the other CTAs
+// write that buffer again.  For callers that push turn t + 1 before reading
+// turn t and turn t + 2 after it (NB = 4): a CTA writes a buffer again, turn
+// t + 4, only after every warp of the cluster pushed turn t + 2.
+template <int NT, int K, unsigned CM, int NB, int NV>
+__device__ __forceinline__ void cluster_combine(unsigned t, Acc2 (&v)[K],
+                                                NormPush<NT, NB, NV>& xp) {
+    static_assert(NB == 4, "two turns outstanding");
+    constexpr int W = NT / 32, NX = (K + 1) / 2;
+    const int lane = threadIdx.x & 31;
+    const float4(*buf)[NV] = xp.wait(t);
+    const int total = (int)cluster_nctarank() * W;
+#pragma unroll
+    for (int q = 0; q < K; q++) v[q] = acc2_zero();
+    for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
+#pragma unroll
+        for (int n = 0; n < NX; n++) {
+            const float4 en = buf[j][n];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int q = 2 * n + h;
+                if (q < K) {
+                    const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
+                    v[q] = ((CM >> q) & 1u) ? acc2_add(v[q], o) : Acc2{v[q].hi + o.hi, 0.f};
+                }
+            }
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CM >> q) & 1u);
 }
 
 template <int NT, int K, unsigned CM, unsigned CMW = CM, int NB, int NV>
@@ -893,9 +930,11 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         cp_async_wait<S - 3>();  // rows k and k + 1
         if (k + S - 1 < iters) stage_row<NT, CPT, NT>(xs + ((k + S - 1) % S) * CPT * NT, stg, valid);
         cp_async_commit();
+        // LayerNorm centres the row before its sums; RMSNorm loads it after
+        // its turn (fewer registers live across the exchange)
         float f[CPT][V];
-        load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
         if constexpr (LN) {
+            load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
             if constexpr (C)
                 center<CPT, V>(f, valid, mn);
             else
@@ -927,6 +966,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
             cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u, C ? 3u : 0u>(sm, xc, xres);
         } else {
             cluster_finish<NT, 1, C ? 1u : 0u>((unsigned)k, sm, xc, xres);  // row k's turn
+            load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
         }
         const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
         if constexpr (LN) mn = mean_of(sm[LN ? 1 : 0], fd, inv_d);
@@ -1159,7 +1199,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 rms_sums((int)((k + 1) % S), q);
                 cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
             }
-            cluster_finish<NT, K, CM>((unsigned)k, sums, xc, xres);  // row k's turn
+            cluster_combine<NT, K, CM>((unsigned)k, sums, xc);  // row k's turn, in every warp
         } else {
 #pragma unroll
             for (int q = 0; q < K; q++) sums[q] = acc2_zero();

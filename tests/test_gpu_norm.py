@@ -210,6 +210,19 @@ def test_norm_cluster_offset_outliers_strides(wsf, dt):
         _check(layer, x, w, dy, b, *_run(wsf, layer, x, w, dy, b, pad=8))
 
 
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("D", [12288, 20000, 36872])
+def test_norm_cluster_block_means(wsf, dt, D):
+    # blocks of 512 columns (one warp's share of a 16-bit row) with means far
+    # apart, a common offset and a ragged last CTA: the per-warp shifts of
+    # LayerNorm's exchange differ widely from the row mean
+    x, w, dy, b = _inputs(24, D, dt, seed=D % 89)
+    cols = torch.arange(D)
+    x = (x.double() + 20.0 * ((cols // 512) % 7 - 3).double() + 40.0).to(x.dtype)
+    x[5] = x[5, 0]  # a constant row
+    _check(True, x, w, dy, b, *_run(wsf, True, x, w, dy, b))
+
+
 @pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
 def test_norm_cluster_accumulate_reproducible(wsf, layer):
     D = 20000
