@@ -614,18 +614,27 @@ __global__ void __launch_bounds__(NT, MINB)
 // the exchange of row k is awaited, so the exchange's latency overlaps the
 // next row's first pass (two turns outstanding: four exchange buffers).
 //
-// One exchange a row.  LayerNorm needs Σx before the sums over d = x − μ;
-// its Σx travels one row ahead: the exchange of row k carries the sums of
-// row k and Σx of row k + 1 (staged already), so that the mean of row k + 1
-// is known when its turn comes, and only the first row's Σx is exchanged on
-// its own.  Σx is compensated across warps for every storage type: the
-// plain binary32 row sum that suffices for 16-bit rows of the row path is
-// exact only while Σx stays below 2^24 steps of the data's grid, i.e. up to
-// 2^24/2^11 = 8192 binary16 elements of one binade (2^24/2^8 = 65536 for
-// bfloat16), and wider binary16 rows with a large common offset would shift
-// every x̂ of a row by the rounding of their mean.  A warp's 512 16-bit
-// elements stay below 2^20 steps, so within a warp they are added plainly
-// (see staged_sum_x), as on the row path.
+// One exchange a row.  LayerNorm's sums about the mean would need the mean
+// first; it takes them about a shift s instead, the previous row's mean
+// (zero for a cluster's first row, or after a row whose mean is not
+// finite): d = x − s, and the row's turn carries Σ d², Σ x[, Σ g, Σ g·d].
+// The mean μ₀ + c comes from Σ x as on the row path (Σ x compensated across
+// warps for every storage type: the plain binary32 row sum that suffices for
+// 16-bit rows of the row path is exact only while Σx stays below 2^24 steps
+// of the data's grid, i.e. up to 2^24/2^11 = 8192 binary16 elements of one
+// binade, 2^24/2^8 = 65536 for bfloat16, and wider binary16 rows with a large
+// common offset would shift every x̂ of a row by the rounding of their mean;
+// a warp's 512 16-bit elements stay below 2^20 steps, so within a warp they
+// are added plainly).  With m = μ − s,
+//     Σ (x − μ)² = Σ d² − D·m²,    Σ g·(x − μ) = Σ g·d − m·Σ g
+// (exact identities), and the row is centred on μ₀ + c.  The turn of row
+// k + 1 is pushed as soon as row k's is read, before row k's second pass,
+// which its exchange then overlaps (one turn outstanding: two buffers).
+// When the shift is far from the mean the first identity cancels: if D·m² >
+// Σ d²/2 (more than one bit lost; also a NaN) the row's sums are taken again
+// about μ in a turn of their own — every CTA sees the same sums, so every
+// CTA takes the same turns.  Rows whose mean drifts by less than their
+// spread from one row to the next never take it.
 //
 // The forward takes rows cid, cid + ncl, … (cluster cid of ncl).  The
 // backward keeps the row tiles of the row path (a function of N alone, so
@@ -651,82 +660,107 @@ constexpr int64_t kNormClusterRowMax = (int64_t)kClusterMaxCS * kNormClusterNT *
 // the exchange protocol failed.
 __device__ unsigned g_norm_wait_timeouts;
 
+// Most CTAs a cluster of CTAs of NT threads takes: 128-thread CTAs serve rows
+// of up to kNormClusterSmallMaxD elements (8 CTAs of 2048 elements).
+template <int NT>
+constexpr int kNormMaxCS = NT == 128 ? 8 : kClusterMaxCS;
+
 template <int NT, int NB = 2, int NV = 2>
-using NormPush = WarpPush<NT / 32, kClusterMaxCS*(NT / 32), NV, NB>;
+using NormPush = WarpPush<NT / 32, kNormMaxCS<NT>*(NT / 32), NV, NB>;
 
 __device__ __forceinline__ Acc2 warp_sum(Acc2 v, bool comp) {
     return comp ? group_sum2<32>(v) : Acc2{group_sum<32>(v.hi), 0.f};
+}
+
+// An entry carries K sums as float4s: as (hi, lo) pairs, two to a float4,
+// or, when no sum is compensated (CM = 0, so every lo is zero), as values,
+// four to a float4.
+template <int K, unsigned CM>
+constexpr int kEntryX = CM == 0 ? (K + 3) / 4 : (K + 1) / 2;
+
+template <int K, unsigned CM>
+__device__ __forceinline__ void entry_put(float4* e, const Acc2 (&v)[K]) {
+    float f[4 * kEntryX<K, CM>];
+#pragma unroll
+    for (int i = 0; i < 4 * kEntryX<K, CM>; i++) f[i] = 0.f;
+#pragma unroll
+    for (int q = 0; q < K; q++) {
+        if constexpr (CM == 0) {
+            f[q] = v[q].hi;
+        } else {
+            f[2 * q] = v[q].hi;
+            f[2 * q + 1] = v[q].lo;
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < kEntryX<K, CM>; n++)
+        e[n] = make_float4(f[4 * n], f[4 * n + 1], f[4 * n + 2], f[4 * n + 3]);
+}
+
+template <unsigned CM>
+__device__ __forceinline__ Acc2 entry_get(const float4* e, int q) {
+    if constexpr (CM == 0) {
+        const float4 v = e[q / 4];
+        const int h = q % 4;
+        return Acc2{h == 0 ? v.x : h == 1 ? v.y : h == 2 ? v.z : v.w, 0.f};
+    } else {
+        const float4 v = e[q / 2];
+        return (q & 1) ? Acc2{v.z, v.w} : Acc2{v.x, v.y};
+    }
+}
+
+// Add the K sums of one entry into s (compensated for the sums in CM).
+template <int K, unsigned CM>
+__device__ __forceinline__ void entry_add(Acc2 (&s)[K], const float4* e) {
+#pragma unroll
+    for (int q = 0; q < K; q++) {
+        const Acc2 o = entry_get<CM>(e, q);
+        s[q] = ((CM >> q) & 1u) ? acc2_add(s[q], o) : Acc2{s[q].hi + o.hi, 0.f};
+    }
 }
 
 // Sum K (up to 4) row sums over the cluster in two steps.  cluster_push: each
 // warp's sums (xor butterfly; compensated for the sums in CMW) pushed as the
 // warp's entry; returns the turn.  cluster_finish: warp 0 waits for the turn,
 // combines the entries (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
-// butterfly; compensated for the sums in CM) and posts the sums in `res`; a
-// CTA barrier hands them to every warp (and orders the turn's reads before
-// any warp's later pushes).  Every thread of every CTA of the cluster calls
-// both together; other work may sit between them (another turn's push when
-// NB = 4).
+// butterfly; compensated for the sums in CM) and posts the sums in `out`
+// (one of two slots, taken in turn by successive calls, so that a slot is
+// written again only after the CTA barrier of the call in between); a CTA
+// barrier hands them to every warp (and orders the turn's reads before any
+// warp's later pushes).  Every thread of every CTA of the cluster calls
+// both together; other work may sit between them (other turns' pushes when
+// NB is 4 or more).
 template <int NT, int K, unsigned CM, unsigned CMW, int NB, int NV>
 __device__ __forceinline__ unsigned cluster_push(Acc2 (&v)[K], NormPush<NT, NB, NV>& xp) {
     static_assert(K >= 1 && K <= 4, "up to four sums");
     static_assert((CMW & ~CM) == 0, "warp-level compensation implies exchange-level");
-    constexpr int NX = (K + 1) / 2;
     Acc2 w[K];
 #pragma unroll
     for (int q = 0; q < K; q++) w[q] = warp_sum(v[q], (CMW >> q) & 1u);
-    float4 e[NX];
-#pragma unroll
-    for (int n = 0; n < NX; n++) {
-        const Acc2 a = w[2 * n], b = 2 * n + 1 < K ? w[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
-        e[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
-    }
-    return xp.template push<NX>(e);
+    float4 e[kEntryX<K, CM>];
+    entry_put<K, CM>(e, w);
+    return xp.template push<kEntryX<K, CM>>(e);
 }
 
 template <int NT, int K, unsigned CM, int NB, int NV>
 __device__ __forceinline__ void cluster_finish(unsigned t, Acc2 (&v)[K], NormPush<NT, NB, NV>& xp,
-                                               float4 (*res)[2]) {
-    constexpr int W = NT / 32, NX = (K + 1) / 2;
+                                               float4* out) {
+    constexpr int W = NT / 32;
     const int lane = threadIdx.x & 31;
-    float4* out = res[t & 1u];
     if (threadIdx.x < 32) {
         const float4(*buf)[NV] = xp.wait(t);
         const int total = (int)cluster_nctarank() * W;
         Acc2 s[K];
 #pragma unroll
         for (int q = 0; q < K; q++) s[q] = acc2_zero();
-        for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
-#pragma unroll
-            for (int n = 0; n < NX; n++) {
-                const float4 en = buf[j][n];
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int q = 2 * n + h;
-                    if (q < K) {
-                        const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
-                        s[q] = ((CM >> q) & 1u) ? acc2_add(s[q], o) : Acc2{s[q].hi + o.hi, 0.f};
-                    }
-                }
-            }
-        }
+        for (int j = lane; j < total; j += 32) entry_add<K, CM>(s, buf[j]);  // bound uniform
 #pragma unroll
         for (int q = 0; q < K; q++) s[q] = warp_sum(s[q], (CM >> q) & 1u);
-        if (lane == 0)
-#pragma unroll
-            for (int n = 0; n < NX; n++) {
-                const Acc2 a = s[2 * n],
-                           b = 2 * n + 1 < K ? s[2 * n + 1 < K ? 2 * n + 1 : 0] : acc2_zero();
-                out[n] = make_float4(a.hi, a.lo, b.hi, b.lo);
-            }
+        if (lane == 0) entry_put<K, CM>(out, s);
     }
     __syncthreads();
 #pragma unroll
-    for (int n = 0; n < NX; n++) {
-        const float4 r = out[n];
-        v[2 * n] = Acc2{r.x, r.y};
-        if (2 * n + 1 < K) v[2 * n + 1 < K ? 2 * n + 1 : 0] = Acc2{r.z, r.w};
-    }
+    for (int q = 0; q < K; q++) v[q] = entry_get<CM>(out, q);
 }
 
 // cluster_finish without the CTA barrier: every warp waits for turn t and
@@ -740,26 +774,13 @@ template <int NT, int K, unsigned CM, int NB, int NV>
 __device__ __forceinline__ void cluster_combine(unsigned t, Acc2 (&v)[K],
                                                 NormPush<NT, NB, NV>& xp) {
     static_assert(NB == 4, "two turns outstanding");
-    constexpr int W = NT / 32, NX = (K + 1) / 2;
+    constexpr int W = NT / 32;
     const int lane = threadIdx.x & 31;
     const float4(*buf)[NV] = xp.wait(t);
     const int total = (int)cluster_nctarank() * W;
 #pragma unroll
     for (int q = 0; q < K; q++) v[q] = acc2_zero();
-    for (int j = lane; j < total; j += 32) {  // bound uniform across the warp
-#pragma unroll
-        for (int n = 0; n < NX; n++) {
-            const float4 en = buf[j][n];
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const int q = 2 * n + h;
-                if (q < K) {
-                    const Acc2 o = h ? Acc2{en.z, en.w} : Acc2{en.x, en.y};
-                    v[q] = ((CM >> q) & 1u) ? acc2_add(v[q], o) : Acc2{v[q].hi + o.hi, 0.f};
-                }
-            }
-        }
-    }
+    for (int j = lane; j < total; j += 32) entry_add<K, CM>(v, buf[j]);  // bound uniform
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < K; q++) v[q] = warp_sum(v[q], (CM >> q) & 1u);
@@ -767,9 +788,9 @@ __device__ __forceinline__ void cluster_combine(unsigned t, Acc2 (&v)[K],
 
 template <int NT, int K, unsigned CM, unsigned CMW = CM, int NB, int NV>
 __device__ __forceinline__ void cluster_reduce(Acc2 (&v)[K], NormPush<NT, NB, NV>& xp,
-                                               float4 (*res)[2]) {
+                                               float4* out) {
     const unsigned t = cluster_push<NT, K, CM, CMW, NB, NV>(v, xp);
-    cluster_finish<NT, K, CM, NB, NV>(t, v, xp, res);
+    cluster_finish<NT, K, CM, NB, NV>(t, v, xp, out);
 }
 
 // Σx over this thread's valid chunks of a staged row: binary32 elements with
@@ -873,6 +894,13 @@ __device__ __forceinline__ Acc2 sum_sq2(const float (&f)[CPT][V], unsigned valid
     return Acc2{a0 + a1, 0.f};
 }
 
+// Whether sums about a shift give Σ (x − μ)² = Σ d² − D·m² (m = μ − s) to
+// within one bit of cancellation: D·m² ≤ Σ d² / 2.  Otherwise the row's
+// sums are taken again about μ.  False for NaN sums.
+__device__ __forceinline__ bool shift_ok(float sdd, float m, float fd) {
+    return fd * m * m <= 0.5f * sdd;
+}
+
 template <typename T, bool LN, int NT, int S>
 __global__ void __launch_bounds__(NT, 768 / NT)
     norm_fwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
@@ -888,8 +916,8 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     static_assert(S >= 3, "two staged rows");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
-    constexpr int NV = LN ? 2 : 1;  // float4 an entry
-    __shared__ __align__(16) float4 xbuf[NB][kClusterMaxCS * (NT / 32)][NV];
+    constexpr int NV = 1;  // one float4 an entry: up to two sums
+    __shared__ __align__(16) float4 xbuf[NB][kNormMaxCS<NT> * (NT / 32)][NV];
     __shared__ __align__(8) uint64_t xbar[NB];
     __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
     NormPush<NT, NB, NV> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
@@ -918,7 +946,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     if (LN && iters > 0) {  // the first row's Σx
         cp_async_wait<S - 2>();
         Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
+        cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres[0]);
         mn = mean_of(s0[0], fd, inv_d);
     }
     if (PIPE && iters > 0) {  // the first row's Σx², turn 0
@@ -963,9 +991,9 @@ __global__ void __launch_bounds__(NT, 768 / NT)
             sm[LN ? 1 : 0] = k + 1 < iters
                 ? staged_sum_x<E, CPT, NT, V, C>(xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid)
                 : acc2_zero();
-            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u, C ? 3u : 0u>(sm, xc, xres);
+            cluster_reduce<NT, 2, (C ? 1u : 0u) | 2u, C ? 3u : 0u>(sm, xc, xres[(k + 1) & 1]);
         } else {
-            cluster_finish<NT, 1, C ? 1u : 0u>((unsigned)k, sm, xc, xres);  // row k's turn
+            cluster_finish<NT, 1, C ? 1u : 0u>((unsigned)k, sm, xc, xres[k & 1]);  // row k's turn
             load_row<E, CPT, NT, V>(xs + (k % S) * CPT * NT + threadIdx.x, valid, f);
         }
         const float r = rstd_of<C>(s_val(sm[0]), inv_d, eps);
@@ -1015,8 +1043,10 @@ __device__ __forceinline__ void tile_advance(TileCursor& c, int step, int P, int
     }
 }
 
+// binary32 rows: at most four CTAs an SM fit their staged rows, so their
+// threads may hold more registers
 template <typename T, bool LN, int NT, int S, bool WS>
-__global__ void __launch_bounds__(NT, 768 / NT)
+__global__ void __launch_bounds__(NT, (std::is_same<T, float>::value ? 512 : 768) / NT)
     norm_bwd_cluster(const T* __restrict__ x, int64_t ldx, const float* __restrict__ w,
                      const T* __restrict__ dy, int64_t lddy, float eps, T* __restrict__ dx,
                      int64_t lddx, float* __restrict__ part, int64_t N, int Dv, int64_t P) {
@@ -1024,18 +1054,23 @@ __global__ void __launch_bounds__(NT, 768 / NT)
     constexpr int V = E::V, CPT = 16 / V;
     constexpr bool C = std::is_same<T, float>::value;
     static_assert(S >= 3, "two staged rows");
-    // sums: Σ d², Σ g·d[, Σ g, Σx of the next row]
+    // sums: Σ d², Σ g·d[, Σ g, Σ x], d = x (RMSNorm) or x − s (LayerNorm,
+    // about a shift s); Σ x is compensated across warps for every type
     constexpr int K = LN ? 4 : 2;
     constexpr unsigned CM = (C ? (LN ? 7u : 3u) : 0u) | (LN ? 8u : 0u);
-    // RMSNorm keeps two rows in flight: row k + 1's sums are pushed before
-    // row k's exchange is awaited (four exchange buffers, see WarpPush)
-    constexpr bool PIPE = !LN;
-    constexpr int NB = PIPE ? 4 : 2, NV = LN ? 2 : 1;
+    // Two rows in flight.  RMSNorm pushes row k + 1's sums before awaiting
+    // row k's exchange (four exchange buffers, see WarpPush).  LayerNorm
+    // takes its sums about a shift, the previous row's mean, and pushes row
+    // k + 1's sums once row k's turn is read, before row k's second pass,
+    // which its exchange overlaps (one turn outstanding: two buffers); when
+    // the shift is far from the row's mean, the sums are taken again about
+    // the mean in a turn of their own.
+    constexpr int NB = LN ? 2 : 4, NV = kEntryX<K, CM>;
     const int64_t D = (int64_t)Dv * V;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* xs = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
     Raw16* gs = xs + S * CPT * NT;                    // [S][CPT][NT]
-    __shared__ __align__(16) float4 xbuf[NB][kClusterMaxCS * (NT / 32)][NV];
+    __shared__ __align__(16) float4 xbuf[NB][kNormMaxCS<NT> * (NT / 32)][NV];
     __shared__ __align__(8) uint64_t xbar[NB];
     __shared__ __align__(16) float4 xres[2][2];  // combined sums, by turn parity
     NormPush<NT, NB, NV> xc{xbuf, xbar, &g_norm_wait_timeouts, 0u, true};
@@ -1118,13 +1153,15 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         stage(k);
         cp_async_commit();
     }
-    // RMSNorm's sums of the staged row in `slot`: Σ x², Σ g·x, g = dy·w
-    auto rms_sums = [&](int slot, Acc2 (&q)[K]) {
+    // row sums of the staged row in `slot` (g = dy·w): Σ d², Σ g·d[, Σ g,
+    // Σ x], d = x (RMSNorm) or x − sh (LayerNorm)
+    auto row_sums = [&](int slot, float sh, Acc2 (&q)[K]) {
         const Raw16* px = xs + slot * CPT * NT + threadIdx.x;
         const Raw16* pg = gs + slot * CPT * NT + threadIdx.x;
 #pragma unroll
         for (int n = 0; n < K; n++) q[n] = acc2_zero();
-        uint64_t a0 = 0ull, a1 = 0ull;  // 16-bit rows: packed lanes of Σ x², Σ g·x
+        uint64_t a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;  // 16-bit rows: packed lanes
+        const uint64_t sh2 = f2_pack(sh, sh);
 #pragma unroll
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
@@ -1135,17 +1172,28 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 if constexpr (C) {
 #pragma unroll
                     for (int v = 0; v < V; v++) {
-                        s_fma<C>(q[0], dc[v], dc[v]);
-                        s_fma<C>(q[1], gc[v] * wc[v], dc[v]);
+                        const float d = LN ? dc[v] - sh : dc[v];
+                        const float gg = gc[v] * wc[v];
+                        s_fma<C>(q[0], d, d);
+                        s_fma<C>(q[1], gg, d);
+                        if constexpr (LN) {
+                            s_add<C>(q[LN ? 2 : 0], gg);
+                            s_add<C>(q[LN ? 3 : 0], dc[v]);  // Σ x
+                        }
                     }
                 } else {
 #pragma unroll
                     for (int h = 0; h < V / 2; h++) {
-                        const uint64_t d2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
+                        const uint64_t x2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
+                        const uint64_t d2 = LN ? f2_sub(x2, sh2) : x2;
                         const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
                                                    f2_pack(wc[2 * h], wc[2 * h + 1]));
                         a0 = f2_fma(d2, d2, a0);
                         a1 = f2_fma(g2, d2, a1);
+                        if constexpr (LN) {
+                            a2 = f2_add(a2, g2);
+                            a3 = f2_add(a3, x2);
+                        }
                     }
                 }
             }
@@ -1153,20 +1201,20 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         if constexpr (!C) {
             q[0] = lanes_sum(a0);
             q[1] = lanes_sum(a1);
+            if constexpr (LN) {
+                q[LN ? 2 : 0] = lanes_sum(a2);
+                q[LN ? 3 : 0] = lanes_sum(a3);
+            }
         }
     };
-    Mean mn{0.f, 0.f};
-    if (LN && iters > 0) {  // the first row's Σx
-        cp_async_wait<S - 2>();
-        Acc2 s0[1] = {staged_sum_x<E, CPT, NT, V, C>(xs + threadIdx.x, valid)};
-        cluster_reduce<NT, 1, 1u, C ? 1u : 0u>(s0, xc, xres);
-        mn = mean_of(s0[0], fd, inv_d);
-    }
-    if (PIPE && iters > 0) {  // the first row's sums, turn 0
+    // LayerNorm: the shift of row k and the turn of row k
+    float s_cur = 0.f;
+    unsigned t_cur = 0u;
+    if (iters > 0) {  // the first row's sums
         cp_async_wait<S - 2>();
         Acc2 q[K];
-        rms_sums(0, q);
-        cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
+        row_sums(0, 0.f, q);
+        t_cur = cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
     }
     for (int64_t k = 0; k < iters; k++) {
         cp_async_wait<S - 3>();  // rows k and k + 1
@@ -1175,16 +1223,22 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         const int64_t row = cw.row;
         const Raw16* cx = xs + (k % S) * CPT * NT + threadIdx.x;
         const Raw16* cg = gs + (k % S) * CPT * NT + threadIdx.x;
-        // d of chunk c (x, or x − μ), widened from the staged slot in each
-        // pass rather than held across the exchange
-        const uint64_t mu2 = f2_pack(mn.mu0, mn.mu0), mc2 = f2_pack(mn.c, mn.c);
-        auto d_of = [&](int c, float (&o)[V]) {
+        auto push_next = [&](float sh) {  // row k + 1's sums
+            Acc2 q[K];
+            row_sums((int)((k + 1) % S), sh, q);
+            return cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
+        };
+        if (!LN && k + 1 < iters) push_next(0.f);
+        // d of chunk c (x, or x − μ with μ = μ₀ + c), widened from the staged
+        // slot in each pass rather than held across the exchange
+        auto d_of = [&](int c, const Mean& m, float (&o)[V]) {
             E::widen(cx[c * NT], o);
             if constexpr (LN) {
                 if constexpr (C) {
 #pragma unroll
-                    for (int v = 0; v < V; v++) o[v] = (o[v] - mn.mu0) - mn.c;
+                    for (int v = 0; v < V; v++) o[v] = (o[v] - m.mu0) - m.c;
                 } else {
+                    const uint64_t mu2 = f2_pack(m.mu0, m.mu0), mc2 = f2_pack(m.c, m.c);
 #pragma unroll
                     for (int h = 0; h < V / 2; h++)
                         f2_unpack(f2_sub(f2_sub(f2_pack(o[2 * h], o[2 * h + 1]), mu2), mc2),
@@ -1192,60 +1246,67 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 }
             }
         };
+        // row k's turn: Σ (x − μ)², Σ g·(x − μ)[, Σ g]
         Acc2 sums[K];
-        if constexpr (PIPE) {
-            if (k + 1 < iters) {  // row k + 1's sums, turn k + 1
-                Acc2 q[K];
-                rms_sums((int)((k + 1) % S), q);
-                cluster_push<NT, K, CM, C ? CM : 0u>(q, xc);
-            }
-            cluster_combine<NT, K, CM>((unsigned)k, sums, xc);  // row k's turn, in every warp
-        } else {
+        Mean mn{0.f, 0.f};
+        float ss, sgd, sg = 0.f;
+        if constexpr (LN) {
+            cluster_finish<NT, K, CM>(t_cur, sums, xc, xres[t_cur & 1u]);
+            const float sdd = s_val(sums[0]);
+            mn = mean_of(sums[LN ? 3 : 0], fd, inv_d);
+            const float m = (mn.mu0 - s_cur) + mn.c;  // μ − s
+            sg = s_val(sums[LN ? 2 : 0]);
+            ss = sdd - fd * m * m;
+            sgd = s_val(sums[1]) - m * sg;
+            if (!shift_ok(sdd, m, fd)) {  // the same in every thread of the cluster
+                Acc2 q[2] = {acc2_zero(), acc2_zero()};
+                uint64_t a0 = 0ull, a1 = 0ull;
 #pragma unroll
-            for (int q = 0; q < K; q++) sums[q] = acc2_zero();
-            uint64_t a0 = 0ull, a1 = 0ull, a2 = 0ull;  // 16-bit rows: packed lanes
+                for (int c = 0; c < CPT; c++) {
+                    if (valid >> c & 1u) {
+                        float dc[V], gc[V], wc[V];
+                        d_of(c, mn, dc);
+                        E::widen(cg[c * NT], gc);
+                        w_of(c, wc);
+                        if constexpr (C) {
 #pragma unroll
-            for (int c = 0; c < CPT; c++) {
-                if (valid >> c & 1u) {
-                    float dc[V], gc[V], wc[V];
-                    d_of(c, dc);
-                    E::widen(cg[c * NT], gc);
-                    w_of(c, wc);
-                    if constexpr (C) {
+                            for (int v = 0; v < V; v++) {
+                                s_fma<C>(q[0], dc[v], dc[v]);
+                                s_fma<C>(q[1], gc[v] * wc[v], dc[v]);
+                            }
+                        } else {
 #pragma unroll
-                        for (int v = 0; v < V; v++) {
-                            const float gg = gc[v] * wc[v];
-                            s_fma<C>(sums[0], dc[v], dc[v]);
-                            s_fma<C>(sums[1], gg, dc[v]);
-                            if constexpr (LN) s_add<C>(sums[LN ? 2 : 0], gg);
-                        }
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < V / 2; h++) {
-                            const uint64_t d2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
-                            const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
-                                                       f2_pack(wc[2 * h], wc[2 * h + 1]));
-                            a0 = f2_fma(d2, d2, a0);
-                            a1 = f2_fma(g2, d2, a1);
-                            if constexpr (LN) a2 = f2_add(a2, g2);
+                            for (int h = 0; h < V / 2; h++) {
+                                const uint64_t d2 = f2_pack(dc[2 * h], dc[2 * h + 1]);
+                                const uint64_t g2 = f2_mul(f2_pack(gc[2 * h], gc[2 * h + 1]),
+                                                           f2_pack(wc[2 * h], wc[2 * h + 1]));
+                                a0 = f2_fma(d2, d2, a0);
+                                a1 = f2_fma(g2, d2, a1);
+                            }
                         }
                     }
                 }
+                if constexpr (!C) {
+                    q[0] = lanes_sum(a0);
+                    q[1] = lanes_sum(a1);
+                }
+                cluster_reduce<NT, 2, C ? 3u : 0u, C ? 3u : 0u>(q, xc, xres[(t_cur + 1u) & 1u]);
+                ss = s_val(q[0]);
+                sgd = s_val(q[1]);
             }
-            if constexpr (!C) {
-                sums[0] = lanes_sum(a0);
-                sums[1] = lanes_sum(a1);
-                if constexpr (LN) sums[LN ? 2 : 0] = lanes_sum(a2);
+            if (k + 1 < iters) {  // row k + 1's sums, about this row's mean
+                s_cur = mn.mu0 + mn.c;
+                if (!isfinite(s_cur)) s_cur = 0.f;  // a row with a NaN or ∞ shifts no other
+                t_cur = push_next(s_cur);
             }
-            if constexpr (LN)
-                if (k + 1 < iters)
-                    sums[LN ? 3 : 0] = staged_sum_x<E, CPT, NT, V, C>(
-                        xs + ((k + 1) % S) * CPT * NT + threadIdx.x, valid);
-            cluster_reduce<NT, K, CM, C ? CM : 0u>(sums, xc, xres);
+        } else {
+            cluster_combine<NT, K, CM>((unsigned)k, sums, xc);  // row k's turn, in every warp
+            ss = s_val(sums[0]);
+            sgd = s_val(sums[1]);
         }
-        const float r = rstd_of<C>(s_val(sums[0]), inv_d, eps);
-        const float rmgx = r * (r * (s_val(sums[1]) * inv_d));
-        const float rmg = LN ? r * (s_val(sums[LN ? 2 : 0]) * inv_d) : 0.f;
+        const float r = rstd_of<C>(ss, inv_d, eps);
+        const float rmgx = r * (r * (sgd * inv_d));
+        const float rmg = LN ? r * (sg * inv_d) : 0.f;
         T* dxrow = dx + row * lddx + (int64_t)l * V;
         const uint64_t r2 = f2_pack(r, r), nrmgx2 = f2_pack(-rmgx, -rmgx),
                        nrmg2 = f2_pack(-rmg, -rmg);
@@ -1253,7 +1314,7 @@ __global__ void __launch_bounds__(NT, 768 / NT)
         for (int c = 0; c < CPT; c++) {
             if (valid >> c & 1u) {
                 float o[V], dc[V], gc[V], wc[V];
-                d_of(c, dc);
+                d_of(c, mn, dc);
                 E::widen(cg[c * NT], gc);
                 w_of(c, wc);
                 // dx = r·((g − mean g) − x̂·mean(g·x̂)), g = dy·w, two columns
@@ -1273,7 +1334,6 @@ __global__ void __launch_bounds__(NT, 768 / NT)
                 st_stream(dxrow + (int64_t)c * NT * V, E::narrow(o));
             }
         }
-        if constexpr (LN) mn = mean_of(sums[LN ? 3 : 0], fd, inv_d);  // the next row's
         if (row + 1 == cw.end) {  // the tile's last row: its partial row(s)
             float* pw = part + cw.tile * D;
             float* pb = part + (P + cw.tile) * D;
@@ -1474,6 +1534,7 @@ static cudaError_t norm_fwd_cluster_go(const T* x, int64_t ldx, const float* w, 
     constexpr auto k = norm_fwd_cluster<T, LN, NT, S>;
     const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
     const size_t smem = (size_t)S * CPT * NT * 16;
+    if (cs > (unsigned)kNormMaxCS<NT>) return cudaErrorNotSupported;
     int fit = 0;
     const cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
     if (e != cudaSuccess) return e;
@@ -1492,6 +1553,7 @@ static cudaError_t norm_bwd_cluster_go(const T* x, int64_t ldx, const float* w, 
     const unsigned cs = (unsigned)cdiv(Dv, (int64_t)NT * CPT);
     // staged x and dy, then (WS) this thread's w slots
     const size_t smem = (size_t)2 * S * CPT * NT * 16 + (WS ? (size_t)CPT * V * NT * 4 : 0);
+    if (cs > (unsigned)kNormMaxCS<NT>) return cudaErrorNotSupported;
     int fit = 0;
     const cudaError_t e = cluster_fit<k>(cs, NT, smem, fit);
     if (e != cudaSuccess) return e;

@@ -216,11 +216,35 @@ def test_norm_cluster_block_means(wsf, dt, D):
     # blocks of 512 columns (one warp's share of a 16-bit row) with means far
     # apart, a common offset and a ragged last CTA: the per-warp shifts of
     # LayerNorm's exchange differ widely from the row mean
-    x, w, dy, b = _inputs(24, D, dt, seed=D % 89)
+    # enough rows that every cluster takes several, each shifted by the mean
+    # of the one before
+    x, w, dy, b = _inputs(480, D, dt, seed=D % 89)
     cols = torch.arange(D)
     x = (x.double() + 20.0 * ((cols // 512) % 7 - 3).double() + 40.0).to(x.dtype)
     x[5] = x[5, 0]  # a constant row
     _check(True, x, w, dy, b, *_run(wsf, True, x, w, dy, b))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_norm_cluster_nonfinite_row_keeps_others(wsf, dt):
+    # a row holding NaN or ∞ leaves the rows after it (same cluster, later
+    # rows; every cluster takes several) exact: y and dx of every other row
+    # match the oracle
+    N, D = 400, 20000
+    x, w, dy, b = _inputs(N, D, dt, seed=11, mean=3.0)
+    bad = [4, 9]
+    x[4, 100] = float("nan")
+    x[9, 5] = float("inf")
+    y, dx, _, _ = _run(wsf, True, x, w, dy, b)
+    keep = [i for i in range(N) if i not in bad]
+    xs, gs = x[keep], dy[keep]
+    f = oracle.norm_fwd(xs, w, b, EPS, True)
+    res = check_elementwise(y[keep], f["y"], f["y_exact"], scale=f["y_scale"])
+    assert res, ("y", res)
+    r = oracle.norm_bwd(xs, w, gs, EPS, True)
+    res = check_elementwise(dx[keep], r["dx"], r["dx_exact"], scale=r["dx_scale"])
+    assert res, ("dx", res)
+    assert not torch.isfinite(y[4]).all() and not torch.isfinite(dx[9]).all()
 
 
 @pytest.mark.parametrize("layer", [False, True], ids=["rms", "ln"])
