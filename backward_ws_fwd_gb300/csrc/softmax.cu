@@ -86,6 +86,19 @@ __device__ __forceinline__ uint64_t exp_diff_f32x2(uint64_t a2, uint64_t nb2) {
     return f2_fma(r, f2_mul(tl, f2_pack(kLn2f, kLn2f)), r);
 }
 
+// exp(a − b) for the terms of the first pass's sum only (two lanes; a ≤ b,
+// b finite): the rounded difference scaled by log2(e) in one rounding, then
+// ex2.approx.  Each term is off by at most about (|a − b| + 3)·2^-24 of
+// itself, with the sign of its own roundings; the sum is dominated by the
+// terms nearest the maximum, where the error is smallest, and the outputs
+// take their exponentials from exp_diff_f32x2.
+__device__ __forceinline__ uint64_t exp_sum_f32x2(uint64_t a2, uint64_t nb2) {
+    const uint64_t t = f2_mul(f2_add(a2, nb2), f2_pack(kLog2eHi, kLog2eHi));
+    float t0, t1;
+    f2_unpack(t, t0, t1);
+    return f2_pack(ex2_keep_subnormal(t0), ex2_keep_subnormal(t1));
+}
+
 // exp(a − b).  Binary32 storage: exp_diff_f32 above.  16-bit storage: the
 // hardware exponential of the rounded difference (its error is far below a
 // 16-bit unit).
@@ -1000,22 +1013,29 @@ __global__ void __launch_bounds__(kTwoPassNT, std::is_same<T, float>::value ? 4 
                 }
                 m = mb;
                 const uint64_t nm2 = f2_pack(-m, -m);
+                // the batch's exponentials, two lanes a value, added as a
+                // pairwise tree (within 3·2^-24 of the batch's sum, every term
+                // being positive), then into each lane's running sum by TwoSum
+                constexpr int NP = UU * V / 2;
+                static_assert((NP & (NP - 1)) == 0, "a power of two");
+                uint64_t e[NP];
 #pragma unroll
                 for (int u = 0; u < UU; u++) {
                     float f[V];
                     chunk(u, f);
 #pragma unroll
-                    for (int q = 0; q < V / 2; q++) {
-                        const uint64_t e = exp_diff_f32x2(f2_pack(f[2 * q], f[2 * q + 1]), nm2);
-                        // TwoSum of each lane's running sum and e
-                        const uint64_t t = f2_add(s2.hi, e);
-                        const uint64_t bp = f2_sub(t, s2.hi);
-                        const uint64_t err =
-                            f2_add(f2_sub(s2.hi, f2_sub(t, bp)), f2_sub(e, bp));
-                        s2.hi = t;
-                        s2.lo = f2_add(s2.lo, err);
-                    }
+                    for (int q = 0; q < V / 2; q++)
+                        e[u * (V / 2) + q] = exp_sum_f32x2(f2_pack(f[2 * q], f[2 * q + 1]), nm2);
                 }
+#pragma unroll
+                for (int w = NP / 2; w >= 1; w /= 2)
+#pragma unroll
+                    for (int i = 0; i < w; i++) e[i] = f2_add(e[i], e[i + w]);
+                const uint64_t t = f2_add(s2.hi, e[0]);
+                const uint64_t bp = f2_sub(t, s2.hi);
+                const uint64_t err = f2_add(f2_sub(s2.hi, f2_sub(t, bp)), f2_sub(e[0], bp));
+                s2.hi = t;
+                s2.lo = f2_add(s2.lo, err);
             } else {
                 if (mb > m && s.hi != 0.f) s.hi *= rescale<kComp>(m, mb);
                 m = mb;

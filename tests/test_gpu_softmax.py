@@ -243,6 +243,27 @@ def test_softmax_two_pass_extremes(wsf):
     assert bool((y[3, 1000:] == 0).all()) and bool((y[4, :150000] == 0).all())
 
 
+@pytest.mark.parametrize("k", [2, 5, 11, 50])
+def test_softmax_two_pass_few_terms(wsf, k):
+    """Two-pass binary32 rows whose sum is made of a few terms spread over
+    [−4, 0] (the rest masked, or far below): the first pass's sum comes
+    from a shorter exponential than the outputs', and with few terms its
+    per-term errors do not average out.  Every y within 1e-6 of the exact
+    value."""
+    N, D = 6, 200000
+    g = torch.Generator().manual_seed(k)
+    x = torch.full((N, D), float("-inf"))
+    x[3:] = -100.0 * torch.rand(N - 3, D, generator=g)
+    for r in range(N):
+        idx = torch.randperm(D, generator=g)[:k]
+        x[r, idx] = -4.0 * torch.rand(k, generator=g)
+        x[r, idx[0]] = 0.0
+    dy = torch.randn(N, D, generator=g)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+
+
 @pytest.mark.parametrize("N,D,mis", [(64, 64, 0), (16, 1001, 0), (8, 40000, 0), (4, 300000, 0),
                                      (4, 300007, 1)])
 def test_softmax_f32_exponential_range(wsf, N, D, mis):
