@@ -882,14 +882,15 @@ __global__ void __launch_bounds__(NT)
 // (windowed edges, the tail of the last slice) enter as −inf (forward) or 0
 // (backward).
 constexpr int kTwoPassNT = 256, kTwoPassU = 4;
-// CTAs a cluster (a row's slices).  Measured at s4 (fp32 [2048, 262144]) and
-// bf16 [1024, 524288], forward GB/s: binary32 rows 3136 / 3972 / 4194 with
-// clusters of 16 / 8 / 4 (4 CTAs an SM), 16-bit rows 5046 / 5490 / 4785;
-// more resident clusters keep more loads in flight, fewer CTAs a cluster
-// make each exchange cheaper.  The backward (s4): 4745 / 5278 / 4309 with
-// clusters of 16 / 8 (two CTAs an SM) / 4 (three).
+// CTAs a cluster (a row's slices).  Measured at bf16 [1024, 524288], forward
+// GB/s: 5046 / 5490 / 4785 with clusters of 16 / 8 / 4; more resident
+// clusters keep more loads in flight, fewer CTAs a cluster make each exchange
+// cheaper, and the rows in flight must stay in L2 for the second pass.  The
+// backward (s4, fp32 [2048, 262144]): 4745 / 5278 / 4309 with clusters of
+// 16 / 8 (two CTAs an SM) / 4 (three).  The binary32 forward chooses its
+// cluster size at launch (two_pass_cs).
 template <typename T, bool Fwd>
-constexpr int kTwoPassCS = (Fwd && std::is_same<T, float>::value) ? 4 : 8;
+constexpr int kTwoPassCS = 8;
 
 // The raw chunks c0 + b + u·NT (u < NU) of a row: the row's own 16-byte
 // blocks, zeros for chunks past the slice or the row.
@@ -1395,12 +1396,33 @@ static cudaError_t softmax_bwd_cluster_t(const T* y, int64_t ldy, const T* dy, i
 }
 
 // Two-pass cluster launches (rows over kClusterRowChunks chunks, D < 2^30).
+// The binary32 forward's second pass reads its slice again from L2, so the
+// rows in flight (one a resident cluster) should fit in it: the smallest
+// cluster of 4, 8 or 16 CTAs whose resident rows hold at most this many
+// bytes, else 16.  Measured (GB/s, fp32 rows of 140,000 / 262,144 /
+// 1,048,576 columns; clusters of 4, 8, 16): 5120 / 4462 / 3431,
+// 4682 / 5190 / 4271, 4440 / 4604 / 4651.
+constexpr int64_t kTwoPassL2Rows = (int64_t)96 << 20;
+
+template <auto kernel>
+static unsigned two_pass_cs(int64_t N, int64_t row_bytes) {
+    for (unsigned cs : {4u, 8u}) {
+        int fit = 0;
+        if (cluster_fit<kernel>(cs, kTwoPassNT, 0, fit) == cudaSuccess &&
+            std::min<int64_t>(N, fit) * row_bytes <= kTwoPassL2Rows)
+            return cs;
+    }
+    return 16u;
+}
+
 template <typename T, bool U>
 static cudaError_t softmax_fwd_cluster2_t(const T* x, int64_t ldx, T* y, int64_t ldy, int64_t N,
                                           int64_t D, int64_t Dc, cudaStream_t s) {
-    const int SL = (int)cdiv(Dc, kTwoPassCS<T, true>);
-    return go_cluster<softmax_fwd_cluster2<T, U>>(kTwoPassNT, kTwoPassCS<T, true>, 0, N, s, x, ldx,
-                                                  y, ldy, N, (int)D, SL);
+    constexpr auto k = softmax_fwd_cluster2<T, U>;
+    const unsigned cs = std::is_same<T, float>::value ? two_pass_cs<k>(N, D * (int64_t)sizeof(T))
+                                                      : (unsigned)kTwoPassCS<T, true>;
+    const int SL = (int)cdiv(Dc, cs);
+    return go_cluster<k>(kTwoPassNT, cs, 0, N, s, x, ldx, y, ldy, N, (int)D, SL);
 }
 
 template <typename T, bool U>

@@ -227,6 +227,16 @@ def test_softmax_two_pass_rows(wsf, dt, N, D, pad, mis):
     _check(x, dy, y, dx, yin)
 
 
+@pytest.mark.parametrize("N,D", [(160, 262144), (40, 1048576)])
+def test_softmax_two_pass_f32_cluster_sizes(wsf, N, D):
+    # binary32 rows take clusters of 8 (160 rows of 1 MB: too many rows in
+    # flight for L2 with clusters of 4) and of 16 (rows of 4 MB)
+    x, dy = _inputs(N, D, "f32", seed=N)
+    _, yin = oracle.softmax_fwd(x)
+    y, dx = _run(wsf, x, dy, yin)
+    _check(x, dy, y, dx, yin)
+
+
 def test_softmax_two_pass_extremes(wsf):
     # the row maximum in the first and in the last slice, a growing maximum
     # within one thread's chunks, masked spans covering whole slices
