@@ -589,6 +589,7 @@ __global__ void __launch_bounds__(NT)
 // a cluster runs the same number of rows (it depends only on the cluster's
 // index), hence the same exchanges.
 constexpr int kClusterCPT = 4;
+constexpr int kClusterCPT5 = 5;  // the forward's wider CTAs (see softmax_fwd_cluster_t)
 
 // Waits of the cluster exchanges that ran out (see WarpPush); zero unless
 // the exchange protocol failed.
@@ -611,12 +612,12 @@ __device__ __forceinline__ float rescale(float a, float b) {
     else return exp2_approx(fmaf(a, kLog2e, -b * kLog2e));
 }
 
-template <typename T, int NT, int S, bool U>
-__global__ void __launch_bounds__(NT, 1024 / NT)
+template <typename T, int NT, int S, bool U, int CPT>
+__global__ void __launch_bounds__(NT, (CPT > kClusterCPT ? 768 : 1024) / NT)
     softmax_fwd_cluster(const T* __restrict__ x, int64_t ldx, T* __restrict__ y, int64_t ldy,
                         int64_t N, int D) {
     using E = Elt<T>;
-    constexpr int V = E::V, CPT = kClusterCPT, W = NT / 32;
+    constexpr int V = E::V, W = NT / 32;
     constexpr bool kComp = std::is_same<T, float>::value;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Raw16* slots = reinterpret_cast<Raw16*>(smem_raw);  // [S][CPT][NT]
@@ -1370,11 +1371,23 @@ static cudaError_t softmax_fwd_cluster_t(const T* x, int64_t ldx, T* y, int64_t 
     cluster_shape(Dc, nt, cs);
     if (nt == 256) {
         constexpr int S = 3;
-        return go_cluster<softmax_fwd_cluster<T, 256, S, U>>(
+        // five chunks a thread (three CTAs an SM) where they fill the row's
+        // CTAs better by more than 3%: a last CTA with only a few chunks
+        // costs a whole CTA's exchange and residency.  Measured (bf16, GB/s,
+        // four / five chunks): rows of 50,257 (windowed) 4648 / 5222, of
+        // 50,264 5090 / 5718 (7 CTAs, the last with 139 chunks, / 5), of
+        // 20,480 5600 / 6040; of 49,152 (6 full CTAs / 5 at 96%) 6292 / 6015.
+        const unsigned cs5 = (unsigned)cdiv(Dc, (int64_t)256 * kClusterCPT5);
+        const double fill4 = (double)Dc / ((double)cs * 256 * kClusterCPT),
+                     fill5 = (double)Dc / ((double)cs5 * 256 * kClusterCPT5);
+        if (fill5 > fill4 + 0.03)
+            return go_cluster<softmax_fwd_cluster<T, 256, S, U, kClusterCPT5>>(
+                256, cs5, (size_t)S * kClusterCPT5 * 256 * 16, N, s, x, ldx, y, ldy, N, (int)D);
+        return go_cluster<softmax_fwd_cluster<T, 256, S, U, kClusterCPT>>(
             256, cs, (size_t)S * kClusterCPT * 256 * 16, N, s, x, ldx, y, ldy, N, (int)D);
     }
     constexpr int S = 2;
-    return go_cluster<softmax_fwd_cluster<T, 512, S, U>>(
+    return go_cluster<softmax_fwd_cluster<T, 512, S, U, kClusterCPT>>(
         512, cs, (size_t)S * kClusterCPT * 512 * 16, N, s, x, ldx, y, ldy, N, (int)D);
 }
 
