@@ -26,8 +26,10 @@
 // rounding (up to ulp(μ)/2) would shift every x̂ of a row with a large common
 // offset by the same amount, an error that does not cancel in Σ dy·x̂; and c
 // cannot be taken from Σ(x − μ₀) either, since the rounding of x − μ₀ has
-// one sign across a binade.  Σx is therefore carried as an exact pair for
-// every storage type (row_sum_x); for binary32 the other row sums are
+// one sign across a binade.  Σx must therefore be exact (center_row): for
+// binary32 rows a compensated pair; for 16-bit rows the plain binary32 sum,
+// which for at most 8192 elements of 8 or 11 significant bits stays exact
+// unless the row spans many binades; for binary32 the other row sums are
 // compensated too (Dot2), so that y and dx stay within 1e-6.  In the
 // backward each thread sums dy·x̂ (and dy) for its own columns over the rows
 // of its CTA's row tile; the CTA's row groups are combined in index order into

@@ -910,18 +910,28 @@ OP_SOURCES = {"silu": "silu.cu", "ws": "ws.cu", "rmsnorm": "norm.cu", "layernorm
 SHARED_SOURCES = ("abi.cu", "wsf_device.cuh", "wsf_internal.h")
 
 
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and its whitespace
+    collapsed (string and character literals kept as written)."""
+    import re
+    token = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|/\*.*?\*/|//[^\n]*',
+                       re.S)
+    src = token.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    return " ".join(src.split())
+
+
 def source_hash(op: str | None = None) -> str:
-    """Hash of the kernel sources an operator is built from (all of them for
-    op=None): a DRAM-traffic capture stays valid while its operator's hash
-    is unchanged."""
+    """Hash of the code of the kernel sources an operator is built from (all
+    of them for op=None; comments and layout aside): a DRAM-traffic capture
+    stays valid while its operator's hash is unchanged."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "backward_ws_fwd_gb300", "csrc")
     files = sorted(os.listdir(d)) if op is None else sorted((OP_SOURCES[op],) + SHARED_SOURCES)
     for f in files:
-        with open(os.path.join(d, f), "rb") as fh:
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

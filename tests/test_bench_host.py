@@ -97,12 +97,22 @@ def test_traffic_records_keyed_by_operator_sources(tmp_path, monkeypatch):
         (fake / name).write_bytes(open(os.path.join(src, name), "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     before = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
-    (fake / "norm.cu").write_bytes((fake / "norm.cu").read_bytes() + b"\n// edit\n")
+    # comments and layout are not code: the records stay valid
+    (fake / "norm.cu").write_bytes(b"// a comment\n/* and a block */\n" +
+                                   (fake / "norm.cu").read_bytes() + b"\n\n   \n")
+    assert {op: bench.source_hash(op) for op in bench.OP_SOURCES} == before
+    (fake / "norm.cu").write_bytes((fake / "norm.cu").read_bytes() + b"\nstatic int edit;\n")
     after = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
     assert {op for op in before if before[op] != after[op]} == {"rmsnorm", "layernorm"}
-    (fake / "wsf_device.cuh").write_bytes((fake / "wsf_device.cuh").read_bytes() + b"\n")
+    (fake / "wsf_device.cuh").write_bytes((fake / "wsf_device.cuh").read_bytes() +
+                                          b"\nstatic int edit2;\n")
     final = {op: bench.source_hash(op) for op in bench.OP_SOURCES}
     assert all(final[op] != after[op] for op in bench.OP_SOURCES)
+    # a "//" inside a string literal is code
+    (fake / "ws.cu").write_bytes((fake / "ws.cu").read_bytes() + b'\nconst char* u = "a//b";\n')
+    h1 = bench.source_hash("ws")
+    (fake / "ws.cu").write_bytes((fake / "ws.cu").read_bytes().replace(b'"a//b"', b'"a//c"'))
+    assert bench.source_hash("ws") != h1
 
 
 def test_reference_arm_line_contract():
