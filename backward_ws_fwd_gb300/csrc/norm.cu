@@ -601,9 +601,10 @@ __global__ void __launch_bounds__(NT, MINB)
 // split over a thread-block cluster of CS CTAs of NT = 256 threads: the CTA
 // of rank r owns the chunks [r·NT·CPT, (r+1)·NT·CPT) (16 elements a thread,
 // 4096 a CTA) and stages them S rows ahead into the threads' private slots.
-// The forward holds its slice of w (and b) in registers; the backward reads
-// it through the read-only cache, re-widens x and dy from their slots in each
-// pass, and holds only the dw/db accumulators of exactly those columns.  The row sums are reduced inside each warp (xor butterfly)
+// The forward holds its slice of w (and b) in registers; the backward keeps
+// w in per-thread shared-memory slots, re-widens x and dy from their slots in
+// each pass, and holds only the dw/db accumulators of exactly those columns.
+// The row sums are reduced inside each warp (xor butterfly)
 // and exchanged as one entry a warp with WarpPush: every CTA receives the
 // entries of all CS·NT/32 warps of the cluster in its own shared memory;
 // warp 0 combines them (lane ℓ takes entries ℓ, ℓ+32, …, then an xor
@@ -616,8 +617,12 @@ __global__ void __launch_bounds__(NT, MINB)
 // the exchange of row k is awaited, so the exchange's latency overlaps the
 // next row's first pass (two turns outstanding: four exchange buffers).
 //
-// One exchange a row.  LayerNorm's sums about the mean would need the mean
-// first; it takes them about a shift s instead, the previous row's mean
+// One exchange a row.  LayerNorm's sums about the mean need the mean first.
+// The forward carries it one row ahead: the exchange of row k carries Σ d²
+// of row k and Σx of row k + 1 (staged already), so that the mean of row
+// k + 1 is known when its turn comes; only the first row's Σx is exchanged on
+// its own.  The backward takes its sums about a shift s instead, the previous
+// row's mean
 // (zero for a cluster's first row, or after a row whose mean is not
 // finite): d = x − s, and the row's turn carries Σ d², Σ x[, Σ g, Σ g·d].
 // The mean μ₀ + c comes from Σ x as on the row path (Σ x compensated across
