@@ -88,10 +88,11 @@ __device__ __forceinline__ uint64_t exp_diff_f32x2(uint64_t a2, uint64_t nb2) {
 
 // exp(a − b) for the terms of the first pass's sum only (two lanes; a ≤ b,
 // b finite): the rounded difference scaled by log2(e) in one rounding, then
-// ex2.approx.  Each term is off by at most about (|a − b| + 3)·2^-24 of
-// itself, with the sign of its own roundings; the sum is dominated by the
-// terms nearest the maximum, where the error is smallest, and the outputs
-// take their exponentials from exp_diff_f32x2.
+// ex2.approx.  The two roundings put a term off by up to about
+// 2·|a − b|·2^-24 of itself, ex2.approx adds its own few units; the signs
+// follow each term's own roundings.  The sum is dominated by the terms
+// nearest the maximum, where the error is smallest, and the outputs take
+// their exponentials from exp_diff_f32x2.
 __device__ __forceinline__ uint64_t exp_sum_f32x2(uint64_t a2, uint64_t nb2) {
     const uint64_t t = f2_mul(f2_add(a2, nb2), f2_pack(kLog2eHi, kLog2eHi));
     float t0, t1;
